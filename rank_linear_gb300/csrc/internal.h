@@ -1,0 +1,78 @@
+// internal.h -- host-side interfaces shared by the library's translation
+// units.  Not part of the public ABI (that is include/lora_linear.h).
+#pragma once
+
+#include <cuda.h>
+#include <cuda_runtime.h>
+#include <cstdint>
+
+namespace lora {
+
+// ---- K-extended tensor-core GEMM (bf16 in, fp32 accumulate, bf16 out) ----
+//   out[m, n] = sum_{k < K1} A(m, k) B(n, k)  +  sum_{k < k_ext} A2(m, k) B2(n, k)
+// A / A2 are K-major [M, K] tensor maps (box 64 x 128).  B / B2 are K-major
+// [N, K] maps (box 64 x 256) or, with b_mn, MN-major [K, N] maps (box 64 x 64).
+struct MainGemmArgs {
+  CUtensorMap tmA, tmB, tmA2, tmB2;
+  int M = 0, N = 0;
+  int kb_main = 0;  // number of 64-wide K blocks of the first segment
+  int k_ext = 0;    // K of the extension: a multiple of 16 in [0, 256]
+  void *out = nullptr;
+  int64_t ldo = 0;  // row pitch of out, elements
+  bool b_mn = false;
+  unsigned *dev_status = nullptr;
+};
+constexpr int kMainBM = 128, kMainBN = 256, kMainBK = 64, kMainStages = 4;
+size_t main_gemm_smem_bytes();
+cudaError_t launch_main_gemm(const MainGemmArgs &a, int num_sms, cudaStream_t s);
+
+// ---- skinny tensor-core pass with cluster split-K -------------------------
+//   acc[row, j] = sum_k A(row, k) B(j, k),  row < rows, j < RP (RP = N of the MMA)
+//   out0[row * ld0 + j] = bf16(scale * acc)  for j < n0   (row-major, optional)
+//   out1[j * ld1 + row] = bf16(scale * acc)  for j < n1   (transposed, optional)
+// A is K-major [rows, K] (box 64 x 128) or, with a_mn, MN-major [K, rows]
+// (box 64 x 64); B is K-major [RP, K] (box 64 x RP).  The K range is split
+// over the CTAs of a cluster whose partial sums meet in distributed shared
+// memory and are added in cluster-rank order.
+struct SkinnyArgs {
+  CUtensorMap tmA, tmB;
+  bool a_mn = false;
+  int rows = 0, RP = 16, K = 0;
+  float scale = 1.f;
+  void *out0 = nullptr;
+  int64_t ld0 = 0;
+  int n0 = 0;
+  void *out1 = nullptr;
+  int64_t ld1 = 0;
+  int n1 = 0;
+  unsigned *dev_status = nullptr;
+};
+cudaError_t launch_skinny(const SkinnyArgs &a, int num_sms, cudaStream_t s);
+int skinny_split(int rows, int K, int num_sms);
+
+// ---- fp32 CUDA-core GEMM (debug dtype) ------------------------------------
+//   c[m * c0 + n * c1] = alpha * (sum_{k<K1} a1(m,k) b1(k,n) + sum_{k<K2} a2(m,k) b2(k,n))
+// with x(i, k) = p[i * s0 + k * s1] for an A operand and
+//      x(k, n) = p[k * s0 + n * s1] for a B operand.
+struct F32Operand {
+  const float *p = nullptr;
+  int64_t s0 = 0, s1 = 0;
+};
+struct F32GemmArgs {
+  int M = 0, N = 0, K1 = 0, K2 = 0;
+  F32Operand a1, b1, a2, b2;
+  float alpha = 1.f;
+  float *c = nullptr;
+  int64_t c0 = 0, c1 = 0;
+};
+cudaError_t launch_f32_gemm(const F32GemmArgs &a, cudaStream_t s);
+
+// ---- small bf16 copies of the adapter B ----------------------------------
+// Bt[j * d_out + o] = (j < r) ? B[o * r + j] : 0     for j < r_pad
+cudaError_t launch_transpose_pad_bf16(const void *B, int d_out, int r, int r_pad, void *Bt,
+                                      cudaStream_t s);
+// Bp[o * r_pad + j] = (j < r) ? B[o * r + j] : 0     for j < r_pad
+cudaError_t launch_pad_cols_bf16(const void *B, int d_out, int r, int r_pad, void *Bp,
+                                 cudaStream_t s);
+
+}  // namespace lora

@@ -1,0 +1,310 @@
+// tc_skinny.cu -- the skinny (N = r) tensor-core passes of the layer.
+//
+// Four products of ch05 "Acceleration principles: Triton kernels and fused
+// LoRA", §5.3 have one side of width r and are bound by the HBM read of the
+// wide operand:
+//     forward   sH  = s X A^T           rows = tokens, K = d_in   (A K-major)
+//     backward  sG  = s dY B            rows = tokens, K = d_out  (A K-major)
+//               dA^T = X^T sG           rows = d_in,   K = tokens (A MN-major)
+//               dB   = dY^T sH          rows = d_out,  K = tokens (A MN-major)
+// (the last two are the dL/dA and dL/dB of the fused backward's gradient
+// list; s is folded into sH and sG, so dA = s G^T X and dB = s dY^T H).
+//
+// One CTA owns 128 output rows and one slice of K.  The S CTAs that share
+// the rows form a thread-block cluster: each accumulates its slice with
+// tcgen05.mma (M = 128, N = RP) into TMEM, stages the fp32 partial in its
+// shared memory, and after a cluster barrier CTA c adds rows
+// [c*128/S, (c+1)*128/S) of all S partials in rank order through
+// distributed shared memory.  The order is fixed, so results are bitwise
+// reproducible and no partials touch HBM.
+#include <cuda_bf16.h>
+
+#include "internal.h"
+#include "ptx.cuh"
+
+namespace lora {
+namespace {
+
+constexpr int BM = 128, BK = 64;
+constexpr int MAX_STAGES = 8;
+constexpr int NUM_THREADS = 192;
+constexpr uint32_t A_BYTES = BM * BK * 2;   // 16 KB
+constexpr size_t kSmemBudget = 100 * 1024;  // two CTAs per SM when RP <= 128
+
+struct __align__(8) SkinnyTail {
+  uint64_t full[MAX_STAGES];
+  uint64_t empty[MAX_STAGES];
+  uint64_t tfull;
+  uint64_t drain;
+  uint32_t tmem_base;
+  int abort_flag;
+};
+
+struct SkinnyLayout {
+  int stages;
+  uint32_t b_bytes, pipe_bytes, red_bytes, region_bytes;
+  size_t smem_bytes;
+  uint32_t tmem_cols;
+};
+
+__host__ __device__ inline SkinnyLayout skinny_layout(int RP) {
+  SkinnyLayout L;
+  L.b_bytes = static_cast<uint32_t>(RP) * BK * 2;
+  const uint32_t stage_bytes = A_BYTES + L.b_bytes;
+  int st = static_cast<int>(kSmemBudget / stage_bytes);
+  st = st < 2 ? 2 : (st > MAX_STAGES ? MAX_STAGES : st);
+  L.stages = st;
+  L.pipe_bytes = st * stage_bytes;
+  L.red_bytes = BM * (RP + 4) * 4;  // fp32 partial, row pitch RP + 4 floats
+  L.region_bytes = L.pipe_bytes > L.red_bytes ? L.pipe_bytes : L.red_bytes;
+  L.smem_bytes = 1024 + L.region_bytes + sizeof(SkinnyTail);
+  uint32_t c = 32;
+  while (c < static_cast<uint32_t>(RP)) c <<= 1;
+  L.tmem_cols = c;
+  return L;
+}
+
+template <bool A_MN>
+__global__ void __launch_bounds__(NUM_THREADS, 1)
+    k_skinny(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
+             int rows, int RP, int num_kb, int kb_per, int S, float scale,
+             __nv_bfloat16 *__restrict__ out0, int64_t ld0, int n0,
+             __nv_bfloat16 *__restrict__ out1, int64_t ld1, int n1, unsigned *dev_status) {
+  extern __shared__ uint8_t smem_raw[];
+  const SkinnyLayout L = skinny_layout(RP);
+  const uint32_t raw = smem_u32(smem_raw);
+  const uint32_t base = (raw + 1023u) & ~1023u;
+  uint8_t *base_ptr = smem_raw + (base - raw);
+  SkinnyTail *tail = reinterpret_cast<SkinnyTail *>(base_ptr + L.region_bytes);
+  float *red = reinterpret_cast<float *>(base_ptr);  // reuses the pipeline buffers
+  const uint32_t sA = base;
+  const uint32_t sB = base + L.stages * A_BYTES;
+  const int STAGES = L.stages;
+  const int pitch = RP + 4;
+
+  const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
+  const int rank = static_cast<int>(cluster_ctarank());
+  const int m0 = (blockIdx.x / S) * BM;
+  const int kb_begin = rank * kb_per;
+  const int kb_end = min(num_kb, kb_begin + kb_per);
+  const bool has_k = kb_end > kb_begin;
+  volatile int *abort_flag = &tail->abort_flag;
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < STAGES; ++s) {
+      mbar_init(smem_u32(&tail->full[s]), 1);
+      mbar_init(smem_u32(&tail->empty[s]), 1);
+    }
+    mbar_init(smem_u32(&tail->tfull), 1);
+    mbar_init(smem_u32(&tail->drain), 1);
+    tail->abort_flag = 0;
+    fence_barrier_init();
+    tma_prefetch(&tmA);
+    tma_prefetch(&tmB);
+  }
+  if (warp == 1) {
+    tmem_alloc(smem_u32(&tail->tmem_base), L.tmem_cols);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem_base = tail->tmem_base;
+
+  if (warp == 0) {
+    // ------------------------------------------------------ TMA producer
+    if (lane == 0) {
+      uint32_t issued[MAX_STAGES];
+      for (int s = 0; s < MAX_STAGES; ++s) issued[s] = 0;
+      int stage = 0;
+      uint32_t phase = 0;
+      bool ok = true;
+      const uint32_t tx = A_BYTES + L.b_bytes;
+      for (int kb = kb_begin; kb < kb_end; ++kb) {
+        if (!mbar_wait(smem_u32(&tail->empty[stage]), phase ^ 1u, abort_flag, dev_status)) {
+          ok = false;
+          break;
+        }
+        const uint32_t full = smem_u32(&tail->full[stage]);
+        mbar_expect_tx(full, tx);
+        const int k0 = kb * BK;
+        if (A_MN) {  // A^T stored [K][rows]: two 64-wide boxes of rows
+          tma_load_2d(sA + stage * A_BYTES, &tmA, full, m0, k0);
+          tma_load_2d(sA + stage * A_BYTES + 8192u, &tmA, full, m0 + 64, k0);
+        } else {
+          tma_load_2d(sA + stage * A_BYTES, &tmA, full, k0, m0);
+        }
+        tma_load_2d(sB + stage * L.b_bytes, &tmB, full, k0, 0);
+        issued[stage] += 1;
+        if (++stage == STAGES) {
+          stage = 0;
+          phase ^= 1u;
+        }
+      }
+      if (!ok) {
+        for (int s = 0; s < STAGES; ++s)
+          if (issued[s]) mbar_wait_drain(smem_u32(&tail->full[s]), (issued[s] - 1u) & 1u);
+      }
+    }
+  } else if (warp == 1) {
+    // ------------------------------------------------------ MMA issuer
+    if (lane == 0) {
+      const uint32_t idesc = idesc_bf16(BM, static_cast<uint32_t>(RP), A_MN, false);
+      int stage = 0;
+      uint32_t phase = 0;
+      bool ok = true;
+      for (int kb = kb_begin; kb < kb_end; ++kb) {
+        if (!mbar_wait(smem_u32(&tail->full[stage]), phase, abort_flag, dev_status)) {
+          ok = false;
+          break;
+        }
+        tc_fence_after();
+        const uint32_t a0 = sA + stage * A_BYTES, b0 = sB + stage * L.b_bytes;
+#pragma unroll
+        for (int kk = 0; kk < BK / 16; ++kk) {
+          const uint64_t ad = A_MN ? sdesc_sw128(a0 + kk * 2048, 8192, 1024)
+                                   : sdesc_sw128(a0 + kk * 32, 16, 1024);
+          const uint64_t bd = sdesc_sw128(b0 + kk * 32, 16, 1024);
+          tc_mma_bf16(tmem_base, ad, bd, idesc, (kb > kb_begin || kk > 0) ? 1u : 0u);
+        }
+        tc_commit(smem_u32(&tail->empty[stage]));
+        if (++stage == STAGES) {
+          stage = 0;
+          phase ^= 1u;
+        }
+      }
+      if (ok) {
+        tc_commit(smem_u32(&tail->tfull));
+      } else {
+        tc_commit(smem_u32(&tail->drain));
+        mbar_wait_drain(smem_u32(&tail->drain), 0);
+      }
+    }
+  } else {
+    // ------------------------------------------------------ TMEM -> smem partial
+    const int q = warp & 3;
+    const bool got = mbar_wait(smem_u32(&tail->tfull), 0, abort_flag, dev_status);
+    if (__all_sync(0xffffffffu, got)) {
+      tc_fence_after();
+      fence_proxy_async_smem();  // smem last read by the tensor cores is rewritten below
+      const int rl = q * 32 + lane;
+      float4 *dst = reinterpret_cast<float4 *>(red + rl * pitch);
+      const uint32_t taddr = tmem_base + (static_cast<uint32_t>(q * 32) << 16);
+      for (int c = 0; c < RP / 16; ++c) {
+        float v[16];
+        tmem_ld_16cols(taddr + c * 16, v);
+        if (!has_k) {
+#pragma unroll
+          for (int i = 0; i < 16; ++i) v[i] = 0.f;
+        }
+#pragma unroll
+        for (int i = 0; i < 4; ++i)
+          dst[c * 4 + i] = make_float4(v[4 * i], v[4 * i + 1], v[4 * i + 2], v[4 * i + 3]);
+      }
+    }
+  }
+
+  // ------------------------------------------------------ cluster reduction
+  __syncwarp();
+  cluster_sync();  // every CTA's partial is in its shared memory
+  const int R = BM / S;
+  const int r_lo = rank * R;
+  const int c4n = RP / 4;
+  const uint32_t red_addr = smem_u32(red);
+  const bool vec0 = (ld0 % 4 == 0) && (n0 % 4 == 0);
+  for (int e = threadIdx.x; e < R * c4n; e += NUM_THREADS) {
+    const int rl = r_lo + e / c4n;
+    const int c4 = e % c4n;
+    const uint32_t off = static_cast<uint32_t>((rl * pitch + c4 * 4) * 4);
+    float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+    for (int p = 0; p < S; ++p) {
+      const float4 v = dsmem_ld_f4(dsmem_map(red_addr + off, static_cast<uint32_t>(p)));
+      acc.x += v.x;
+      acc.y += v.y;
+      acc.z += v.z;
+      acc.w += v.w;
+    }
+    acc.x *= scale;
+    acc.y *= scale;
+    acc.z *= scale;
+    acc.w *= scale;
+    *reinterpret_cast<float4 *>(red + rl * pitch + c4 * 4) = acc;  // own slice only
+    const int row = m0 + rl;
+    if (out0 != nullptr && row < rows) {
+      const int c = c4 * 4;
+      __nv_bfloat16 *o = out0 + static_cast<int64_t>(row) * ld0 + c;
+      if (vec0 && c + 4 <= n0) {
+        __nv_bfloat162 lo = __floats2bfloat162_rn(acc.x, acc.y);
+        __nv_bfloat162 hi = __floats2bfloat162_rn(acc.z, acc.w);
+        uint2 pk;
+        pk.x = *reinterpret_cast<uint32_t *>(&lo);
+        pk.y = *reinterpret_cast<uint32_t *>(&hi);
+        *reinterpret_cast<uint2 *>(o) = pk;
+      } else {
+        const float vv[4] = {acc.x, acc.y, acc.z, acc.w};
+        for (int i = 0; i < 4; ++i)
+          if (c + i < n0) o[i] = __float2bfloat16_rn(vv[i]);
+      }
+    }
+  }
+  cluster_sync();  // peers are done reading this CTA's shared memory
+
+  if (out1 != nullptr) {  // transposed copy: consecutive threads, consecutive rows
+    for (int e = threadIdx.x; e < R * n1; e += NUM_THREADS) {
+      const int j = e / R;
+      const int rl = r_lo + e % R;
+      const int row = m0 + rl;
+      if (row < rows)
+        out1[static_cast<int64_t>(j) * ld1 + row] = __float2bfloat16_rn(red[rl * pitch + j]);
+    }
+  }
+
+  __syncthreads();
+  if (warp == 1) {
+    __syncwarp();
+    tc_fence_after();
+    tmem_dealloc(tmem_base, L.tmem_cols);
+  }
+}
+
+}  // namespace
+
+// Cluster size: enough CTAs to keep every SM streaming (about two per SM),
+// while each CTA keeps at least four K blocks.
+int skinny_split(int rows, int K, int num_sms) {
+  const int mt = (rows + BM - 1) / BM;
+  const int nkb = (K + BK - 1) / BK;
+  int S = 1;
+  while (S < 8 && mt * S < 2 * num_sms && nkb >= 8 * S) S *= 2;
+  return S;
+}
+
+cudaError_t launch_skinny(const SkinnyArgs &a, int num_sms, cudaStream_t s) {
+  if (a.rows <= 0) return cudaSuccess;
+  const SkinnyLayout L = skinny_layout(a.RP);
+  const int mt = (a.rows + BM - 1) / BM;
+  const int num_kb = (a.K + BK - 1) / BK;
+  const int S = skinny_split(a.rows, a.K, num_sms);
+  const int kb_per = (num_kb + S - 1) / S;
+  auto kern = a.a_mn ? k_skinny<true> : k_skinny<false>;
+  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                       static_cast<int>(L.smem_bytes));
+  if (e != cudaSuccess) return e;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(static_cast<unsigned>(mt * S), 1, 1);
+  cfg.blockDim = dim3(NUM_THREADS, 1, 1);
+  cfg.dynamicSmemBytes = L.smem_bytes;
+  cfg.stream = s;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = static_cast<unsigned>(S);
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, kern, a.tmA, a.tmB, a.rows, a.RP, num_kb, kb_per, S, a.scale,
+                            static_cast<__nv_bfloat16 *>(a.out0), a.ld0, a.n0,
+                            static_cast<__nv_bfloat16 *>(a.out1), a.ld1, a.n1, a.dev_status);
+}
+
+}  // namespace lora
