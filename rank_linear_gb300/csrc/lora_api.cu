@@ -1,0 +1,613 @@
+// lora_api.cu -- the C ABI of include/lora_linear.h: argument checks,
+// buffer planning, TMA tensor maps and the launch sequence of the forward
+// and backward passes.  No allocation, no synchronisation (except
+// lora_device_status, which reads the device status word).
+#include <cudaTypedefs.h>
+
+#include <atomic>
+#include <cmath>
+#include <cstdarg>
+#include <cstdio>
+#include <mutex>
+#include <string>
+
+#include "internal.h"
+#include "lora_linear.h"
+#include "ptx.cuh"
+
+namespace lora {
+namespace {
+
+__device__ unsigned g_dev_status = 0;
+
+thread_local std::string t_err;
+
+struct TimingHook {
+  void *const *events = nullptr;
+  int *kinds = nullptr;
+  int n = 0;
+  int used = 0;
+};
+thread_local TimingHook t_hook;
+std::atomic<uint64_t> g_launches{0};
+
+lora_status_t fail(lora_status_t st, const char *fmt, ...) {
+  char buf[512];
+  va_list ap;
+  va_start(ap, fmt);
+  vsnprintf(buf, sizeof(buf), fmt, ap);
+  va_end(ap);
+  t_err = buf;
+  return st;
+}
+
+// ---------------------------------------------------------------- device
+struct DevInfo {
+  bool init = false;
+  int sms = 0, major = 0, minor = 0;
+  unsigned *status = nullptr;
+};
+std::mutex g_mtx;
+constexpr int kMaxDevices = 64;
+DevInfo g_dev[kMaxDevices];
+
+lora_status_t device_info(DevInfo &out) {
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return fail(LORA_ERR_CUDA, "cudaGetDevice: %s", cudaGetErrorString(e));
+  if (dev < 0 || dev >= kMaxDevices) return fail(LORA_ERR_UNSUPPORTED, "device index %d", dev);
+  std::lock_guard<std::mutex> lock(g_mtx);
+  DevInfo &d = g_dev[dev];
+  if (!d.init) {
+    if ((e = cudaDeviceGetAttribute(&d.sms, cudaDevAttrMultiProcessorCount, dev)) != cudaSuccess ||
+        (e = cudaDeviceGetAttribute(&d.major, cudaDevAttrComputeCapabilityMajor, dev)) !=
+            cudaSuccess ||
+        (e = cudaDeviceGetAttribute(&d.minor, cudaDevAttrComputeCapabilityMinor, dev)) !=
+            cudaSuccess)
+      return fail(LORA_ERR_CUDA, "device attributes: %s", cudaGetErrorString(e));
+    void *p = nullptr;
+    if ((e = cudaGetSymbolAddress(&p, g_dev_status)) != cudaSuccess)
+      return fail(LORA_ERR_CUDA, "status word address: %s", cudaGetErrorString(e));
+    d.status = static_cast<unsigned *>(p);
+    d.init = true;
+  }
+  if (!(d.major == 10 && d.minor == 3))
+    return fail(LORA_ERR_UNSUPPORTED, "device %d is sm_%d%d; this library is built for sm_103a",
+                dev, d.major, d.minor);
+  out = d;
+  return LORA_OK;
+}
+
+// ---------------------------------------------------------------- TMA maps
+PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
+  static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    void *p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault,
+                                         &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
+  });
+  return fn;
+}
+
+// 2-D bf16 map over a row-major [outer][inner] tensor with the given row
+// pitch; boxes of box_inner x box_outer elements, 128-byte swizzle,
+// out-of-bounds elements read as zero.
+lora_status_t tmap(CUtensorMap *tm, const void *ptr, uint64_t inner, uint64_t outer,
+                   uint64_t pitch_bytes, uint32_t box_inner, uint32_t box_outer, const char *what) {
+  auto fn = encode_fn();
+  if (!fn) return fail(LORA_ERR_CUDA, "cuTensorMapEncodeTiled is not available from the driver");
+  cuuint64_t dims[2] = {inner, outer};
+  cuuint64_t strides[1] = {pitch_bytes};
+  cuuint32_t box[2] = {box_inner, box_outer};
+  cuuint32_t es[2] = {1, 1};
+  CUresult r = fn(tm, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void *>(ptr), dims, strides,
+                  box, es, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                  CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  if (r != CUDA_SUCCESS)
+    return fail(LORA_ERR_CUDA, "tensor map for %s (%llu x %llu, pitch %llu) failed: CUresult %d",
+                what, (unsigned long long)outer, (unsigned long long)inner,
+                (unsigned long long)pitch_bytes, static_cast<int>(r));
+  return LORA_OK;
+}
+
+// ---------------------------------------------------------------- launches
+template <class F>
+lora_status_t run(lora_kernel_kind_t kind, cudaStream_t s, const char *what, F &&launch) {
+  int j = -1;
+  if (t_hook.events != nullptr && t_hook.used < t_hook.n) {
+    j = t_hook.used++;
+    cudaEventRecord(static_cast<cudaEvent_t>(t_hook.events[2 * j]), s);
+    if (t_hook.kinds) t_hook.kinds[j] = static_cast<int>(kind);
+  }
+  const cudaError_t e = launch();
+  if (j >= 0) cudaEventRecord(static_cast<cudaEvent_t>(t_hook.events[2 * j + 1]), s);
+  if (e != cudaSuccess) return fail(LORA_ERR_CUDA, "%s: %s", what, cudaGetErrorString(e));
+  g_launches.fetch_add(1, std::memory_order_relaxed);
+  return LORA_OK;
+}
+
+#define LORA_TRY(expr)                     \
+  do {                                     \
+    const lora_status_t st_ = (expr);      \
+    if (st_ != LORA_OK) return st_;        \
+  } while (0)
+
+// ---------------------------------------------------------------- planning
+int64_t rup(int64_t x, int64_t m) { return (x + m - 1) / m * m; }
+
+// Byte layout of the saved buffer and of the workspace for one shape.
+struct Plan {
+  int r_pad = 0;     // bf16: r rounded up to 16 (K step of the MMA)
+  int64_t Mp = 0;    // bf16: M rounded up to 8 (16-byte pitch of the transposed copies)
+  size_t saved = 0;  // saved-buffer bytes
+  size_t sHt_off = 0;
+  // workspace offsets
+  size_t bpad_off = 0, bt_off = 0, sg_off = 0, sgt_off = 0, resaved_off = 0;
+  size_t fwd_ws = 0, bwd_ws = 0;
+};
+
+Plan make_plan(int64_t M, int64_t d_in, int64_t d_out, int r, lora_dtype_t dt) {
+  (void)d_in;
+  Plan P;
+  if (dt == LORA_BF16) {
+    P.r_pad = static_cast<int>(rup(r, 16));
+    P.Mp = rup(M, 8);
+    const size_t sH = size_t(M) * P.r_pad * 2;
+    P.sHt_off = rup(sH, 256);
+    P.saved = M > 0 ? P.sHt_off + size_t(P.r_pad) * P.Mp * 2 : 0;
+    P.fwd_ws = (r % 8) ? rup(size_t(d_out) * P.r_pad * 2, 256) : 0;
+    size_t off = 0;
+    P.bt_off = off;
+    off += rup(size_t(P.r_pad) * d_out * 2, 256);
+    P.sg_off = off;
+    off += rup(size_t(M) * P.r_pad * 2, 256);
+    P.sgt_off = off;
+    off += rup(size_t(P.r_pad) * P.Mp * 2, 256);
+    P.resaved_off = off;
+    off += rup(P.saved, 256);
+    P.bwd_ws = M > 0 ? off : 0;
+  } else {
+    P.r_pad = r;
+    P.Mp = M;
+    P.saved = size_t(M) * r * 4;
+    P.fwd_ws = 0;
+    P.sg_off = 0;
+    P.resaved_off = rup(size_t(M) * r * 4, 256);
+    P.bwd_ws = M > 0 ? P.resaved_off + rup(P.saved, 256) : 0;
+  }
+  return P;
+}
+
+// ---------------------------------------------------------------- checks
+lora_status_t check_shape(int r, int64_t M, int64_t d_in, int64_t d_out, lora_dtype_t dt,
+                          float alpha) {
+  if (dt != LORA_BF16 && dt != LORA_FP32)
+    return fail(LORA_ERR_INVALID_ARG, "dtype %d is not LORA_BF16 or LORA_FP32", int(dt));
+  if (r < 1 || r > 256) return fail(LORA_ERR_INVALID_ARG, "r = %d is outside [1, 256]", r);
+  if (M < 0) return fail(LORA_ERR_INVALID_ARG, "M = %lld is negative", (long long)M);
+  if (d_in < 1 || d_out < 1)
+    return fail(LORA_ERR_INVALID_ARG, "d_in = %lld, d_out = %lld must be >= 1", (long long)d_in,
+                (long long)d_out);
+  if (!std::isfinite(alpha)) return fail(LORA_ERR_INVALID_ARG, "alpha is not finite");
+  const int64_t kMaxDim = int64_t(1) << 28;
+  if (M > kMaxDim || d_in > kMaxDim || d_out > kMaxDim)
+    return fail(LORA_ERR_UNSUPPORTED, "a dimension exceeds 2^28");
+  const int64_t t1 = ((M + 127) / 128) * ((d_out + 255) / 256);
+  const int64_t t2 = ((M + 127) / 128) * ((d_in + 255) / 256);
+  if (t1 > INT32_MAX / 2 || t2 > INT32_MAX / 2)
+    return fail(LORA_ERR_UNSUPPORTED, "too many output tiles");
+  if (dt == LORA_BF16 && (d_in % 8 != 0 || d_out % 8 != 0))
+    return fail(LORA_ERR_UNSUPPORTED,
+                "bf16 needs d_in and d_out to be multiples of 8 (got %lld, %lld)",
+                (long long)d_in, (long long)d_out);
+  return LORA_OK;
+}
+
+lora_status_t check_ptr(const void *p, const char *name, bool may_be_null = false) {
+  if (p == nullptr) {
+    if (may_be_null) return LORA_OK;
+    return fail(LORA_ERR_INVALID_ARG, "%s is NULL", name);
+  }
+  if (reinterpret_cast<uintptr_t>(p) % 16 != 0)
+    return fail(LORA_ERR_INVALID_ARG, "%s is not 16-byte aligned", name);
+  return LORA_OK;
+}
+
+lora_status_t check_ws(const void *ws, size_t have, size_t need) {
+  if (need == 0) return LORA_OK;
+  if (ws == nullptr || have < need)
+    return fail(LORA_ERR_WORKSPACE, "workspace of %zu bytes needed, got %zu%s", need, have,
+                ws == nullptr ? " (NULL)" : "");
+  if (reinterpret_cast<uintptr_t>(ws) % 16 != 0)
+    return fail(LORA_ERR_INVALID_ARG, "workspace is not 16-byte aligned");
+  return LORA_OK;
+}
+
+uint8_t *at(void *base, size_t off) { return static_cast<uint8_t *>(base) + off; }
+
+// ---------------------------------------------------------------- bf16 path
+// sH = s X A^T into saved (row-major [M][r_pad]) and its transpose.
+lora_status_t down_fwd_bf16(const DevInfo &di, const Plan &P, const void *X, const void *A,
+                            float s, int r, int64_t M, int64_t d_in, void *saved,
+                            cudaStream_t st) {
+  SkinnyArgs f1;
+  LORA_TRY(tmap(&f1.tmA, X, d_in, M, d_in * 2, 64, 128, "X"));
+  LORA_TRY(tmap(&f1.tmB, A, d_in, r, d_in * 2, 64, P.r_pad, "A"));
+  f1.a_mn = false;
+  f1.rows = static_cast<int>(M);
+  f1.RP = P.r_pad;
+  f1.K = static_cast<int>(d_in);
+  f1.scale = s;
+  f1.out0 = saved;
+  f1.ld0 = P.r_pad;
+  f1.n0 = P.r_pad;
+  f1.out1 = at(saved, P.sHt_off);
+  f1.ld1 = P.Mp;
+  f1.n1 = P.r_pad;
+  f1.dev_status = di.status;
+  return run(LORA_K_DOWN_FWD, st, "s X A^T pass", [&] { return launch_skinny(f1, di.sms, st); });
+}
+
+lora_status_t fwd_bf16(const void *X, const void *W, const void *A, const void *B, float alpha,
+                       int r, int64_t M, int64_t d_in, int64_t d_out, void *Y, void *saved,
+                       void *ws, cudaStream_t st) {
+  DevInfo di;
+  LORA_TRY(device_info(di));
+  const Plan P = make_plan(M, d_in, d_out, r, LORA_BF16);
+  const float s = alpha / static_cast<float>(r);
+  const void *Bsrc = B;
+  int64_t b_inner = r;
+  if (r % 8 != 0) {  // B's row pitch is not a multiple of 16 bytes: pad it
+    void *Bp = at(ws, 0);
+    LORA_TRY(run(LORA_K_PREP, st, "pad B", [&] {
+      return launch_pad_cols_bf16(B, static_cast<int>(d_out), r, P.r_pad, Bp, st);
+    }));
+    Bsrc = Bp;
+    b_inner = P.r_pad;
+  }
+  LORA_TRY(down_fwd_bf16(di, P, X, A, s, r, M, d_in, saved, st));
+  MainGemmArgs f2;
+  LORA_TRY(tmap(&f2.tmA, X, d_in, M, d_in * 2, 64, 128, "X"));
+  LORA_TRY(tmap(&f2.tmB, W, d_in, d_out, d_in * 2, 64, 256, "W"));
+  LORA_TRY(tmap(&f2.tmA2, saved, P.r_pad, M, P.r_pad * 2, 64, 128, "sH"));
+  LORA_TRY(tmap(&f2.tmB2, Bsrc, b_inner, d_out, b_inner * 2, 64, 256, "B"));
+  f2.M = static_cast<int>(M);
+  f2.N = static_cast<int>(d_out);
+  f2.kb_main = static_cast<int>((d_in + 63) / 64);
+  f2.k_ext = P.r_pad;
+  f2.out = Y;
+  f2.ldo = d_out;
+  f2.b_mn = false;
+  f2.dev_status = di.status;
+  return run(LORA_K_MAIN_FWD, st, "forward GEMM", [&] { return launch_main_gemm(f2, di.sms, st); });
+}
+
+lora_status_t bwd_bf16(const void *dY, const void *X, const void *W, const void *A, const void *B,
+                       const void *saved, float alpha, int r, int64_t M, int64_t d_in,
+                       int64_t d_out, void *dX, void *dA, void *dB, void *ws, cudaStream_t st) {
+  DevInfo di;
+  LORA_TRY(device_info(di));
+  const Plan P = make_plan(M, d_in, d_out, r, LORA_BF16);
+  const float s = alpha / static_cast<float>(r);
+  if (saved == nullptr) {  // recompute s X A^T into the workspace
+    void *re = at(ws, P.resaved_off);
+    LORA_TRY(down_fwd_bf16(di, P, X, A, s, r, M, d_in, re, st));
+    saved = re;
+  }
+  const void *sHt = static_cast<const uint8_t *>(saved) + P.sHt_off;
+  void *Bt = at(ws, P.bt_off);
+  void *sG = at(ws, P.sg_off);
+  void *sGt = at(ws, P.sgt_off);
+
+  LORA_TRY(run(LORA_K_PREP, st, "transpose B", [&] {
+    return launch_transpose_pad_bf16(B, static_cast<int>(d_out), r, P.r_pad, Bt, st);
+  }));
+
+  // sG = s dY B, and its transpose
+  SkinnyArgs b1;
+  LORA_TRY(tmap(&b1.tmA, dY, d_out, M, d_out * 2, 64, 128, "dY"));
+  LORA_TRY(tmap(&b1.tmB, Bt, d_out, P.r_pad, d_out * 2, 64, P.r_pad, "B^T"));
+  b1.a_mn = false;
+  b1.rows = static_cast<int>(M);
+  b1.RP = P.r_pad;
+  b1.K = static_cast<int>(d_out);
+  b1.scale = s;
+  b1.out0 = sG;
+  b1.ld0 = P.r_pad;
+  b1.n0 = P.r_pad;
+  b1.out1 = sGt;
+  b1.ld1 = P.Mp;
+  b1.n1 = P.r_pad;
+  b1.dev_status = di.status;
+  LORA_TRY(run(LORA_K_DOWN_BWD, st, "s dY B pass", [&] { return launch_skinny(b1, di.sms, st); }));
+
+  // dB = dY^T sH   (rows = d_out, K = tokens)
+  SkinnyArgs b4;
+  LORA_TRY(tmap(&b4.tmA, dY, d_out, M, d_out * 2, 64, 64, "dY^T"));
+  LORA_TRY(tmap(&b4.tmB, sHt, M, P.r_pad, P.Mp * 2, 64, P.r_pad, "sH^T"));
+  b4.a_mn = true;
+  b4.rows = static_cast<int>(d_out);
+  b4.RP = P.r_pad;
+  b4.K = static_cast<int>(M);
+  b4.scale = 1.f;
+  b4.out0 = dB;
+  b4.ld0 = r;
+  b4.n0 = r;
+  b4.dev_status = di.status;
+  LORA_TRY(run(LORA_K_GRAD_B, st, "dB pass", [&] { return launch_skinny(b4, di.sms, st); }));
+
+  // dX = [dY | sG] . [W ; A]
+  if (dX != nullptr) {
+    MainGemmArgs b2;
+    LORA_TRY(tmap(&b2.tmA, dY, d_out, M, d_out * 2, 64, 128, "dY"));
+    LORA_TRY(tmap(&b2.tmB, W, d_in, d_out, d_in * 2, 64, 64, "W (MN-major)"));
+    LORA_TRY(tmap(&b2.tmA2, sG, P.r_pad, M, P.r_pad * 2, 64, 128, "sG"));
+    LORA_TRY(tmap(&b2.tmB2, A, d_in, r, d_in * 2, 64, 64, "A (MN-major)"));
+    b2.M = static_cast<int>(M);
+    b2.N = static_cast<int>(d_in);
+    b2.kb_main = static_cast<int>((d_out + 63) / 64);
+    b2.k_ext = P.r_pad;
+    b2.out = dX;
+    b2.ldo = d_in;
+    b2.b_mn = true;
+    b2.dev_status = di.status;
+    LORA_TRY(run(LORA_K_MAIN_BWD, st, "dX GEMM", [&] { return launch_main_gemm(b2, di.sms, st); }));
+  }
+
+  // dA^T = X^T sG   (rows = d_in, K = tokens), written transposed into dA
+  SkinnyArgs b3;
+  LORA_TRY(tmap(&b3.tmA, X, d_in, M, d_in * 2, 64, 64, "X^T"));
+  LORA_TRY(tmap(&b3.tmB, sGt, M, P.r_pad, P.Mp * 2, 64, P.r_pad, "sG^T"));
+  b3.a_mn = true;
+  b3.rows = static_cast<int>(d_in);
+  b3.RP = P.r_pad;
+  b3.K = static_cast<int>(M);
+  b3.scale = 1.f;
+  b3.out1 = dA;
+  b3.ld1 = d_in;
+  b3.n1 = r;
+  b3.dev_status = di.status;
+  return run(LORA_K_GRAD_A, st, "dA pass", [&] { return launch_skinny(b3, di.sms, st); });
+}
+
+// ---------------------------------------------------------------- fp32 path
+F32Operand op(const void *p, int64_t s0, int64_t s1) {
+  F32Operand o;
+  o.p = static_cast<const float *>(p);
+  o.s0 = s0;
+  o.s1 = s1;
+  return o;
+}
+
+lora_status_t gemm32(lora_kernel_kind_t kind, const char *what, const F32GemmArgs &a,
+                     cudaStream_t st) {
+  return run(kind, st, what, [&] { return launch_f32_gemm(a, st); });
+}
+
+lora_status_t down_fwd_f32(const void *X, const void *A, float s, int r, int64_t M, int64_t d_in,
+                           void *sH, cudaStream_t st) {
+  F32GemmArgs f1;  // sH[m][i] = s sum_k X[m][k] A[i][k]
+  f1.M = static_cast<int>(M);
+  f1.N = r;
+  f1.K1 = static_cast<int>(d_in);
+  f1.a1 = op(X, d_in, 1);
+  f1.b1 = op(A, 1, d_in);
+  f1.alpha = s;
+  f1.c = static_cast<float *>(sH);
+  f1.c0 = r;
+  f1.c1 = 1;
+  return gemm32(LORA_K_DOWN_FWD, "s X A^T pass (fp32)", f1, st);
+}
+
+lora_status_t fwd_f32(const void *X, const void *W, const void *A, const void *B, float alpha,
+                      int r, int64_t M, int64_t d_in, int64_t d_out, void *Y, void *saved,
+                      cudaStream_t st) {
+  DevInfo di;
+  LORA_TRY(device_info(di));
+  const float s = alpha / static_cast<float>(r);
+  LORA_TRY(down_fwd_f32(X, A, s, r, M, d_in, saved, st));
+  F32GemmArgs f2;  // Y[m][o] = sum_k X[m][k] W[o][k] + sum_i sH[m][i] B[o][i]
+  f2.M = static_cast<int>(M);
+  f2.N = static_cast<int>(d_out);
+  f2.K1 = static_cast<int>(d_in);
+  f2.a1 = op(X, d_in, 1);
+  f2.b1 = op(W, 1, d_in);
+  f2.K2 = r;
+  f2.a2 = op(saved, r, 1);
+  f2.b2 = op(B, 1, r);
+  f2.c = static_cast<float *>(Y);
+  f2.c0 = d_out;
+  f2.c1 = 1;
+  return gemm32(LORA_K_MAIN_FWD, "forward GEMM (fp32)", f2, st);
+}
+
+lora_status_t bwd_f32(const void *dY, const void *X, const void *W, const void *A, const void *B,
+                      const void *saved, float alpha, int r, int64_t M, int64_t d_in,
+                      int64_t d_out, void *dX, void *dA, void *dB, void *ws, cudaStream_t st) {
+  DevInfo di;
+  LORA_TRY(device_info(di));
+  const Plan P = make_plan(M, d_in, d_out, r, LORA_FP32);
+  const float s = alpha / static_cast<float>(r);
+  if (saved == nullptr) {
+    void *re = at(ws, P.resaved_off);
+    LORA_TRY(down_fwd_f32(X, A, s, r, M, d_in, re, st));
+    saved = re;
+  }
+  void *sG = at(ws, P.sg_off);
+  F32GemmArgs b1;  // sG[m][i] = s sum_o dY[m][o] B[o][i]
+  b1.M = static_cast<int>(M);
+  b1.N = r;
+  b1.K1 = static_cast<int>(d_out);
+  b1.a1 = op(dY, d_out, 1);
+  b1.b1 = op(B, r, 1);
+  b1.alpha = s;
+  b1.c = static_cast<float *>(sG);
+  b1.c0 = r;
+  b1.c1 = 1;
+  LORA_TRY(gemm32(LORA_K_DOWN_BWD, "s dY B pass (fp32)", b1, st));
+
+  F32GemmArgs b4;  // dB[o][i] = sum_m dY[m][o] sH[m][i]
+  b4.M = static_cast<int>(d_out);
+  b4.N = r;
+  b4.K1 = static_cast<int>(M);
+  b4.a1 = op(dY, 1, d_out);
+  b4.b1 = op(saved, r, 1);
+  b4.c = static_cast<float *>(dB);
+  b4.c0 = r;
+  b4.c1 = 1;
+  LORA_TRY(gemm32(LORA_K_GRAD_B, "dB pass (fp32)", b4, st));
+
+  if (dX != nullptr) {
+    F32GemmArgs b2;  // dX[m][k] = sum_o dY[m][o] W[o][k] + sum_i sG[m][i] A[i][k]
+    b2.M = static_cast<int>(M);
+    b2.N = static_cast<int>(d_in);
+    b2.K1 = static_cast<int>(d_out);
+    b2.a1 = op(dY, d_out, 1);
+    b2.b1 = op(W, d_in, 1);
+    b2.K2 = r;
+    b2.a2 = op(sG, r, 1);
+    b2.b2 = op(A, d_in, 1);
+    b2.c = static_cast<float *>(dX);
+    b2.c0 = d_in;
+    b2.c1 = 1;
+    LORA_TRY(gemm32(LORA_K_MAIN_BWD, "dX GEMM (fp32)", b2, st));
+  }
+
+  F32GemmArgs b3;  // dA[i][k] = sum_m sG[m][i] X[m][k]
+  b3.M = r;
+  b3.N = static_cast<int>(d_in);
+  b3.K1 = static_cast<int>(M);
+  b3.a1 = op(sG, 1, r);
+  b3.b1 = op(X, d_in, 1);
+  b3.c = static_cast<float *>(dA);
+  b3.c0 = d_in;
+  b3.c1 = 1;
+  return gemm32(LORA_K_GRAD_A, "dA pass (fp32)", b3, st);
+}
+
+}  // namespace
+}  // namespace lora
+
+using namespace lora;
+
+extern "C" {
+
+size_t lora_linear_saved_bytes(int64_t M, int r, lora_dtype_t dtype) {
+  if (M < 0 || r < 1 || r > 256 || (dtype != LORA_BF16 && dtype != LORA_FP32)) return 0;
+  return make_plan(M, 1, 1, r, dtype).saved;
+}
+
+size_t lora_linear_workspace_bytes(int64_t M, int64_t d_in, int64_t d_out, int r,
+                                   lora_dtype_t dtype) {
+  if (M < 0 || d_in < 1 || d_out < 1 || r < 1 || r > 256 ||
+      (dtype != LORA_BF16 && dtype != LORA_FP32))
+    return 0;
+  const Plan P = make_plan(M, d_in, d_out, r, dtype);
+  return P.fwd_ws > P.bwd_ws ? P.fwd_ws : P.bwd_ws;
+}
+
+lora_status_t lora_linear_fwd(const void *X, const void *W, const void *A, const void *B,
+                              float alpha, int r, int64_t M, int64_t d_in, int64_t d_out,
+                              lora_dtype_t dtype, void *Y, void *saved, void *workspace,
+                              size_t workspace_bytes, void *stream) {
+  t_err.clear();
+  LORA_TRY(check_shape(r, M, d_in, d_out, dtype, alpha));
+  const bool empty = M == 0;
+  LORA_TRY(check_ptr(X, "X", empty));
+  LORA_TRY(check_ptr(W, "W"));
+  LORA_TRY(check_ptr(A, "A"));
+  LORA_TRY(check_ptr(B, "B"));
+  LORA_TRY(check_ptr(Y, "Y", empty));
+  LORA_TRY(check_ptr(saved, "saved", empty));
+  const Plan P = make_plan(M, d_in, d_out, r, dtype);
+  LORA_TRY(check_ws(workspace, workspace_bytes, P.fwd_ws));
+  if (empty) return LORA_OK;
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  if (dtype == LORA_BF16) return fwd_bf16(X, W, A, B, alpha, r, M, d_in, d_out, Y, saved, workspace, st);
+  return fwd_f32(X, W, A, B, alpha, r, M, d_in, d_out, Y, saved, st);
+}
+
+lora_status_t lora_linear_bwd(const void *dY, const void *X, const void *W, const void *A,
+                              const void *B, const void *saved, float alpha, int r, int64_t M,
+                              int64_t d_in, int64_t d_out, lora_dtype_t dtype, void *dX, void *dA,
+                              void *dB, void *workspace, size_t workspace_bytes, void *stream) {
+  t_err.clear();
+  LORA_TRY(check_shape(r, M, d_in, d_out, dtype, alpha));
+  const bool empty = M == 0;
+  LORA_TRY(check_ptr(dY, "dY", empty));
+  LORA_TRY(check_ptr(X, "X", empty));
+  LORA_TRY(check_ptr(W, "W"));
+  LORA_TRY(check_ptr(A, "A"));
+  LORA_TRY(check_ptr(B, "B"));
+  LORA_TRY(check_ptr(saved, "saved", true));
+  LORA_TRY(check_ptr(dX, "dX", true));
+  LORA_TRY(check_ptr(dA, "dA"));
+  LORA_TRY(check_ptr(dB, "dB"));
+  const Plan P = make_plan(M, d_in, d_out, r, dtype);
+  size_t need = P.bwd_ws;
+  if (saved != nullptr) need = need > P.resaved_off ? P.resaved_off : need;  // no recompute room
+  if (empty) need = 0;
+  LORA_TRY(check_ws(workspace, workspace_bytes, need));
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  if (empty) {  // sums over zero tokens
+    const size_t es = dtype == LORA_BF16 ? 2 : 4;
+    cudaError_t e = cudaMemsetAsync(dA, 0, size_t(r) * d_in * es, st);
+    if (e == cudaSuccess) e = cudaMemsetAsync(dB, 0, size_t(d_out) * r * es, st);
+    if (e != cudaSuccess) return fail(LORA_ERR_CUDA, "zero dA/dB: %s", cudaGetErrorString(e));
+    return LORA_OK;
+  }
+  if (dtype == LORA_BF16)
+    return bwd_bf16(dY, X, W, A, B, saved, alpha, r, M, d_in, d_out, dX, dA, dB, workspace, st);
+  return bwd_f32(dY, X, W, A, B, saved, alpha, r, M, d_in, d_out, dX, dA, dB, workspace, st);
+}
+
+const char *lora_status_string(lora_status_t status) {
+  switch (status) {
+    case LORA_OK: return "LORA_OK";
+    case LORA_ERR_INVALID_ARG: return "LORA_ERR_INVALID_ARG";
+    case LORA_ERR_UNSUPPORTED: return "LORA_ERR_UNSUPPORTED";
+    case LORA_ERR_WORKSPACE: return "LORA_ERR_WORKSPACE";
+    case LORA_ERR_CUDA: return "LORA_ERR_CUDA";
+    case LORA_ERR_TIMEOUT: return "LORA_ERR_TIMEOUT";
+  }
+  return "LORA_ERR_UNKNOWN";
+}
+
+const char *lora_last_error(void) { return t_err.c_str(); }
+
+lora_status_t lora_device_status(int clear) {
+  t_err.clear();
+  cudaError_t e = cudaDeviceSynchronize();
+  if (e != cudaSuccess) return fail(LORA_ERR_CUDA, "synchronize: %s", cudaGetErrorString(e));
+  unsigned v = 0;
+  e = cudaMemcpyFromSymbol(&v, g_dev_status, sizeof(v));
+  if (e != cudaSuccess) return fail(LORA_ERR_CUDA, "read status: %s", cudaGetErrorString(e));
+  if (clear) {
+    const unsigned zero = 0;
+    e = cudaMemcpyToSymbol(g_dev_status, &zero, sizeof(zero));
+    if (e != cudaSuccess) return fail(LORA_ERR_CUDA, "clear status: %s", cudaGetErrorString(e));
+  }
+  if (v & kDevErrTimeout) return fail(LORA_ERR_TIMEOUT, "a device-side wait ran out (0x%x)", v);
+  return LORA_OK;
+}
+
+uint64_t lora_launch_count(void) { return g_launches.load(); }
+
+lora_status_t lora_set_timing_events(void *const *events, int *kinds, int n_pairs) {
+  t_err.clear();
+  if (events != nullptr && n_pairs < 0)
+    return fail(LORA_ERR_INVALID_ARG, "n_pairs = %d is negative", n_pairs);
+  t_hook.events = events;
+  t_hook.kinds = kinds;
+  t_hook.n = events ? n_pairs : 0;
+  t_hook.used = 0;
+  return LORA_OK;
+}
+
+int lora_timing_used(void) { return t_hook.used; }
+
+}  // extern "C"

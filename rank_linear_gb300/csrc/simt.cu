@@ -1,0 +1,111 @@
+// simt.cu -- CUDA-core kernels: the fp32 debug GEMM that runs the same
+// decomposition as the bf16 tensor-core path, and the small copies of the
+// adapter B that the tensor-core path reads.
+#include <cuda_bf16.h>
+
+#include "internal.h"
+
+namespace lora {
+namespace {
+
+constexpr int TM = 64, TN = 64, TK = 16;  // block tile; 16 x 16 threads, 4 x 4 outputs each
+
+// c = alpha * (A1 B1 + A2 B2) with strided operands, fp32 FFMA, one
+// accumulator per output, K visited in increasing order (segment 1 first).
+__global__ void __launch_bounds__(256) k_f32_gemm(F32GemmArgs a) {
+  __shared__ float As[TK][TM + 1];
+  __shared__ float Bs[TK][TN + 1];
+  const int tx = threadIdx.x % 16, ty = threadIdx.x / 16;
+  const int m0 = blockIdx.y * TM, n0 = blockIdx.x * TN;
+  float acc[4][4] = {};
+  for (int seg = 0; seg < 2; ++seg) {
+    const int K = seg == 0 ? a.K1 : a.K2;
+    const F32Operand A = seg == 0 ? a.a1 : a.a2;
+    const F32Operand B = seg == 0 ? a.b1 : a.b2;
+    for (int k0 = 0; k0 < K; k0 += TK) {
+      for (int i = threadIdx.x; i < TK * TM; i += 256) {
+        const int kk = i / TM, mm = i % TM;
+        const int m = m0 + mm, k = k0 + kk;
+        As[kk][mm] = (m < a.M && k < K) ? A.p[m * A.s0 + k * A.s1] : 0.f;
+      }
+      for (int i = threadIdx.x; i < TK * TN; i += 256) {
+        const int kk = i / TN, nn = i % TN;
+        const int n = n0 + nn, k = k0 + kk;
+        Bs[kk][nn] = (n < a.N && k < K) ? B.p[k * B.s0 + n * B.s1] : 0.f;
+      }
+      __syncthreads();
+#pragma unroll
+      for (int kk = 0; kk < TK; ++kk) {
+#pragma unroll
+        for (int i = 0; i < 4; ++i)
+#pragma unroll
+          for (int j = 0; j < 4; ++j) acc[i][j] = fmaf(As[kk][ty + 16 * i], Bs[kk][tx + 16 * j], acc[i][j]);
+      }
+      __syncthreads();
+    }
+  }
+#pragma unroll
+  for (int i = 0; i < 4; ++i)
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+      const int m = m0 + ty + 16 * i, n = n0 + tx + 16 * j;
+      if (m < a.M && n < a.N) a.c[m * a.c0 + n * a.c1] = a.alpha * acc[i][j];
+    }
+}
+
+// Bt[j][o] = B[o][j] (zero for j >= r), through a 32 x 32 shared tile.
+__global__ void k_transpose_pad(const __nv_bfloat16 *__restrict__ B, int d_out, int r, int r_pad,
+                                __nv_bfloat16 *__restrict__ Bt) {
+  __shared__ __nv_bfloat16 tile[32][33];
+  const int o0 = blockIdx.x * 32, j0 = blockIdx.y * 32;
+  for (int i = threadIdx.y; i < 32; i += 8) {
+    const int o = o0 + i, j = j0 + threadIdx.x;
+    tile[i][threadIdx.x] = (o < d_out && j < r) ? B[static_cast<int64_t>(o) * r + j]
+                                                : __float2bfloat16_rn(0.f);
+  }
+  __syncthreads();
+  for (int i = threadIdx.y; i < 32; i += 8) {
+    const int j = j0 + i, o = o0 + threadIdx.x;
+    if (j < r_pad && o < d_out) Bt[static_cast<int64_t>(j) * d_out + o] = tile[threadIdx.x][i];
+  }
+}
+
+// Bp[o][j] = B[o][j] (zero for r <= j < r_pad).
+__global__ void k_pad_cols(const __nv_bfloat16 *__restrict__ B, int d_out, int r, int r_pad,
+                           __nv_bfloat16 *__restrict__ Bp) {
+  const int64_t total = static_cast<int64_t>(d_out) * r_pad;
+  for (int64_t i = blockIdx.x * int64_t(blockDim.x) + threadIdx.x; i < total;
+       i += int64_t(gridDim.x) * blockDim.x) {
+    const int64_t o = i / r_pad;
+    const int j = static_cast<int>(i % r_pad);
+    Bp[i] = j < r ? B[o * r + j] : __float2bfloat16_rn(0.f);
+  }
+}
+
+}  // namespace
+
+cudaError_t launch_f32_gemm(const F32GemmArgs &a, cudaStream_t s) {
+  if (a.M <= 0 || a.N <= 0) return cudaSuccess;
+  dim3 grid((a.N + TN - 1) / TN, (a.M + TM - 1) / TM);
+  k_f32_gemm<<<grid, 256, 0, s>>>(a);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_transpose_pad_bf16(const void *B, int d_out, int r, int r_pad, void *Bt,
+                                      cudaStream_t s) {
+  dim3 grid((d_out + 31) / 32, (r_pad + 31) / 32), block(32, 8);
+  k_transpose_pad<<<grid, block, 0, s>>>(static_cast<const __nv_bfloat16 *>(B), d_out, r, r_pad,
+                                         static_cast<__nv_bfloat16 *>(Bt));
+  return cudaGetLastError();
+}
+
+cudaError_t launch_pad_cols_bf16(const void *B, int d_out, int r, int r_pad, void *Bp,
+                                 cudaStream_t s) {
+  const int64_t total = static_cast<int64_t>(d_out) * r_pad;
+  const int blocks = static_cast<int>(total / 256 + 1 < 4096 ? total / 256 + 1 : 4096);
+  k_pad_cols<<<blocks, 256, 0, s>>>(static_cast<const __nv_bfloat16 *>(B), d_out, r, r_pad,
+                                    static_cast<__nv_bfloat16 *>(Bp));
+  return cudaGetLastError();
+}
+
+}  // namespace lora

@@ -1,0 +1,134 @@
+"""Python face of the fused LoRA linear layer.
+
+    Y  = X W^T + s (X A^T) B^T,   s = alpha / r
+(ch05 "Acceleration principles: Triton kernels and fused LoRA", §5.3, LoRA
+equation), with the backward's dX, dA and dB (W frozen; the gradient list of
+ch05 §5.3).  Every step runs in the CUDA library through the C ABI; PyTorch
+only allocates device memory and supplies the current stream.  The autograd
+wrapper mirrors the custom autograd function with a hand-derived backward
+that the Unsloth essay describes for LoRA.
+"""
+from __future__ import annotations
+
+import torch
+
+from . import _lib
+
+_DT = {torch.bfloat16: _lib.LORA_BF16, torch.float32: _lib.LORA_FP32}
+
+
+def _dtype_code(t: torch.Tensor) -> int:
+    if t.dtype not in _DT:
+        raise TypeError(f"unsupported dtype {t.dtype}; use bfloat16 or float32")
+    return _DT[t.dtype]
+
+
+def _ptr(t):
+    return None if t is None else t.data_ptr() or None
+
+
+def _check_dev(*ts):
+    for t in ts:
+        if t is not None and (not t.is_cuda or not t.is_contiguous()):
+            raise ValueError("tensors must be contiguous CUDA tensors")
+
+
+def saved_bytes(M: int, r: int, dtype: torch.dtype) -> int:
+    return int(_lib.lib().lora_linear_saved_bytes(M, r, _DT[dtype]))
+
+
+def workspace_bytes(M: int, d_in: int, d_out: int, r: int, dtype: torch.dtype) -> int:
+    return int(_lib.lib().lora_linear_workspace_bytes(M, d_in, d_out, r, _DT[dtype]))
+
+
+def _buffer(nbytes: int, device) -> torch.Tensor:
+    # 256-byte granules keep every sub-buffer 16-byte aligned
+    return torch.empty(max(nbytes, 1), dtype=torch.uint8, device=device)
+
+
+def _stream_ptr(stream):
+    s = stream if stream is not None else torch.cuda.current_stream()
+    return s.cuda_stream or None
+
+
+def forward(X, W, A, B, alpha: float, *, Y=None, saved=None, workspace=None, stream=None):
+    """Y = X W^T + (alpha/r) X A^T B^T.  Returns (Y, saved)."""
+    _check_dev(X, W, A, B)
+    M, d_in = X.shape
+    d_out, r = B.shape
+    dt = _dtype_code(X)
+    L = _lib.lib()
+    if Y is None:
+        Y = torch.empty(M, d_out, dtype=X.dtype, device=X.device)
+    if saved is None:
+        saved = _buffer(L.lora_linear_saved_bytes(M, r, dt), X.device)
+    ws_need = L.lora_linear_workspace_bytes(M, d_in, d_out, r, dt)
+    if workspace is None:
+        workspace = _buffer(ws_need, X.device)
+    st = L.lora_linear_fwd(_ptr(X), _ptr(W), _ptr(A), _ptr(B), float(alpha), r, M, d_in, d_out,
+                           dt, _ptr(Y), _ptr(saved), _ptr(workspace), workspace.numel(),
+                           _stream_ptr(stream))
+    _lib.check(st, "lora_linear_fwd")
+    return Y, saved
+
+
+def backward(dY, X, W, A, B, alpha: float, saved=None, *, need_dX=True, dX=None, dA=None,
+             dB=None, workspace=None, stream=None):
+    """Returns (dX or None, dA, dB) for the upstream gradient dY."""
+    _check_dev(dY, X, W, A, B)
+    M, d_in = X.shape
+    d_out, r = B.shape
+    dt = _dtype_code(X)
+    L = _lib.lib()
+    if need_dX and dX is None:
+        dX = torch.empty(M, d_in, dtype=X.dtype, device=X.device)
+    if dA is None:
+        dA = torch.empty(r, d_in, dtype=X.dtype, device=X.device)
+    if dB is None:
+        dB = torch.empty(d_out, r, dtype=X.dtype, device=X.device)
+    if workspace is None:
+        workspace = _buffer(L.lora_linear_workspace_bytes(M, d_in, d_out, r, dt), X.device)
+    st = L.lora_linear_bwd(_ptr(dY), _ptr(X), _ptr(W), _ptr(A), _ptr(B), _ptr(saved),
+                           float(alpha), r, M, d_in, d_out, dt, _ptr(dX) if need_dX else None,
+                           _ptr(dA), _ptr(dB), _ptr(workspace), workspace.numel(),
+                           _stream_ptr(stream))
+    _lib.check(st, "lora_linear_bwd")
+    return (dX if need_dX else None), dA, dB
+
+
+class LoRALinearFunction(torch.autograd.Function):
+    """Autograd function: saves the low-rank activation for the backward."""
+
+    @staticmethod
+    def forward(ctx, X, W, A, B, alpha):
+        shape = X.shape
+        X2 = X.reshape(-1, shape[-1]).contiguous()
+        Y, saved = forward(X2, W.contiguous(), A.contiguous(), B.contiguous(), alpha)
+        ctx.save_for_backward(X2, W, A, B, saved)
+        ctx.alpha = alpha
+        ctx.x_shape = shape
+        return Y.reshape(*shape[:-1], W.shape[0])
+
+    @staticmethod
+    def backward(ctx, dY):
+        X2, W, A, B, saved = ctx.saved_tensors
+        dY2 = dY.reshape(-1, dY.shape[-1]).contiguous()
+        dX, dA, dB = backward(dY2, X2, W.contiguous(), A.contiguous(), B.contiguous(), ctx.alpha,
+                              saved, need_dX=ctx.needs_input_grad[0])
+        if dX is not None:
+            dX = dX.reshape(ctx.x_shape)
+        return dX, None, dA, dB, None
+
+
+def lora_linear(X, W, A, B, alpha: float):
+    """Y = X W^T + (alpha/r) (X A^T) B^T with gradients for X, A and B."""
+    return LoRALinearFunction.apply(X, W, A, B, alpha)
+
+
+def device_status(clear: bool = True) -> None:
+    """Raise if a bounded device-side wait ran out since the last check."""
+    _lib.check(_lib.lib().lora_device_status(1 if clear else 0), "device status")
+
+
+def launch_count() -> int:
+    return int(_lib.lib().lora_launch_count())

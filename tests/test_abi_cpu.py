@@ -1,0 +1,125 @@
+"""The C ABI library loads, exports every declared entry point, and rejects
+bad arguments with a status before touching CUDA (CPU only: no launches)."""
+import ctypes
+import os
+import re
+
+import pytest
+
+from rank_linear_gb300 import _lib, build
+
+HEADER = os.path.join(os.path.dirname(os.path.dirname(__file__)), "include", "lora_linear.h")
+L = None
+
+
+def setup_module():
+    global L
+    build.build()
+    L = _lib.lib()
+
+
+def declared_functions():
+    src = open(HEADER).read()
+    src = re.sub(r"/\*.*?\*/", "", src, flags=re.S)
+    return sorted(set(re.findall(r"\b(lora_\w+)\s*\(", src)))
+
+
+def test_every_declared_symbol_is_exported():
+    names = declared_functions()
+    assert len(names) >= 10
+    for n in names:
+        assert hasattr(L, n), n
+    assert set(names) == set(_lib.SIGNATURES), "binding and header disagree"
+
+
+def test_status_strings():
+    for code, name in enumerate(["LORA_OK", "LORA_ERR_INVALID_ARG", "LORA_ERR_UNSUPPORTED",
+                                 "LORA_ERR_WORKSPACE", "LORA_ERR_CUDA", "LORA_ERR_TIMEOUT"]):
+        assert L.lora_status_string(code).decode() == name
+
+
+def test_sizes():
+    # bf16: sH [M, r_pad] + transposed copy [r_pad, roundup(M, 8)], 256-B aligned
+    assert L.lora_linear_saved_bytes(4096, 16, _lib.LORA_BF16) == 4096 * 16 * 2 * 2
+    assert L.lora_linear_saved_bytes(100, 8, _lib.LORA_BF16) == 3328 + 16 * 104 * 2
+    assert L.lora_linear_saved_bytes(0, 16, _lib.LORA_BF16) == 0
+    assert L.lora_linear_saved_bytes(64, 8, _lib.LORA_FP32) == 64 * 8 * 4
+    assert L.lora_linear_saved_bytes(64, 0, _lib.LORA_BF16) == 0
+    ws = L.lora_linear_workspace_bytes(4096, 4096, 4096, 16, _lib.LORA_BF16)
+    # B^T [16, 4096] + sG [4096, 16] + sG^T [16, 4096] + room for a recomputed saved buffer
+    assert ws == 3 * 4096 * 16 * 2 + 4096 * 16 * 2 * 2
+    assert L.lora_linear_workspace_bytes(0, 64, 64, 16, _lib.LORA_BF16) == 0
+
+
+FAKE = 0x100000  # aligned non-null "device" address; never dereferenced here
+
+
+def fwd(**kw):
+    a = dict(X=FAKE, W=FAKE, A=FAKE, B=FAKE, alpha=16.0, r=16, M=128, d_in=256, d_out=256,
+             dt=_lib.LORA_BF16, Y=FAKE, saved=FAKE, ws=FAKE, ws_bytes=1 << 30)
+    a.update(kw)
+    return L.lora_linear_fwd(a["X"], a["W"], a["A"], a["B"], a["alpha"], a["r"], a["M"],
+                             a["d_in"], a["d_out"], a["dt"], a["Y"], a["saved"], a["ws"],
+                             a["ws_bytes"], None)
+
+
+def bwd(**kw):
+    a = dict(dY=FAKE, X=FAKE, W=FAKE, A=FAKE, B=FAKE, saved=FAKE, alpha=16.0, r=16, M=128,
+             d_in=256, d_out=256, dt=_lib.LORA_BF16, dX=FAKE, dA=FAKE, dB=FAKE, ws=FAKE,
+             ws_bytes=1 << 30)
+    a.update(kw)
+    return L.lora_linear_bwd(a["dY"], a["X"], a["W"], a["A"], a["B"], a["saved"], a["alpha"],
+                             a["r"], a["M"], a["d_in"], a["d_out"], a["dt"], a["dX"], a["dA"],
+                             a["dB"], a["ws"], a["ws_bytes"], None)
+
+
+@pytest.mark.parametrize("kw,code", [
+    (dict(r=0), _lib.LORA_ERR_INVALID_ARG),
+    (dict(r=257), _lib.LORA_ERR_INVALID_ARG),
+    (dict(M=-1), _lib.LORA_ERR_INVALID_ARG),
+    (dict(d_in=0), _lib.LORA_ERR_INVALID_ARG),
+    (dict(dt=7), _lib.LORA_ERR_INVALID_ARG),
+    (dict(alpha=float("nan")), _lib.LORA_ERR_INVALID_ARG),
+    (dict(X=None), _lib.LORA_ERR_INVALID_ARG),
+    (dict(W=None), _lib.LORA_ERR_INVALID_ARG),
+    (dict(Y=None), _lib.LORA_ERR_INVALID_ARG),
+    (dict(saved=None), _lib.LORA_ERR_INVALID_ARG),
+    (dict(A=FAKE + 8), _lib.LORA_ERR_INVALID_ARG),
+    (dict(d_in=260), _lib.LORA_ERR_UNSUPPORTED),
+    (dict(d_out=100), _lib.LORA_ERR_UNSUPPORTED),
+    (dict(M=1 << 29), _lib.LORA_ERR_UNSUPPORTED),
+    (dict(r=12, ws=None, ws_bytes=0), _lib.LORA_ERR_WORKSPACE),   # r % 8 != 0 pads B
+    (dict(r=12, ws_bytes=16), _lib.LORA_ERR_WORKSPACE),
+])
+def test_fwd_rejects(kw, code):
+    assert fwd(**kw) == code
+    assert L.lora_last_error().decode() != ""
+
+
+@pytest.mark.parametrize("kw,code", [
+    (dict(dY=None), _lib.LORA_ERR_INVALID_ARG),
+    (dict(dA=None), _lib.LORA_ERR_INVALID_ARG),
+    (dict(dB=None), _lib.LORA_ERR_INVALID_ARG),
+    (dict(dB=FAKE + 2), _lib.LORA_ERR_INVALID_ARG),
+    (dict(ws=None, ws_bytes=0), _lib.LORA_ERR_WORKSPACE),
+    (dict(ws_bytes=1024), _lib.LORA_ERR_WORKSPACE),
+    (dict(saved=None, ws_bytes=3 * 128 * 16 * 2 + 256), _lib.LORA_ERR_WORKSPACE),
+    (dict(dt=_lib.LORA_FP32, ws_bytes=4), _lib.LORA_ERR_WORKSPACE),
+    (dict(d_out=12), _lib.LORA_ERR_UNSUPPORTED),
+    (dict(r=300), _lib.LORA_ERR_INVALID_ARG),
+])
+def test_bwd_rejects(kw, code):
+    assert bwd(**kw) == code
+
+
+def test_timing_hook_set_and_clear():
+    assert L.lora_set_timing_events(None, None, 0) == _lib.LORA_OK
+    assert L.lora_timing_used() == 0
+
+
+def test_product_path_needs_the_library(monkeypatch, tmp_path):
+    """Without the built library the Python layer raises; it has no fallback."""
+    monkeypatch.setattr(_lib, "_lib", None)
+    monkeypatch.setattr(_lib, "LIB_PATH", str(tmp_path / "missing.so"))
+    with pytest.raises(RuntimeError, match="no CPU or PyTorch fallback"):
+        _lib.lib()
