@@ -1,0 +1,457 @@
+"""Benchmark of the fused LoRA linear layer, forward + backward, on GB300.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME]
+                    [--impl ours|reference]
+
+One step = one forward and one backward of the layer (every kernel of the
+hot path) over one synthetic batch of the named workload, inputs resident in
+HBM.  The metric is algorithmic TFLOP/s,
+    4 M d_in d_out + 6 M r (d_in + d_out)   FLOPs per step (no dW: W frozen),
+divided by the device time of the step (CUDA events on the launching stream;
+L2 is flushed by a 256 MiB write before every step, outside the events).
+
+Rank 0 prints one JSON line.  Under torchrun each rank runs an independent
+replica on its own GPU (the layer needs no exchange), the timed region is
+bracketed by barriers, and the slowest rank's time is used.
+
+--impl reference times the fp64 CPU oracle on the host cores instead, on a
+bounded token sample of the same workload (the pages ship no runnable
+reference implementation).
+"""
+from __future__ import annotations
+
+import argparse
+import ctypes
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = ("fused LoRA fwd+bwd TFLOP/s on 1 GB300 (Llama-3-8B shapes); "
+          "% of BF16 tensor peak")
+DEFAULT_WORKLOAD = "llama3_8b_q_proj"
+FLUSH_BYTES = 256 << 20
+FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0}
+
+
+def step_flops(M, d_in, d_out, r):
+    return 4 * M * d_in * d_out + 6 * M * r * (d_in + d_out)
+
+
+def kernel_work(kind, M, d_in, d_out, r):
+    """Algorithmic (flops, bytes) of one launch of each kernel kind (bf16)."""
+    e = 2
+    return {
+        "prep": (0, e * 2 * d_out * r),
+        "down_fwd": (2 * M * d_in * r, e * (M * d_in + r * d_in + M * r)),
+        "main_fwd": (2 * M * d_out * (d_in + r),
+                     e * (M * d_in + d_out * d_in + M * r + d_out * r + M * d_out)),
+        "down_bwd": (2 * M * d_out * r, e * (M * d_out + r * d_out + M * r)),
+        "main_bwd": (2 * M * d_in * (d_out + r),
+                     e * (M * d_out + d_out * d_in + M * r + r * d_in + M * d_in)),
+        "grad_a": (2 * M * d_in * r, e * (M * d_in + M * r + r * d_in)),
+        "grad_b": (2 * M * d_out * r, e * (M * d_out + M * r + d_out * r)),
+    }[kind]
+
+
+BOUND = {"prep": "hbm", "down_fwd": "hbm", "down_bwd": "hbm", "grad_a": "hbm",
+         "grad_b": "hbm", "main_fwd": "tensor", "main_bwd": "tensor"}
+
+
+def load_peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        d = json.load(open(p))
+        return {"hbm_gbs": float(d["hbm_gbs"]), "bf16_tflops": float(d["bf16_tflops"]),
+                "source": "measured"}
+    except Exception:
+        return dict(FALLBACK_PEAKS, source="fallback")
+
+
+def kernel_source_hash():
+    h = hashlib.sha256()
+    csrc = os.path.join(ROOT, "rank_linear_gb300", "csrc")
+    for f in sorted(os.listdir(csrc)):
+        h.update(open(os.path.join(csrc, f), "rb").read())
+    return h.hexdigest()[:16]
+
+
+def load_traffic(workload, kind):
+    """DRAM bytes per launch from a committed ncu capture, if it matches the
+    current kernel sources; else None."""
+    p = os.path.join(ROOT, "profiles", "traffic.json")
+    try:
+        d = json.load(open(p))
+    except Exception:
+        return None
+    ent = d.get(workload, {}).get(kind)
+    if not ent or ent.get("source_hash") != kernel_source_hash():
+        return None
+    return ent.get("bytes_per_launch")
+
+
+# ---------------------------------------------------------------- clocks
+class ClockSampler:
+    """nvidia-smi samples of SM clock and throttle reasons while running."""
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.gpu = gpu_index
+        self.samples = []
+        self.proc = None
+        self.thread = None
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.gpu), f"--query-gpu={self.FIELDS}",
+                 "--format=csv,noheader,nounits", "-lms", "50"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except Exception:
+            self.proc = None
+            return
+        self.thread = threading.Thread(target=self._read, daemon=True)
+        self.thread.start()
+
+    def _read(self):
+        for line in self.proc.stdout:
+            parts = [x.strip() for x in line.split(",")]
+            if len(parts) >= 9:
+                self.samples.append((time.time(), parts))
+
+    def stop(self):
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except Exception:
+                self.proc.kill()
+        if self.thread is not None:
+            self.thread.join(timeout=5)
+
+    def summary(self, t0, t1):
+        def num(x):
+            try:
+                return float(x)
+            except ValueError:
+                return None
+        inside = [p for t, p in self.samples if t0 <= t <= t1]
+        window = "timed"
+        if not inside:  # timed region shorter than the sampling period
+            near = sorted(self.samples, key=lambda s: min(abs(s[0] - t0), abs(s[0] - t1)))[:3]
+            inside = [p for _, p in near]
+            window = "nearest"
+        if not inside:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["unsampled"]}
+        sm = [num(p[1]) for p in inside if num(p[1]) is not None]
+        mx = [num(p[2]) for p in inside if num(p[2]) is not None]
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({n for p in inside for n, v in zip(names, p[5:9]) if v == "Active"})
+        return {"sm_mhz": statistics.median(sm) if sm else None,
+                "sm_max_mhz": max(mx) if mx else None, "reasons": reasons,
+                "samples": len(inside), "window": window}
+
+
+# ---------------------------------------------------------------- dist
+def dist_env():
+    return (int(os.environ.get("RANK", 0)), int(os.environ.get("WORLD_SIZE", 1)),
+            int(os.environ.get("LOCAL_RANK", 0)))
+
+
+def max_over_ranks(x: float, world: int, device=None) -> float:
+    """Largest value of x over all ranks (x itself when world == 1)."""
+    if world == 1:
+        return x
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([x], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def barrier(world: int):
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+
+
+# ---------------------------------------------------------------- CPU oracle
+def oracle_run(t, alpha):
+    import oracle
+    oracle.forward(t["X"], t["W"], t["A"], t["B"], alpha)
+    oracle.backward(t["dY"], t["X"], t["W"], t["A"], t["B"], alpha)
+
+
+def oracle_inputs(w, tokens):
+    from rank_linear_gb300.synth import make_inputs
+    t = make_inputs(tokens, w.d_in, w.d_out, w.r, w.dtype, seed=0)
+    import numpy as np
+    return {k: np.ascontiguousarray(v.double().numpy()) for k, v in t.items()}
+
+
+def oracle_sample_tokens(w, budget_s):
+    """Largest token count (power of two, <= M) whose oracle fwd+bwd fits
+    budget_s seconds, from one calibration run on 8 tokens."""
+    t = oracle_inputs(w, 8)
+    t0 = time.perf_counter()
+    oracle_run(t, w.alpha)
+    per_token = (time.perf_counter() - t0) / 8
+    tokens = 8
+    while tokens * 2 <= w.M and tokens * 2 * per_token <= budget_s:
+        tokens *= 2
+    return tokens
+
+
+def cpu_baseline(w, budget_s=15.0):
+    import oracle
+    tokens = oracle_sample_tokens(w, budget_s)
+    t = oracle_inputs(w, tokens)
+    t0 = time.perf_counter()
+    oracle_run(t, w.alpha)
+    dt = time.perf_counter() - t0
+    return {"value": step_flops(tokens, w.d_in, w.d_out, w.r) / dt / 1e12, "unit": "TFLOP/s",
+            "cores": oracle.threads(), "kind": "oracle",
+            "sample": f"one fp64 fwd+bwd of {tokens} of the {w.M} tokens "
+                      f"({w.d_in}x{w.d_out}, r={w.r}); {dt:.2f} s"}
+
+
+def run_reference(args, w):
+    rank, world, _ = dist_env()
+    if rank != 0:
+        return
+    import oracle
+    total_budget = 90.0
+    per_step = max(0.05, total_budget / max(1, args.steps + args.warmup))
+    tokens = oracle_sample_tokens(w, per_step)
+    t = oracle_inputs(w, tokens)
+    for _ in range(args.warmup):
+        oracle_run(t, w.alpha)
+    times = []
+    for _ in range(args.steps):
+        t0 = time.perf_counter()
+        oracle_run(t, w.alpha)
+        times.append(time.perf_counter() - t0)
+    sec = sum(times)
+    value = step_flops(tokens, w.d_in, w.d_out, w.r) * args.steps / sec / 1e12
+    line = {
+        "impl": "reference", "metric": METRIC, "value": value, "unit": "TFLOP/s",
+        "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": 1e3 * sec / args.steps, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": {"workload": w.name, "M": w.M, "d_in": w.d_in, "d_out": w.d_out, "r": w.r,
+                   "alpha": w.alpha, "sample_tokens": tokens},
+        "cpu_baseline": {"value": value, "unit": "TFLOP/s", "cores": oracle.threads(),
+                         "kind": "oracle",
+                         "sample": f"each step: fp64 fwd+bwd of {tokens} of the {w.M} tokens"},
+        "e2e": {"value": value, "unit": "TFLOP/s", "h2d_bytes_per_step": 0,
+                "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+
+
+# ---------------------------------------------------------------- GPU
+def run_ours(args, w):
+    import torch
+    import rank_linear_gb300 as rl
+    from rank_linear_gb300 import _lib
+    from rank_linear_gb300.synth import make_inputs
+
+    rank, world, local = dist_env()
+    if world > 1:
+        import torch.distributed as dist
+        torch.cuda.set_device(local)
+        dist.init_process_group("nccl", device_id=torch.device("cuda", local))
+    dev = torch.device("cuda", local)
+    torch.cuda.set_device(dev)
+    L = _lib.lib()
+
+    # CPU baseline first (rank 0, N = 1 only), before the GPU is busy
+    cpu = cpu_baseline(w) if (rank == 0 and world == 1 and not args.no_cpu_baseline) else None
+
+    M, d_in, d_out, r, alpha = w.M, w.d_in, w.d_out, w.r, w.alpha
+    tdt = torch.bfloat16 if w.dtype == "bf16" else torch.float32
+    t = make_inputs(M, d_in, d_out, r, w.dtype, seed=rank, device=dev)
+    X, W, A, B, dY = t["X"], t["W"], t["A"], t["B"], t["dY"]
+    Y = torch.empty(M, d_out, dtype=tdt, device=dev)
+    dX = torch.empty(M, d_in, dtype=tdt, device=dev)
+    dA = torch.empty(r, d_in, dtype=tdt, device=dev)
+    dB = torch.empty(d_out, r, dtype=tdt, device=dev)
+    saved = torch.empty(max(1, rl.saved_bytes(M, r, tdt)), dtype=torch.uint8, device=dev)
+    ws = torch.empty(max(1, rl.workspace_bytes(M, d_in, d_out, r, tdt)), dtype=torch.uint8,
+                     device=dev)
+    flush = torch.empty(FLUSH_BYTES, dtype=torch.uint8, device=dev)
+    stream = torch.cuda.current_stream()
+
+    def step():
+        rl.forward(X, W, A, B, alpha, Y=Y, saved=saved, workspace=ws, stream=stream)
+        rl.backward(dY, X, W, A, B, alpha, saved, dX=dX, dA=dA, dB=dB, workspace=ws,
+                    stream=stream)
+
+    for _ in range(args.warmup):
+        flush.zero_()
+        step()
+    torch.cuda.synchronize()
+    rl.device_status()
+
+    # per-kernel events over the timed region
+    launches_per_step = 0
+    n0 = rl.launch_count()
+    step()
+    torch.cuda.synchronize()
+    launches_per_step = rl.launch_count() - n0
+    n_pairs = launches_per_step * args.steps
+    kev = [torch.cuda.Event(enable_timing=True) for _ in range(2 * n_pairs)]
+    karr = (ctypes.c_void_p * (2 * n_pairs))(*[e.cuda_event for e in kev])
+    kinds = (ctypes.c_int * n_pairs)()
+    s_ev = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+    e_ev = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+
+    clocks = ClockSampler(local) if rank == 0 else None
+    if clocks:
+        clocks.start()
+        time.sleep(0.3)
+    barrier(world)
+    torch.cuda.synchronize()
+    L.lora_set_timing_events(karr, kinds, n_pairs)
+    c0 = rl.launch_count()
+    wall0 = time.time()
+    for i in range(args.steps):
+        flush.zero_()
+        s_ev[i].record(stream)
+        step()
+        e_ev[i].record(stream)
+    torch.cuda.synchronize()
+    wall1 = time.time()
+    launched = rl.launch_count() - c0
+    used = L.lora_timing_used()
+    L.lora_set_timing_events(None, None, 0)
+    barrier(world)
+    rl.device_status()
+    if clocks:
+        time.sleep(0.2)
+        clocks.stop()
+
+    step_ms = [s.elapsed_time(e) for s, e in zip(s_ev, e_ev)]
+    sec = max_over_ranks(sum(step_ms) / 1e3, world, dev)
+    flops = step_flops(M, d_in, d_out, r)
+    value = world * flops * args.steps / sec / 1e12
+
+    per_kind = {}
+    for j in range(used):
+        k = _lib.KERNEL_KINDS[kinds[j]]
+        per_kind.setdefault(k, []).append(kev[2 * j].elapsed_time(kev[2 * j + 1]))
+    total_k = sum(sum(v) for v in per_kind.values())
+    kern = {k: {"launches": len(v), "avg_us": 1e3 * sum(v) / len(v),
+                "share": sum(v) / total_k} for k, v in per_kind.items()}
+    dom = max(per_kind, key=lambda k: sum(per_kind[k]))
+
+    peaks = load_peaks()
+    fl, by = kernel_work(dom, M, d_in, d_out, r)
+    avg_s = sum(per_kind[dom]) / len(per_kind[dom]) / 1e3
+    if BOUND[dom] == "tensor":
+        ach, peak, unit = fl / avg_s / 1e12, peaks["bf16_tflops"], "TFLOP/s"
+    else:
+        ach, peak, unit = by / avg_s / 1e9, peaks["hbm_gbs"], "GB/s"
+    roofline = {"kernel": dom, "bound": BOUND[dom], "achieved": ach, "peak": peak,
+                "unit": unit, "frac": ach / peak, "peak_source": peaks["source"] + " (burst)",
+                "traffic": load_traffic(w.name, dom)}
+
+    e2e = None if args.no_e2e else run_e2e(args, w, t, tdt, dev, stream, world)
+
+    if rank == 0:
+        line = {
+            "metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": world,
+            "steps": args.steps, "warmup": args.warmup,
+            "ms_per_step": 1e3 * sec / args.steps, "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": w.dtype, "data": "synthetic",
+            "config": {"workload": w.name, "M": M, "d_in": d_in, "d_out": d_out, "r": r,
+                       "alpha": alpha, "l2": "flushed before every step (256 MiB write)",
+                       "parallelism": "replicas" if world > 1 else "single GPU"},
+            "pct_of_bf16_peak": 100.0 * value / world / peaks["bf16_tflops"],
+            "roofline": roofline, "kernels": kern,
+            "cpu_baseline": cpu, "e2e": e2e,
+            "gpu_launches": launched,
+            "clocks": clocks.summary(wall0, wall1) if clocks else None,
+        }
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+
+
+def run_e2e(args, w, t, tdt, dev, stream, world):
+    """Same metric through the C ABI with pinned host buffers: every step
+    copies the inputs in and the results (Y, dX, dA, dB) out."""
+    import torch
+    import rank_linear_gb300 as rl
+    M, d_in, d_out, r, alpha = w.M, w.d_in, w.d_out, w.r, w.alpha
+    h_in = {k: v.cpu().pin_memory() for k, v in t.items()}
+    d_in_t = {k: torch.empty_like(v) for k, v in t.items()}
+    outs = {"Y": (M, d_out), "dX": (M, d_in), "dA": (r, d_in), "dB": (d_out, r)}
+    d_out_t = {k: torch.empty(s, dtype=tdt, device=dev) for k, s in outs.items()}
+    h_out = {k: torch.empty(s, dtype=tdt).pin_memory() for k, s in outs.items()}
+    saved = torch.empty(max(1, rl.saved_bytes(M, r, tdt)), dtype=torch.uint8, device=dev)
+    ws = torch.empty(max(1, rl.workspace_bytes(M, d_in, d_out, r, tdt)), dtype=torch.uint8,
+                     device=dev)
+
+    def step():
+        for k in h_in:
+            d_in_t[k].copy_(h_in[k], non_blocking=True)
+        g = d_in_t
+        rl.forward(g["X"], g["W"], g["A"], g["B"], alpha, Y=d_out_t["Y"], saved=saved,
+                   workspace=ws, stream=stream)
+        rl.backward(g["dY"], g["X"], g["W"], g["A"], g["B"], alpha, saved, dX=d_out_t["dX"],
+                    dA=d_out_t["dA"], dB=d_out_t["dB"], workspace=ws, stream=stream)
+        for k in h_out:
+            h_out[k].copy_(d_out_t[k], non_blocking=True)
+
+    for _ in range(max(1, args.warmup)):
+        step()
+    torch.cuda.synchronize()
+    n = max(3, min(args.steps, 50))
+    e0 = torch.cuda.Event(enable_timing=True)
+    e1 = torch.cuda.Event(enable_timing=True)
+    barrier(world)
+    e0.record(stream)
+    for _ in range(n):
+        step()
+    e1.record(stream)
+    torch.cuda.synchronize()
+    sec = max_over_ranks(e0.elapsed_time(e1) / 1e3, world, dev)
+    bi = sum(v.numel() * v.element_size() for v in h_in.values())
+    bo = sum(v.numel() * v.element_size() for v in h_out.values())
+    return {"value": world * step_flops(M, d_in, d_out, r) * n / sec / 1e12, "unit": "TFLOP/s",
+            "h2d_bytes_per_step": bi, "d2h_bytes_per_step": bo, "steps": n,
+            "inputs": "X, W, A, B, dY copied in; Y, dX, dA, dB copied out (pinned host)"}
+
+
+def main(argv=None):
+    from rank_linear_gb300.synth import WORKLOADS
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=200)
+    ap.add_argument("--warmup", type=int, default=10)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--workload", default=DEFAULT_WORKLOAD, choices=sorted(WORKLOADS))
+    ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args(argv)
+    args.warmup = max(args.warmup, 3)  # at least three untimed warm-up steps
+    w = WORKLOADS[args.workload]
+    if args.impl == "reference":
+        run_reference(args, w)
+    else:
+        run_ours(args, w)
+
+
+if __name__ == "__main__":
+    main()

@@ -44,6 +44,8 @@ _SIGS = {
     "lora_oracle_db": ([_D, _D, ctypes.c_double, _i64, _i64, _i64, _D], None),
     "lora_oracle_h_col": ([_D, _D, _i64, _i64, _i64, _D], None),
     "lora_oracle_g_col": ([_D, _D, _i64, _i64, _i64, _i64, _D], None),
+    "lora_oracle_h_rows": ([_D, _D, _i64, _i64, _I, _i64, _D], None),
+    "lora_oracle_g_rows": ([_D, _D, _i64, _i64, _I, _i64, _D], None),
     "lora_oracle_y_rows": ([_D, _D, _D, _D, ctypes.c_double, _i64, _i64, _i64, _I, _i64, _D], None),
     "lora_oracle_dx_rows": ([_D, _D, _D, _D, ctypes.c_double, _i64, _i64, _i64, _I, _i64, _D], None),
     "lora_oracle_da_entries": ([_D, _D, ctypes.c_double, _i64, _i64, _I, _i64, _D], None),
@@ -178,10 +180,26 @@ class Sampled:
                                    self.r, _p(self._G))
         return self._G
 
+    def _h_rows(self, rows) -> np.ndarray:
+        if self._H is not None:
+            return self._H
+        H = np.zeros((self.M, self.r))
+        self.lib.lora_oracle_h_rows(_p(self.X), _p(self.A), self.d_in, self.r,
+                                    _ip(rows), len(rows), _p(H))
+        return H
+
+    def _g_rows(self, rows) -> np.ndarray:
+        if self._G is not None:
+            return self._G
+        G = np.zeros((self.M, self.r))
+        self.lib.lora_oracle_g_rows(_p(self.dY), _p(self.B), self.d_out, self.r,
+                                    _ip(rows), len(rows), _p(G))
+        return G
+
     def y_rows(self, rows) -> np.ndarray:
         rows = np.ascontiguousarray(rows, dtype=np.int64)
         out = np.empty((len(rows), self.d_out))
-        H = self.H()
+        H = self._h_rows(rows)
         self.lib.lora_oracle_y_rows(_p(self.X), _p(self.W), _p(self.B), _p(H),
                                     self.s, self.d_in, self.d_out, self.r,
                                     _ip(rows), len(rows), _p(out))
@@ -190,7 +208,7 @@ class Sampled:
     def dx_rows(self, rows) -> np.ndarray:
         rows = np.ascontiguousarray(rows, dtype=np.int64)
         out = np.empty((len(rows), self.d_in))
-        G = self.G()
+        G = self._g_rows(rows)
         self.lib.lora_oracle_dx_rows(_p(self.dY), _p(self.W), _p(self.A), _p(G),
                                      self.s, self.d_in, self.d_out, self.r,
                                      _ip(rows), len(rows), _p(out))

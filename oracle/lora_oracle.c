@@ -196,8 +196,30 @@ void lora_oracle_g_col(const double *dY, const double *B, int64_t M,
         out[m] = g_elem(dY, B, d_out, r, m, i);
 }
 
+/* Rows rows[j] of H and of G, written in place into full-size [M][r]
+ * arrays (other rows are left untouched). */
+void lora_oracle_h_rows(const double *X, const double *A, int64_t d_in,
+                        int64_t r, const int64_t *rows, int64_t n_rows,
+                        double *H)
+{
+#pragma omp parallel for schedule(static) collapse(2)
+    for (int64_t j = 0; j < n_rows; ++j)
+        for (int64_t i = 0; i < r; ++i)
+            H[rows[j] * r + i] = h_elem(X, A, d_in, rows[j], i);
+}
+
+void lora_oracle_g_rows(const double *dY, const double *B, int64_t d_out,
+                        int64_t r, const int64_t *rows, int64_t n_rows,
+                        double *G)
+{
+#pragma omp parallel for schedule(static) collapse(2)
+    for (int64_t j = 0; j < n_rows; ++j)
+        for (int64_t i = 0; i < r; ++i)
+            G[rows[j] * r + i] = g_elem(dY, B, d_out, r, rows[j], i);
+}
+
 /* Y[rows[j]][:] for n_rows rows, out [n_rows][d_out].  H holds the full
- * [M][r] matrix (only the sampled rows are read). */
+ * [M][r] matrix or one filled by lora_oracle_h_rows for the sampled rows. */
 void lora_oracle_y_rows(const double *X, const double *W, const double *B,
                         const double *H, double s, int64_t d_in,
                         int64_t d_out, int64_t r, const int64_t *rows,

@@ -1,0 +1,206 @@
+"""CUDA path vs the fp64 oracle, through the C ABI (needs a GB300).
+
+Metric for every output tensor T: max|T_gpu - T_ref| / max|T_ref|, which
+must be <= 1e-2 for bf16 and <= 1e-5 for the fp32 debug dtype.  Small and
+ragged shapes are compared element by element; the full-size workloads are
+compared on sampled rows of Y and dX and sampled entries of dA and dB, in the
+launch configuration the benchmark times.
+"""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import rank_linear_gb300 as rl
+from rank_linear_gb300.synth import WORKLOADS, make_inputs
+
+pytestmark = pytest.mark.gpu
+
+TOL = {"bf16": 1e-2, "fp32": 1e-5}
+DEV = "cuda:0"
+
+
+def rel_err(got, ref) -> float:
+    got = got.double().cpu().numpy() if isinstance(got, torch.Tensor) else got
+    den = np.abs(ref).max()
+    return float(np.abs(got - ref).max() / (den if den > 0 else 1.0))
+
+
+def run_gpu(t, alpha, saved_none=False, need_dX=True):
+    g = {k: v.to(DEV) for k, v in t.items()}
+    Y, saved = rl.forward(g["X"], g["W"], g["A"], g["B"], alpha)
+    dX, dA, dB = rl.backward(g["dY"], g["X"], g["W"], g["A"], g["B"], alpha,
+                             None if saved_none else saved, need_dX=need_dX)
+    torch.cuda.synchronize()
+    rl.device_status()
+    return Y, dX, dA, dB
+
+
+def check_full(t, alpha, dt):
+    Y, dX, dA, dB = run_gpu(t, alpha)
+    _, Yr = oracle.forward(t["X"], t["W"], t["A"], t["B"], alpha)
+    dXr, dAr, dBr = oracle.backward(t["dY"], t["X"], t["W"], t["A"], t["B"], alpha)
+    errs = {"Y": rel_err(Y, Yr), "dX": rel_err(dX, dXr), "dA": rel_err(dA, dAr),
+            "dB": rel_err(dB, dBr)}
+    for k, e in errs.items():
+        assert e <= TOL[dt], f"{k}: {e:.3e} > {TOL[dt]} ({errs})"
+    return errs
+
+
+# M, d_in, d_out, r, alpha: several tiles in every dimension plus ragged tails
+SMALL_BF16 = [
+    (300, 392, 264, 16, 32.0),     # M, K and N all ragged
+    (520, 520, 1000, 24, 48.0),    # r not a multiple of 16 (padded to 32)
+    (129, 136, 264, 12, 24.0),     # r not a multiple of 8 (B padded in the forward)
+    (1, 64, 64, 1, 2.0),           # one token, rank one
+    (256, 512, 384, 256, 512.0),   # maximum rank
+    (1000, 1024, 768, 64, 128.0),
+    (2048, 1536, 2560, 128, 256.0),
+    (64, 8, 8, 8, 16.0),           # K smaller than one block
+    (777, 4104, 520, 16, 16.0),    # long ragged K (dX GEMM has a ragged N)
+]
+
+
+@pytest.mark.parametrize("M,d_in,d_out,r,alpha", SMALL_BF16)
+def test_bf16_elementwise(M, d_in, d_out, r, alpha):
+    t = make_inputs(M, d_in, d_out, r, "bf16", seed=M + r)
+    check_full(t, alpha, "bf16")
+
+
+@pytest.mark.parametrize("M,d_in,d_out,r,alpha", [
+    (64, 256, 256, 8, 16.0),       # the tiny fp32 workload
+    (130, 200, 72, 5, 10.0),       # ragged, odd widths allowed in fp32
+])
+def test_fp32_elementwise(M, d_in, d_out, r, alpha):
+    t = make_inputs(M, d_in, d_out, r, "fp32", seed=3)
+    check_full(t, alpha, "fp32")
+
+
+def test_tiny_workload_fp32():
+    w = WORKLOADS["tiny_fp32"]
+    t = make_inputs(w.M, w.d_in, w.d_out, w.r, w.dtype, seed=0)
+    check_full(t, w.alpha, "fp32")
+
+
+@pytest.mark.parametrize("name", ["llama3_8b_q_proj", "llama3_8b_gate_up",
+                                  "llama3_8b_down_proj", "qwen_wide_ffn"])
+def test_full_size_sampled(name):
+    w = WORKLOADS[name]
+    t = make_inputs(w.M, w.d_in, w.d_out, w.r, w.dtype, seed=0, device=DEV)
+    Y, dX, dA, dB = run_gpu(t, w.alpha)
+    host = {k: v.cpu() for k, v in t.items()}
+    S = oracle.Sampled(host["X"], host["W"], host["A"], host["B"], host["dY"], w.alpha)
+    rng = np.random.default_rng(1)
+    rows = np.unique(np.concatenate([[0, 127, 128, w.M - 1], rng.integers(0, w.M, 4)]))
+    e_y = rel_err(Y[rows].double().cpu().numpy(), S.y_rows(rows))
+    e_x = rel_err(dX[rows].double().cpu().numpy(), S.dx_rows(rows))
+    ii = np.repeat(rng.choice(w.r, 3, replace=False), 8)
+    kk = rng.integers(0, w.d_in, len(ii))
+    oo = rng.integers(0, w.d_out, len(ii))
+    e_a = rel_err(dA[ii, kk].double().cpu().numpy(), S.da_entries(ii, kk))
+    e_b = rel_err(dB[oo, ii].double().cpu().numpy(), S.db_entries(oo, ii))
+    for k, e in (("Y", e_y), ("dX", e_x), ("dA", e_a), ("dB", e_b)):
+        assert e <= TOL["bf16"], f"{name} {k}: {e:.3e}"
+    # no NaN / Inf anywhere in the full outputs
+    for T in (Y, dX, dA, dB):
+        assert torch.isfinite(T).all()
+
+
+def test_bitwise_deterministic():
+    t = make_inputs(1000, 1024, 768, 64, "bf16", seed=11)
+    a = run_gpu(t, 128.0)
+    b = run_gpu(t, 128.0)
+    for x, y in zip(a, b):
+        assert torch.equal(x, y)
+
+
+def test_recompute_when_saved_is_null():
+    t = make_inputs(300, 392, 264, 16, "bf16", seed=5)
+    a = run_gpu(t, 32.0)
+    b = run_gpu(t, 32.0, saved_none=True)
+    for x, y in zip(a, b):
+        assert torch.equal(x, y)
+
+
+def test_skip_dx():
+    t = make_inputs(300, 392, 264, 16, "bf16", seed=5)
+    a = run_gpu(t, 32.0)
+    b = run_gpu(t, 32.0, need_dX=False)
+    assert b[1] is None
+    assert torch.equal(a[2], b[2]) and torch.equal(a[3], b[3])
+
+
+def test_b_zero_gives_exact_zero_dA():
+    """B = 0 (a fresh LoRA adapter): dA = 0 exactly and Y = X W^T."""
+    t = make_inputs(300, 392, 264, 16, "bf16", seed=6)
+    t["B"] = torch.zeros_like(t["B"])
+    Y, dX, dA, dB = run_gpu(t, 32.0)
+    assert torch.count_nonzero(dA) == 0
+    ref = t["X"].double() @ t["W"].double().T
+    assert rel_err(Y, ref.numpy()) <= TOL["bf16"]
+
+
+def test_transposition_identity():
+    """dX(dY; W, A, B) equals Y(X := dY; W := W^T, A := B^T, B := A^T)."""
+    M, d_in, d_out, r, alpha = 300, 392, 264, 16, 32.0
+    t = make_inputs(M, d_in, d_out, r, "bf16", seed=7)
+    _, dX, _, _ = run_gpu(t, alpha)
+    g = {k: v.to(DEV) for k, v in t.items()}
+    Yt, _ = rl.forward(g["dY"], g["W"].T.contiguous(), g["B"].T.contiguous(),
+                       g["A"].T.contiguous(), alpha)
+    torch.cuda.synchronize()
+    ref = dX.double().cpu().numpy()
+    assert rel_err(Yt, ref) <= 4e-3
+
+
+def test_empty_batch():
+    t = make_inputs(1, 64, 64, 16, "bf16", seed=8)
+    g = {k: v.to(DEV) for k, v in t.items()}
+    X0 = g["X"][:0]
+    dY0 = g["dY"][:0]
+    Y, saved = rl.forward(X0, g["W"], g["A"], g["B"], 32.0)
+    dX, dA, dB = rl.backward(dY0, X0, g["W"], g["A"], g["B"], 32.0, saved)
+    torch.cuda.synchronize()
+    assert Y.shape == (0, 64) and dX.shape == (0, 64)
+    assert torch.count_nonzero(dA) == 0 and torch.count_nonzero(dB) == 0
+
+
+def test_autograd_function():
+    M, d_in, d_out, r, alpha = 2 * 150, 256, 320, 16, 32.0
+    t = make_inputs(M, d_in, d_out, r, "bf16", seed=9)
+    X = t["X"].to(DEV).reshape(2, 150, d_in).requires_grad_(True)
+    W = t["W"].to(DEV)
+    A = t["A"].to(DEV).requires_grad_(True)
+    B = t["B"].to(DEV).requires_grad_(True)
+    Y = rl.lora_linear(X, W, A, B, alpha)
+    Y.backward(t["dY"].to(DEV).reshape(2, 150, d_out))
+    torch.cuda.synchronize()
+    _, Yr = oracle.forward(t["X"], t["W"], t["A"], t["B"], alpha)
+    dXr, dAr, dBr = oracle.backward(t["dY"], t["X"], t["W"], t["A"], t["B"], alpha)
+    assert rel_err(Y.reshape(M, d_out), Yr) <= 1e-2
+    assert rel_err(X.grad.reshape(M, d_in), dXr) <= 1e-2
+    assert rel_err(A.grad, dAr) <= 1e-2
+    assert rel_err(B.grad, dBr) <= 1e-2
+
+
+def test_timing_hook_records_every_launch():
+    import ctypes
+    from rank_linear_gb300 import _lib
+    t = make_inputs(300, 392, 264, 16, "bf16", seed=5)
+    g = {k: v.to(DEV) for k, v in t.items()}
+    evs = [torch.cuda.Event(enable_timing=True) for _ in range(16)]
+    arr = (ctypes.c_void_p * 16)(*[e.cuda_event for e in evs])
+    kinds = (ctypes.c_int * 8)()
+    L = _lib.lib()
+    n0 = rl.launch_count()
+    assert L.lora_set_timing_events(arr, kinds, 8) == 0
+    Y, saved = rl.forward(g["X"], g["W"], g["A"], g["B"], 32.0)
+    rl.backward(g["dY"], g["X"], g["W"], g["A"], g["B"], 32.0, saved)
+    used = L.lora_timing_used()
+    L.lora_set_timing_events(None, None, 0)
+    torch.cuda.synchronize()
+    assert used == rl.launch_count() - n0 == 7
+    assert [_lib.KERNEL_KINDS[k] for k in kinds[:used]] == [
+        "down_fwd", "main_fwd", "prep", "down_bwd", "grad_b", "main_bwd", "grad_a"]
+    for j in range(used):
+        assert evs[2 * j].elapsed_time(evs[2 * j + 1]) > 0
