@@ -309,9 +309,7 @@ def run_ours(args, w):
     torch.cuda.synchronize()
     launches_per_step = rl.launch_count() - n0
     n_pairs = launches_per_step * args.steps
-    kev = [torch.cuda.Event(enable_timing=True) for _ in range(2 * n_pairs)]
-    karr = (ctypes.c_void_p * (2 * n_pairs))(*[e.cuda_event for e in kev])
-    kinds = (ctypes.c_int * n_pairs)()
+    kev, karr, kinds = rl.timing_events(n_pairs, stream)
     s_ev = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
     e_ev = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
 
@@ -321,7 +319,7 @@ def run_ours(args, w):
         time.sleep(0.3)
     barrier(world)
     torch.cuda.synchronize()
-    L.lora_set_timing_events(karr, kinds, n_pairs)
+    _lib.check(L.lora_set_timing_events(karr, kinds, n_pairs), "timing hook")
     c0 = rl.launch_count()
     wall0 = time.time()
     for i in range(args.steps):

@@ -120,12 +120,18 @@ lora_status_t run(lora_kernel_kind_t kind, cudaStream_t s, const char *what, F &
   int j = -1;
   if (t_hook.events != nullptr && t_hook.used < t_hook.n) {
     j = t_hook.used++;
-    cudaEventRecord(static_cast<cudaEvent_t>(t_hook.events[2 * j]), s);
+    const cudaError_t er = cudaEventRecord(static_cast<cudaEvent_t>(t_hook.events[2 * j]), s);
+    if (er != cudaSuccess)
+      return fail(LORA_ERR_CUDA, "timing event before %s: %s", what, cudaGetErrorString(er));
     if (t_hook.kinds) t_hook.kinds[j] = static_cast<int>(kind);
   }
   const cudaError_t e = launch();
-  if (j >= 0) cudaEventRecord(static_cast<cudaEvent_t>(t_hook.events[2 * j + 1]), s);
   if (e != cudaSuccess) return fail(LORA_ERR_CUDA, "%s: %s", what, cudaGetErrorString(e));
+  if (j >= 0) {
+    const cudaError_t er = cudaEventRecord(static_cast<cudaEvent_t>(t_hook.events[2 * j + 1]), s);
+    if (er != cudaSuccess)
+      return fail(LORA_ERR_CUDA, "timing event after %s: %s", what, cudaGetErrorString(er));
+  }
   g_launches.fetch_add(1, std::memory_order_relaxed);
   return LORA_OK;
 }
@@ -601,6 +607,10 @@ lora_status_t lora_set_timing_events(void *const *events, int *kinds, int n_pair
   t_err.clear();
   if (events != nullptr && n_pairs < 0)
     return fail(LORA_ERR_INVALID_ARG, "n_pairs = %d is negative", n_pairs);
+  if (events != nullptr)
+    for (int i = 0; i < 2 * n_pairs; ++i)
+      if (events[i] == nullptr)
+        return fail(LORA_ERR_INVALID_ARG, "timing event %d is NULL (not created yet?)", i);
   t_hook.events = events;
   t_hook.kinds = kinds;
   t_hook.n = events ? n_pairs : 0;

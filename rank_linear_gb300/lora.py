@@ -130,5 +130,19 @@ def device_status(clear: bool = True) -> None:
     _lib.check(_lib.lib().lora_device_status(1 if clear else 0), "device status")
 
 
+def timing_events(n_pairs: int, stream=None):
+    """Create 2*n_pairs timing events (recorded once so that the CUDA event
+    objects exist) and the ctypes arrays the library's timing hook takes."""
+    import ctypes
+    st = stream if stream is not None else torch.cuda.current_stream()
+    evs = [torch.cuda.Event(enable_timing=True) for _ in range(2 * n_pairs)]
+    for e in evs:
+        e.record(st)
+    st.synchronize()
+    arr = (ctypes.c_void_p * (2 * n_pairs))(*[e.cuda_event for e in evs])
+    kinds = (ctypes.c_int * max(1, n_pairs))()
+    return evs, arr, kinds
+
+
 def launch_count() -> int:
     return int(_lib.lib().lora_launch_count())

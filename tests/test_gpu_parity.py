@@ -21,7 +21,8 @@ DEV = "cuda:0"
 
 
 def rel_err(got, ref) -> float:
-    got = got.double().cpu().numpy() if isinstance(got, torch.Tensor) else got
+    if isinstance(got, torch.Tensor):
+        got = got.detach().double().cpu().numpy()
     den = np.abs(ref).max()
     return float(np.abs(got - ref).max() / (den if den > 0 else 1.0))
 
@@ -184,13 +185,10 @@ def test_autograd_function():
 
 
 def test_timing_hook_records_every_launch():
-    import ctypes
     from rank_linear_gb300 import _lib
     t = make_inputs(300, 392, 264, 16, "bf16", seed=5)
     g = {k: v.to(DEV) for k, v in t.items()}
-    evs = [torch.cuda.Event(enable_timing=True) for _ in range(16)]
-    arr = (ctypes.c_void_p * 16)(*[e.cuda_event for e in evs])
-    kinds = (ctypes.c_int * 8)()
+    evs, arr, kinds = rl.timing_events(8)
     L = _lib.lib()
     n0 = rl.launch_count()
     assert L.lora_set_timing_events(arr, kinds, 8) == 0
@@ -204,3 +202,10 @@ def test_timing_hook_records_every_launch():
         "down_fwd", "main_fwd", "prep", "down_bwd", "grad_b", "main_bwd", "grad_a"]
     for j in range(used):
         assert evs[2 * j].elapsed_time(evs[2 * j + 1]) > 0
+
+
+def test_timing_hook_rejects_uncreated_events():
+    import ctypes
+    from rank_linear_gb300 import _lib
+    arr = (ctypes.c_void_p * 2)(None, None)
+    assert _lib.lib().lora_set_timing_events(arr, None, 1) == _lib.LORA_ERR_INVALID_ARG
