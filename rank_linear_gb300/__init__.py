@@ -5,7 +5,8 @@ Importing this package does not load the CUDA library; the first call does,
 and fails loudly if it has not been built.
 """
 from .lora import (LoRALinearFunction, backward, device_status, forward, launch_count,
+                   timing_events,
                    lora_linear, saved_bytes, workspace_bytes)
 
 __all__ = ["LoRALinearFunction", "backward", "device_status", "forward", "launch_count",
-           "lora_linear", "saved_bytes", "workspace_bytes"]
+           "lora_linear", "saved_bytes", "timing_events", "workspace_bytes"]
