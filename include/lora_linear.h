@@ -132,6 +132,42 @@ lora_status_t lora_linear_bwd(const void *dY, const void *X, const void *W,
                               void *dA, void *dB, void *workspace,
                               size_t workspace_bytes, void *stream);
 
+/*
+ * Backward without a caller-supplied workspace.  (The pages have no
+ * counterpart: this is a convenience of this library.)
+ *
+ * For callers that cannot allocate device memory when they call the
+ * backward -- for example a plugin running inside a host application that
+ * owns all device memory and gives it no allocator, or a latency-critical
+ * loop that must not call cudaMalloc (which may synchronise the device)
+ * after start-up.  Arguments and results are those of lora_linear_bwd; the
+ * scratch the kernels need comes from one array of
+ * LORA_NOALLOC_SCRATCH_BYTES bytes that the library holds in device memory
+ * on every GPU that loads it, until the process exits.
+ *
+ *  - Limit: shapes whose backward needs more than LORA_NOALLOC_SCRATCH_BYTES
+ *    of scratch (lora_linear_workspace_bytes minus the recompute room when
+ *    saved != NULL) are rejected with LORA_ERR_UNSUPPORTED and nothing runs.
+ *    With saved != NULL, bf16 needs about 2*r_pad*(d_out + 2*M) bytes
+ *    (r_pad = r rounded up to 16); every workload of the benchmark fits.
+ *  - No allocation: it calls no cudaMalloc/cudaFree or allocating routine.
+ *  - Set-up: the first call on each device looks up the array's device
+ *    address (with that device current) and caches it; make that first call
+ *    before any stream capture.
+ *  - Sharing: every call uses the same array.  Calls whose work overlaps on
+ *    the GPU (other streams, other host threads) race on it and give wrong
+ *    results; order them (one stream, or events).  The array keeps the last
+ *    call's contents; nothing in it needs to start at zero.
+ */
+#define LORA_NOALLOC_SCRATCH_BYTES (16u << 20) /* 16 MiB */
+lora_status_t lora_linear_bwd_noalloc(const void *dY, const void *X,
+                                      const void *W, const void *A,
+                                      const void *B, const void *saved,
+                                      float alpha, int r, int64_t M,
+                                      int64_t d_in, int64_t d_out,
+                                      lora_dtype_t dtype, void *dX, void *dA,
+                                      void *dB, void *stream);
+
 /* Human-readable name of a status code (static string). */
 const char *lora_status_string(lora_status_t status);
 

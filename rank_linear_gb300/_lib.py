@@ -27,6 +27,8 @@ SIGNATURES = {
                          _vp, _vp, _vp, _sz, _vp], _int),
     "lora_linear_bwd": ([_vp, _vp, _vp, _vp, _vp, _vp, _f32, _int, _i64, _i64, _i64, _int,
                          _vp, _vp, _vp, _vp, _sz, _vp], _int),
+    "lora_linear_bwd_noalloc": ([_vp, _vp, _vp, _vp, _vp, _vp, _f32, _int, _i64, _i64, _i64,
+                                 _int, _vp, _vp, _vp, _vp], _int),
     "lora_status_string": ([_int], ctypes.c_char_p),
     "lora_last_error": ([], ctypes.c_char_p),
     "lora_device_status": ([_int], _int),

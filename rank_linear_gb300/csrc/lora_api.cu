@@ -500,6 +500,40 @@ lora_status_t bwd_f32(const void *dY, const void *X, const void *W, const void *
 
 using namespace lora;
 
+// ---------------------------------------------------------------- no-alloc scratch
+// Built-in scratch of lora_linear_bwd_noalloc: one file-scope device array of
+// LORA_NOALLOC_SCRATCH_BYTES, held by every GPU that loads this library until
+// the process exits.  All calls share it.
+static __device__ __align__(256) unsigned char g_noalloc_scratch[LORA_NOALLOC_SCRATCH_BYTES];
+
+namespace {
+std::mutex g_noalloc_mtx;
+void *g_noalloc_ptr[lora::kMaxDevices] = {};
+
+// Device address of the scratch array on the current device.  The array's
+// name is only a host-side stand-in, so the address is looked up once per
+// device (with that device current) and cached.
+lora_status_t noalloc_scratch(void **out) {
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return lora::fail(LORA_ERR_CUDA, "cudaGetDevice: %s", cudaGetErrorString(e));
+  if (dev < 0 || dev >= lora::kMaxDevices)
+    return lora::fail(LORA_ERR_UNSUPPORTED, "device index %d", dev);
+  std::lock_guard<std::mutex> lock(g_noalloc_mtx);
+  if (g_noalloc_ptr[dev] == nullptr) {
+    void *p = nullptr;
+    e = cudaGetSymbolAddress(&p, g_noalloc_scratch);
+    if (e != cudaSuccess || p == nullptr)
+      return lora::fail(LORA_ERR_CUDA, "address of the built-in scratch: %s",
+                        cudaGetErrorString(e));
+    g_noalloc_ptr[dev] = p;
+  }
+  *out = g_noalloc_ptr[dev];
+  return LORA_OK;
+}
+}  // namespace
+
+
 extern "C" {
 
 size_t lora_linear_saved_bytes(int64_t M, int r, lora_dtype_t dtype) {
@@ -569,6 +603,40 @@ lora_status_t lora_linear_bwd(const void *dY, const void *X, const void *W, cons
   if (dtype == LORA_BF16)
     return bwd_bf16(dY, X, W, A, B, saved, alpha, r, M, d_in, d_out, dX, dA, dB, workspace, st);
   return bwd_f32(dY, X, W, A, B, saved, alpha, r, M, d_in, d_out, dX, dA, dB, workspace, st);
+}
+
+lora_status_t lora_linear_bwd_noalloc(const void *dY, const void *X, const void *W,
+                                      const void *A, const void *B, const void *saved,
+                                      float alpha, int r, int64_t M, int64_t d_in,
+                                      int64_t d_out, lora_dtype_t dtype, void *dX, void *dA,
+                                      void *dB, void *stream) {
+  t_err.clear();
+  LORA_TRY(check_shape(r, M, d_in, d_out, dtype, alpha));
+  const bool empty = M == 0;
+  LORA_TRY(check_ptr(dY, "dY", empty));
+  LORA_TRY(check_ptr(X, "X", empty));
+  LORA_TRY(check_ptr(W, "W"));
+  LORA_TRY(check_ptr(A, "A"));
+  LORA_TRY(check_ptr(B, "B"));
+  LORA_TRY(check_ptr(saved, "saved", true));
+  LORA_TRY(check_ptr(dX, "dX", true));
+  LORA_TRY(check_ptr(dA, "dA"));
+  LORA_TRY(check_ptr(dB, "dB"));
+  const Plan P = make_plan(M, d_in, d_out, r, dtype);
+  size_t need = P.bwd_ws;
+  if (saved != nullptr) need = need > P.resaved_off ? P.resaved_off : need;
+  if (empty) need = 0;
+  if (need > LORA_NOALLOC_SCRATCH_BYTES)
+    return fail(LORA_ERR_UNSUPPORTED,
+                "this shape needs %zu bytes of scratch; the built-in scratch of "
+                "lora_linear_bwd_noalloc holds %zu (use lora_linear_bwd with a workspace)",
+                need, static_cast<size_t>(LORA_NOALLOC_SCRATCH_BYTES));
+  // Nothing in the scratch has to start at zero: every byte the kernels read
+  // is written earlier in the same call.
+  void *ws = nullptr;
+  LORA_TRY(noalloc_scratch(&ws));
+  return lora_linear_bwd(dY, X, W, A, B, saved, alpha, r, M, d_in, d_out, dtype, dX, dA, dB, ws,
+                         LORA_NOALLOC_SCRATCH_BYTES, stream);
 }
 
 const char *lora_status_string(lora_status_t status) {
