@@ -4,6 +4,7 @@
 #include <cuda_bf16.h>
 
 #include "internal.h"
+#include "ptx.cuh"
 
 namespace lora {
 namespace {
@@ -15,6 +16,8 @@ constexpr int TM = 64, TN = 64, TK = 16;  // block tile; 16 x 16 threads, 4 x 4 
 __global__ void __launch_bounds__(256) k_f32_gemm(F32GemmArgs a) {
   __shared__ float As[TK][TM + 1];
   __shared__ float Bs[TK][TN + 1];
+  griddep_wait();
+  griddep_launch_dependents();
   const int tx = threadIdx.x % 16, ty = threadIdx.x / 16;
   const int m0 = blockIdx.y * TM, n0 = blockIdx.x * TN;
   float acc[4][4] = {};
@@ -57,6 +60,8 @@ __global__ void __launch_bounds__(256) k_f32_gemm(F32GemmArgs a) {
 __global__ void k_transpose_pad(const __nv_bfloat16 *__restrict__ B, int d_out, int r, int r_pad,
                                 __nv_bfloat16 *__restrict__ Bt) {
   __shared__ __nv_bfloat16 tile[32][33];
+  griddep_wait();
+  griddep_launch_dependents();
   const int o0 = blockIdx.x * 32, j0 = blockIdx.y * 32;
   for (int i = threadIdx.y; i < 32; i += 8) {
     const int o = o0 + i, j = j0 + threadIdx.x;
@@ -73,6 +78,8 @@ __global__ void k_transpose_pad(const __nv_bfloat16 *__restrict__ B, int d_out, 
 // Bp[o][j] = B[o][j] (zero for r <= j < r_pad).
 __global__ void k_pad_cols(const __nv_bfloat16 *__restrict__ B, int d_out, int r, int r_pad,
                            __nv_bfloat16 *__restrict__ Bp) {
+  griddep_wait();
+  griddep_launch_dependents();
   const int64_t total = static_cast<int64_t>(d_out) * r_pad;
   for (int64_t i = blockIdx.x * int64_t(blockDim.x) + threadIdx.x; i < total;
        i += int64_t(gridDim.x) * blockDim.x) {
@@ -82,30 +89,45 @@ __global__ void k_pad_cols(const __nv_bfloat16 *__restrict__ B, int d_out, int r
   }
 }
 
+// Launch with programmatic stream serialisation allowed (every kernel of the
+// library waits on griddep_wait before touching global memory).
+template <typename... KArgs, typename... Args>
+cudaError_t launch_pdl(void (*kern)(KArgs...), dim3 grid, dim3 block, cudaStream_t s,
+                       Args... args) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = 0;
+  cfg.stream = s;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, kern, args...);
+}
+
 }  // namespace
 
 cudaError_t launch_f32_gemm(const F32GemmArgs &a, cudaStream_t s) {
   if (a.M <= 0 || a.N <= 0) return cudaSuccess;
   dim3 grid((a.N + TN - 1) / TN, (a.M + TM - 1) / TM);
-  k_f32_gemm<<<grid, 256, 0, s>>>(a);
-  return cudaGetLastError();
+  return launch_pdl(k_f32_gemm, grid, dim3(256), s, a);
 }
 
 cudaError_t launch_transpose_pad_bf16(const void *B, int d_out, int r, int r_pad, void *Bt,
                                       cudaStream_t s) {
   dim3 grid((d_out + 31) / 32, (r_pad + 31) / 32), block(32, 8);
-  k_transpose_pad<<<grid, block, 0, s>>>(static_cast<const __nv_bfloat16 *>(B), d_out, r, r_pad,
-                                         static_cast<__nv_bfloat16 *>(Bt));
-  return cudaGetLastError();
+  return launch_pdl(k_transpose_pad, grid, block, s, static_cast<const __nv_bfloat16 *>(B), d_out,
+                    r, r_pad, static_cast<__nv_bfloat16 *>(Bt));
 }
 
 cudaError_t launch_pad_cols_bf16(const void *B, int d_out, int r, int r_pad, void *Bp,
                                  cudaStream_t s) {
   const int64_t total = static_cast<int64_t>(d_out) * r_pad;
   const int blocks = static_cast<int>(total / 256 + 1 < 4096 ? total / 256 + 1 : 4096);
-  k_pad_cols<<<blocks, 256, 0, s>>>(static_cast<const __nv_bfloat16 *>(B), d_out, r, r_pad,
-                                    static_cast<__nv_bfloat16 *>(Bp));
-  return cudaGetLastError();
+  return launch_pdl(k_pad_cols, dim3(blocks), dim3(256), s, static_cast<const __nv_bfloat16 *>(B),
+                    d_out, r, r_pad, static_cast<__nv_bfloat16 *>(Bp));
 }
 
 }  // namespace lora

@@ -98,6 +98,10 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     tma_prefetch(&tmA2);
     tma_prefetch(&tmB2);
   }
+  // Everything above touches only this CTA's shared memory; inputs, outputs
+  // and TMEM are used only after the preceding kernel has finished.
+  griddep_wait();
+  griddep_launch_dependents();
   if (warp == 1) {
     tmem_alloc(smem_u32(&tail->tmem_base), TMEM_COLS);
     tmem_relinquish();
@@ -257,10 +261,18 @@ cudaError_t launch_main_gemm(const MainGemmArgs &a, int num_sms, cudaStream_t s)
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                        static_cast<int>(SMEM_BYTES));
   if (e != cudaSuccess) return e;
-  kern<<<grid, NUM_THREADS, SMEM_BYTES, s>>>(a.tmA, a.tmB, a.tmA2, a.tmB2, a.M, a.N, a.kb_main,
-                                               a.k_ext, static_cast<__nv_bfloat16 *>(a.out), a.ldo,
-                                               a.dev_status);
-  return cudaGetLastError();
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(static_cast<unsigned>(grid), 1, 1);
+  cfg.blockDim = dim3(NUM_THREADS, 1, 1);
+  cfg.dynamicSmemBytes = SMEM_BYTES;
+  cfg.stream = s;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, kern, a.tmA, a.tmB, a.tmA2, a.tmB2, a.M, a.N, a.kb_main,
+                            a.k_ext, static_cast<__nv_bfloat16 *>(a.out), a.ldo, a.dev_status);
 }
 
 }  // namespace lora

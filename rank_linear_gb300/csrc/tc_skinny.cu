@@ -102,6 +102,10 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     tma_prefetch(&tmA);
     tma_prefetch(&tmB);
   }
+  // Only this CTA's shared memory is touched above; global data and TMEM
+  // are used only after the preceding kernel has finished.
+  griddep_wait();
+  griddep_launch_dependents();
   if (warp == 1) {
     tmem_alloc(smem_u32(&tail->tmem_base), L.tmem_cols);
     tmem_relinquish();
@@ -295,13 +299,15 @@ cudaError_t launch_skinny(const SkinnyArgs &a, int num_sms, cudaStream_t s) {
   cfg.blockDim = dim3(NUM_THREADS, 1, 1);
   cfg.dynamicSmemBytes = L.smem_bytes;
   cfg.stream = s;
-  cudaLaunchAttribute attr[1];
+  cudaLaunchAttribute attr[2];
   attr[0].id = cudaLaunchAttributeClusterDimension;
   attr[0].val.clusterDim.x = static_cast<unsigned>(S);
   attr[0].val.clusterDim.y = 1;
   attr[0].val.clusterDim.z = 1;
+  attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[1].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
-  cfg.numAttrs = 1;
+  cfg.numAttrs = 2;
   return cudaLaunchKernelEx(&cfg, kern, a.tmA, a.tmB, a.rows, a.RP, num_kb, kb_per, S, a.scale,
                             static_cast<__nv_bfloat16 *>(a.out0), a.ld0, a.n0,
                             static_cast<__nv_bfloat16 *>(a.out1), a.ld1, a.n1, a.dev_status);
