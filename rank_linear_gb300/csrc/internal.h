@@ -10,8 +10,10 @@ namespace lora {
 
 // ---- K-extended tensor-core GEMM (bf16 in, fp32 accumulate, bf16 out) ----
 //   out[m, n] = sum_{k < K1} A(m, k) B(n, k)  +  sum_{k < k_ext} A2(m, k) B2(n, k)
+// Computed in 256 x bn pair tiles (bn from main_gemm_pick_bn).
 // A / A2 are K-major [M, K] tensor maps (box 64 x 128).  B / B2 are K-major
-// [N, K] maps (box 64 x 256) or, with b_mn, MN-major [K, N] maps (box 64 x 64).
+// [N, K] maps (box 64 x bn/2) or, with b_mn, MN-major [K, N] maps
+// (box 64 x 64).
 struct MainGemmArgs {
   CUtensorMap tmA, tmB, tmA2, tmB2;
   int M = 0, N = 0;
@@ -20,10 +22,11 @@ struct MainGemmArgs {
   void *out = nullptr;
   int64_t ldo = 0;  // row pitch of out, elements
   bool b_mn = false;
+  int bn = 256;     // pair-tile width
   unsigned *dev_status = nullptr;
 };
-constexpr int kMainBM = 128, kMainBN = 256, kMainBK = 64, kMainStages = 4;
-size_t main_gemm_smem_bytes();
+constexpr int kMainBM = 128, kMainBK = 64;
+int main_gemm_pick_bn(int M, int N, int num_sms);
 cudaError_t launch_main_gemm(const MainGemmArgs &a, int num_sms, cudaStream_t s);
 
 // ---- skinny tensor-core pass with cluster split-K -------------------------

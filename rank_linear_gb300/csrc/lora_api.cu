@@ -277,10 +277,11 @@ lora_status_t fwd_bf16(const void *X, const void *W, const void *A, const void *
   }
   LORA_TRY(down_fwd_bf16(di, P, X, A, s, r, M, d_in, saved, st));
   MainGemmArgs f2;
+  f2.bn = main_gemm_pick_bn(static_cast<int>(M), static_cast<int>(d_out), di.sms);
   LORA_TRY(tmap(&f2.tmA, X, d_in, M, d_in * 2, 64, 128, "X"));
-  LORA_TRY(tmap(&f2.tmB, W, d_in, d_out, d_in * 2, 64, 256, "W"));
+  LORA_TRY(tmap(&f2.tmB, W, d_in, d_out, d_in * 2, 64, f2.bn / 2, "W"));
   LORA_TRY(tmap(&f2.tmA2, saved, P.r_pad, M, P.r_pad * 2, 64, 128, "sH"));
-  LORA_TRY(tmap(&f2.tmB2, Bsrc, b_inner, d_out, b_inner * 2, 64, 256, "B"));
+  LORA_TRY(tmap(&f2.tmB2, Bsrc, b_inner, d_out, b_inner * 2, 64, f2.bn / 2, "B"));
   f2.M = static_cast<int>(M);
   f2.N = static_cast<int>(d_out);
   f2.kb_main = static_cast<int>((d_in + 63) / 64);
@@ -349,6 +350,7 @@ lora_status_t bwd_bf16(const void *dY, const void *X, const void *W, const void 
   // dX = [dY | sG] . [W ; A]
   if (dX != nullptr) {
     MainGemmArgs b2;
+    b2.bn = main_gemm_pick_bn(static_cast<int>(M), static_cast<int>(d_in), di.sms);
     LORA_TRY(tmap(&b2.tmA, dY, d_out, M, d_out * 2, 64, 128, "dY"));
     LORA_TRY(tmap(&b2.tmB, W, d_in, d_out, d_in * 2, 64, 64, "W (MN-major)"));
     LORA_TRY(tmap(&b2.tmA2, sG, P.r_pad, M, P.r_pad * 2, 64, 128, "sG"));

@@ -11,12 +11,18 @@
 // never materialised -- the producer switches tensor maps at the segment
 // boundary.
 //
-// Structure: persistent CTAs (one per SM), 128 x 256 output tiles, 64-wide
-// K blocks in a 4-stage TMA -> shared memory ring.  Warp 0 issues TMA loads,
-// one thread of warp 1 issues tcgen05.mma into a double-buffered TMEM
-// accumulator (2 x 256 columns), warps 2-5 drain the accumulator
-// (tcgen05.ld -> bf16 -> 16-byte global stores) while the next tile's
-// main loop runs.
+// Structure: persistent CTA pairs (a cluster of two CTAs, one CTA per SM).
+// A pair owns a 256 x 256 block of the output and computes it with
+// tcgen05.mma.cta_group::2 (M = 256, N = 256, K = 16): CTA q holds the 128
+// rows of A and of the accumulator of m-block 2p+q, and 128 of the 256 rows
+// (columns of the output) of the B tile, so each SM stages only half of B.
+// 64-wide K blocks flow through a 6-stage TMA ring per CTA; both CTAs' loads
+// complete on the even CTA's barrier.  Warp 0 of each CTA issues its TMA
+// loads; one thread of warp 1 of the even CTA issues the pair MMAs into a
+// double-buffered TMEM accumulator (2 x 256 columns in each CTA) and
+// releases each stage to both CTAs with a multicast commit; warps 2-5 of
+// each CTA drain their half of the accumulator (tcgen05.ld -> bf16 ->
+// 16-byte global stores) while the next tile's main loop runs.
 #include <cuda_bf16.h>
 
 #include "internal.h"
@@ -25,35 +31,51 @@
 namespace lora {
 namespace {
 
-constexpr int BM = kMainBM, BN = kMainBN, BK = kMainBK, STAGES = kMainStages;
-constexpr uint32_t A_BYTES = BM * BK * 2;  // 16 KB
-constexpr uint32_t B_BYTES = BN * BK * 2;  // 32 KB
-constexpr uint32_t STAGE_BYTES = A_BYTES + B_BYTES;
-constexpr uint32_t TMEM_COLS = 2 * BN;  // two accumulators
-constexpr int NUM_THREADS = 192;        // producer warp, MMA warp, 4 epilogue warps
-constexpr int GROUP_M = 8;              // tile rasterisation: m-tiles per group
+constexpr int BM = kMainBM, BK = kMainBK;
+constexpr int CLUSTER = 2;                   // the CTA pair
+constexpr uint16_t PAIR_MASK = 0x3;
+constexpr uint32_t A_BYTES = BM * BK * 2;    // 16 KB: this CTA's 128 rows of A
+constexpr int NUM_THREADS = 192;             // producer warp, MMA warp, 4 epilogue warps
+constexpr int GROUP_M = 4;                   // rasterisation: m-block pairs per group
+constexpr int EPI_ARRIVALS = 4 * CLUSTER;    // epilogue warps of both CTAs
+constexpr size_t kStageBudget = 192 * 1024;  // shared memory for the stage ring
 
+// Tile geometry for a pair tile of 256 x BN (BN = 128 or 256).
+template <int BN>
+struct Geo {
+  static constexpr uint32_t B_BYTES = BN / 2 * BK * 2;  // this CTA's half of B
+  static constexpr uint32_t STAGE_BYTES = A_BYTES + B_BYTES;
+  static constexpr uint32_t PAIR_TX = CLUSTER * STAGE_BYTES;  // bytes per stage for the pair
+  static constexpr int STAGES_RAW = static_cast<int>(kStageBudget / STAGE_BYTES);
+  static constexpr int STAGES = STAGES_RAW > 8 ? 8 : STAGES_RAW;
+  static constexpr uint32_t TMEM_COLS = 2 * BN;  // two accumulators
+};
+
+template <int STAGES>
 struct __align__(8) MainTail {
-  uint64_t full[STAGES];
-  uint64_t empty[STAGES];
-  uint64_t tfull[2];
-  uint64_t tempty[2];
+  uint64_t full[STAGES];    // even CTA: both CTAs' loads of a stage landed
+  uint64_t empty[STAGES];   // each CTA: the pair MMAs finished reading a stage
+  uint64_t tfull[2];        // each CTA: an accumulator is complete
+  uint64_t tempty[2];       // even CTA: both CTAs drained an accumulator
   uint64_t drain;
   uint32_t tmem_base;
   int abort_flag;
 };
 
-constexpr size_t SMEM_BYTES = 1024 + size_t(STAGES) * STAGE_BYTES + sizeof(MainTail);
+template <int BN>
+constexpr size_t smem_bytes() {
+  return 1024 + size_t(Geo<BN>::STAGES) * Geo<BN>::STAGE_BYTES + sizeof(MainTail<Geo<BN>::STAGES>);
+}
 
-// Tile order: groups of GROUP_M m-tiles; within a group m varies fastest, so
-// the CTAs of one wave share a few A panels and a few B panels in L2.
-__device__ __forceinline__ void tile_coords(int tile, int m_tiles, int n_tiles, int &mb, int &nb) {
+// Pair-tile order: groups of GROUP_M m-pairs; within a group the m-pair
+// varies fastest, so the pairs of one wave share a few A and B panels in L2.
+__device__ __forceinline__ void tile_coords(int tile, int m_pairs, int n_tiles, int &mp, int &nb) {
   const int per_group = GROUP_M * n_tiles;
   const int g = tile / per_group;
-  const int first_m = g * GROUP_M;
-  const int gm = min(GROUP_M, m_tiles - first_m);
+  const int first = g * GROUP_M;
+  const int gm = min(GROUP_M, m_pairs - first);
   const int local = tile - g * per_group;
-  mb = first_m + local % gm;
+  mp = first + local % gm;
   nb = local / gm;
 }
 
@@ -62,33 +84,42 @@ __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
   return *reinterpret_cast<uint32_t *>(&v);
 }
 
-template <bool B_MN>
+template <bool B_MN, int BN>
 __global__ void __launch_bounds__(NUM_THREADS, 1)
     k_main_gemm(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                 const __grid_constant__ CUtensorMap tmA2, const __grid_constant__ CUtensorMap tmB2,
                 int M, int N, int kb_main, int k_ext, __nv_bfloat16 *__restrict__ out, int64_t ldo,
                 unsigned *dev_status) {
+  using G = Geo<BN>;
+  constexpr int STAGES = G::STAGES;
+  constexpr uint32_t B_BYTES = G::B_BYTES, STAGE_BYTES = G::STAGE_BYTES, PAIR_TX = G::PAIR_TX;
+  constexpr uint32_t TMEM_COLS = G::TMEM_COLS;
   extern __shared__ uint8_t smem_raw[];
   const uint32_t raw = smem_u32(smem_raw);
   const uint32_t base = (raw + 1023u) & ~1023u;  // 128-B swizzle atoms need 1 KB alignment
-  MainTail *tail = reinterpret_cast<MainTail *>(smem_raw + (base - raw) + STAGES * STAGE_BYTES);
+  auto *tail =
+      reinterpret_cast<MainTail<STAGES> *>(smem_raw + (base - raw) + STAGES * STAGE_BYTES);
   const uint32_t sA = base;
   const uint32_t sB = base + STAGES * A_BYTES;
 
   const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
+  const int q = static_cast<int>(cluster_ctarank());  // 0: even (MMA-issuing) CTA, 1: odd
+  const bool leader = q == 0;
+  const int pair_id = blockIdx.x / CLUSTER, num_pairs = gridDim.x / CLUSTER;
   const int m_tiles = (M + BM - 1) / BM, n_tiles = (N + BN - 1) / BN;
-  const int num_tiles = m_tiles * n_tiles;
+  const int m_pairs = (m_tiles + 1) / 2;
+  const int num_tiles = m_pairs * n_tiles;
   const int kb_total = kb_main + (k_ext + BK - 1) / BK;
   volatile int *abort_flag = &tail->abort_flag;
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < STAGES; ++s) {
-      mbar_init(smem_u32(&tail->full[s]), 1);
-      mbar_init(smem_u32(&tail->empty[s]), 1);
+      mbar_init(smem_u32(&tail->full[s]), 1);   // the even CTA's expect_tx arrival
+      mbar_init(smem_u32(&tail->empty[s]), 1);  // the even CTA's multicast commit
     }
     for (int a = 0; a < 2; ++a) {
       mbar_init(smem_u32(&tail->tfull[a]), 1);
-      mbar_init(smem_u32(&tail->tempty[a]), 4);
+      mbar_init(smem_u32(&tail->tempty[a]), EPI_ARRIVALS);
     }
     mbar_init(smem_u32(&tail->drain), 1);
     tail->abort_flag = 0;
@@ -98,13 +129,15 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     tma_prefetch(&tmA2);
     tma_prefetch(&tmB2);
   }
-  // Everything above touches only this CTA's shared memory; inputs, outputs
-  // and TMEM are used only after the preceding kernel has finished.
+  // Both CTAs' barriers exist before either signals the other's.
+  cluster_sync();
+  // Everything above touches only shared memory; inputs, outputs and TMEM
+  // are used only after the preceding kernel has finished.
   griddep_wait();
   griddep_launch_dependents();
   if (warp == 1) {
-    tmem_alloc(smem_u32(&tail->tmem_base), TMEM_COLS);
-    tmem_relinquish();
+    tmem_alloc_pair(smem_u32(&tail->tmem_base), TMEM_COLS);
+    tmem_relinquish_pair();
   }
   tc_fence_before();
   __syncthreads();
@@ -119,28 +152,30 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
       int stage = 0;
       uint32_t phase = 0;
       bool ok = true;
-      for (int tile = blockIdx.x; tile < num_tiles && ok; tile += gridDim.x) {
-        int mb, nb;
-        tile_coords(tile, m_tiles, n_tiles, mb, nb);
-        const int m0 = mb * BM, n0 = nb * BN;
+      for (int tile = pair_id; tile < num_tiles && ok; tile += num_pairs) {
+        int mp, nb;
+        tile_coords(tile, m_pairs, n_tiles, mp, nb);
+        const int m0 = (2 * mp + q) * BM;
+        const int n0 = nb * BN + q * (BN / 2);  // this CTA's half of the B tile
         for (int kb = 0; kb < kb_total; ++kb) {
           if (!mbar_wait(smem_u32(&tail->empty[stage]), phase ^ 1u, abort_flag, dev_status)) {
             ok = false;
             break;
           }
-          const uint32_t full = smem_u32(&tail->full[stage]);
-          mbar_expect_tx(full, STAGE_BYTES);
+          const uint32_t full_local = smem_u32(&tail->full[stage]);
+          const uint32_t full = dsmem_map(full_local, 0);  // the even CTA's barrier
+          if (leader) mbar_expect_tx(full_local, PAIR_TX);
           const bool ext = kb >= kb_main;
           const CUtensorMap *ta = ext ? &tmA2 : &tmA;
           const CUtensorMap *tb = ext ? &tmB2 : &tmB;
           const int k0 = (ext ? kb - kb_main : kb) * BK;
-          tma_load_2d(sA + stage * A_BYTES, ta, full, k0, m0);
-          if (B_MN) {
+          tma_load_2d_pair(sA + stage * A_BYTES, ta, full, k0, m0);
+          if (B_MN) {  // BN/128 boxes of [64 K x 64 N]
 #pragma unroll
-            for (int j = 0; j < BN / 64; ++j)
-              tma_load_2d(sB + stage * B_BYTES + j * 8192u, tb, full, n0 + 64 * j, k0);
-          } else {
-            tma_load_2d(sB + stage * B_BYTES, tb, full, k0, n0);
+            for (int j = 0; j < BN / 128; ++j)
+              tma_load_2d_pair(sB + stage * B_BYTES + j * 8192u, tb, full, n0 + 64 * j, k0);
+          } else {  // BN/2 rows of [N x 64 K]
+            tma_load_2d_pair(sB + stage * B_BYTES, tb, full, k0, n0);
           }
           issued[stage] += 1;
           if (++stage == STAGES) {
@@ -149,20 +184,27 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
           }
         }
       }
-      if (!ok) {  // let this CTA's copies in flight land before it exits
+      if (ok) {
+        // The pair MMAs have released every stage this CTA filled: no commit
+        // is still on its way to this CTA's barriers.
+        for (int s = 0; s < STAGES; ++s)
+          if (issued[s] && !mbar_wait(smem_u32(&tail->empty[s]), (issued[s] - 1u) & 1u,
+                                      abort_flag, dev_status))
+            break;
+      } else if (leader) {  // let the pair's copies in flight land before exiting
         for (int s = 0; s < STAGES; ++s)
           if (issued[s]) mbar_wait_drain(smem_u32(&tail->full[s]), (issued[s] - 1u) & 1u);
       }
     }
   } else if (warp == 1) {
-    // ------------------------------------------------------ MMA issuer
-    if (lane == 0) {
-      constexpr uint32_t idesc = idesc_bf16(BM, BN, false, B_MN);
+    // ------------------------------------------------------ MMA issuer (even CTA)
+    if (leader && lane == 0) {
+      constexpr uint32_t idesc = idesc_bf16(CLUSTER * BM, BN, false, B_MN);
       int stage = 0;
       uint32_t phase = 0;
       bool ok = true;
       int t = 0;
-      for (int tile = blockIdx.x; tile < num_tiles && ok; tile += gridDim.x, ++t) {
+      for (int tile = pair_id; tile < num_tiles && ok; tile += num_pairs, ++t) {
         const int acc = t & 1;
         const uint32_t use = static_cast<uint32_t>(t >> 1);
         if (!mbar_wait(smem_u32(&tail->tempty[acc]), (use & 1u) ^ 1u, abort_flag, dev_status)) {
@@ -183,36 +225,36 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
             const uint64_t ad = sdesc_sw128(a0 + kk * 32, 16, 1024);
             const uint64_t bd = B_MN ? sdesc_sw128(b0 + kk * 2048, 8192, 1024)
                                      : sdesc_sw128(b0 + kk * 32, 16, 1024);
-            tc_mma_bf16(d, ad, bd, idesc, (kb | kk) != 0 ? 1u : 0u);
+            tc_mma_bf16_pair(d, ad, bd, idesc, (kb | kk) != 0 ? 1u : 0u);
           }
-          tc_commit(smem_u32(&tail->empty[stage]));
+          tc_commit_pair_mc(smem_u32(&tail->empty[stage]), PAIR_MASK);  // free in both CTAs
           if (++stage == STAGES) {
             stage = 0;
             phase ^= 1u;
           }
         }
         if (!ok) break;
-        tc_commit(smem_u32(&tail->tfull[acc]));
+        tc_commit_pair_mc(smem_u32(&tail->tfull[acc]), PAIR_MASK);  // both halves complete
       }
       if (!ok) {  // wait for this thread's MMAs in flight before TMEM is freed
-        tc_commit(smem_u32(&tail->drain));
+        tc_commit_pair(smem_u32(&tail->drain));
         mbar_wait_drain(smem_u32(&tail->drain), 0);
       }
     }
   } else {
-    // ------------------------------------------------------ epilogue
-    const int q = warp & 3;  // TMEM lane quadrant this warp may access
+    // ------------------------------------------------------ epilogue (both CTAs)
+    const int qd = warp & 3;  // TMEM lane quadrant this warp may access
     int t = 0;
-    for (int tile = blockIdx.x; tile < num_tiles; tile += gridDim.x, ++t) {
+    for (int tile = pair_id; tile < num_tiles; tile += num_pairs, ++t) {
       const int acc = t & 1;
       const uint32_t use = static_cast<uint32_t>(t >> 1);
-      int mb, nb;
-      tile_coords(tile, m_tiles, n_tiles, mb, nb);
+      int mp, nb;
+      tile_coords(tile, m_pairs, n_tiles, mp, nb);
       const bool got = mbar_wait(smem_u32(&tail->tfull[acc]), use & 1u, abort_flag, dev_status);
       if (!__all_sync(0xffffffffu, got)) break;
       tc_fence_after();
-      const int row = mb * BM + q * 32 + lane;
-      const uint32_t taddr = tmem_base + (static_cast<uint32_t>(q * 32) << 16) + acc * BN;
+      const int row = (2 * mp + q) * BM + qd * 32 + lane;
+      const uint32_t taddr = tmem_base + (static_cast<uint32_t>(qd * 32) << 16) + acc * BN;
       __nv_bfloat16 *orow = out + static_cast<int64_t>(row) * ldo;
 #pragma unroll 1
       for (int c = 0; c < BN / 32; ++c) {
@@ -236,43 +278,97 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
       }
       tc_fence_before();
       __syncwarp();
-      if (lane == 0) mbar_arrive(smem_u32(&tail->tempty[acc]));
+      if (lane == 0) mbar_arrive_cluster(dsmem_map(smem_u32(&tail->tempty[acc]), 0));
     }
   }
 
+  // Both CTAs are done with TMEM and with each other's barriers before the
+  // collective deallocation; neither leaves while the other may still
+  // touch its shared memory.
   __syncthreads();
+  tc_fence_before();
+  cluster_sync();
   if (warp == 1) {
-    __syncwarp();
     tc_fence_after();
-    tmem_dealloc(tmem_base, TMEM_COLS);
+    tmem_dealloc_pair(tmem_base, TMEM_COLS);
   }
+}
+
+template <bool B_MN, int BN>
+constexpr auto kernel_of() {
+  return &k_main_gemm<B_MN, BN>;
+}
+
+int g_max_clusters[64][2] = {};
+
+// Largest number of two-CTA clusters of a kernel variant that can be
+// resident at once (queried once per device; the variant's shared-memory
+// attribute must already be set).
+template <bool B_MN, int BN>
+int max_clusters(int num_sms) {
+  int dev = 0;
+  cudaGetDevice(&dev);
+  int &n = g_max_clusters[dev & 63][B_MN ? 1 : 0];
+  if (n == 0) {
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(static_cast<unsigned>(num_sms / CLUSTER * CLUSTER), 1, 1);
+    cfg.blockDim = dim3(NUM_THREADS, 1, 1);
+    cfg.dynamicSmemBytes = smem_bytes<BN>();
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = CLUSTER;
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    int c = 0;
+    if (cudaOccupancyMaxActiveClusters(&c, kernel_of<B_MN, BN>(), &cfg) != cudaSuccess || c < 1) {
+      cudaGetLastError();  // clear; fall back to one cluster per SM pair
+      c = num_sms / CLUSTER;
+    }
+    n = c;
+  }
+  return n;
+}
+
+template <bool B_MN, int BN>
+cudaError_t launch_variant(const MainGemmArgs &a, int num_sms, cudaStream_t s) {
+  const int m_tiles = (a.M + BM - 1) / BM, n_tiles = (a.N + BN - 1) / BN;
+  const int tiles = ((m_tiles + 1) / 2) * n_tiles;  // pair tiles
+  if (tiles == 0) return cudaSuccess;
+  auto kern = kernel_of<B_MN, BN>();
+  constexpr size_t smem = smem_bytes<BN>();
+  cudaError_t e =
+      cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));
+  if (e != cudaSuccess) return e;
+  const int maxc = max_clusters<B_MN, BN>(num_sms);
+  const int clusters = tiles < maxc ? tiles : maxc;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(static_cast<unsigned>(clusters * CLUSTER), 1, 1);
+  cfg.blockDim = dim3(NUM_THREADS, 1, 1);
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = s;
+  cudaLaunchAttribute attr[2];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = CLUSTER;
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[1].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 2;
+  return cudaLaunchKernelEx(&cfg, kern, a.tmA, a.tmB, a.tmA2, a.tmB2, a.M, a.N, a.kb_main,
+                            a.k_ext, static_cast<__nv_bfloat16 *>(a.out), a.ldo, a.dev_status);
 }
 
 }  // namespace
 
-size_t main_gemm_smem_bytes() { return SMEM_BYTES; }
+// Pair-tile width.  256 is the only width built: 128-wide pair tiles ran at
+// well under half the tensor rate of 256-wide ones on GB300.
+int main_gemm_pick_bn(int, int, int) { return 256; }
 
 cudaError_t launch_main_gemm(const MainGemmArgs &a, int num_sms, cudaStream_t s) {
-  const int m_tiles = (a.M + BM - 1) / BM, n_tiles = (a.N + BN - 1) / BN;
-  const int tiles = m_tiles * n_tiles;
-  if (tiles == 0) return cudaSuccess;
-  const int grid = tiles < num_sms ? tiles : num_sms;
-  auto kern = a.b_mn ? k_main_gemm<true> : k_main_gemm<false>;
-  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                       static_cast<int>(SMEM_BYTES));
-  if (e != cudaSuccess) return e;
-  cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = dim3(static_cast<unsigned>(grid), 1, 1);
-  cfg.blockDim = dim3(NUM_THREADS, 1, 1);
-  cfg.dynamicSmemBytes = SMEM_BYTES;
-  cfg.stream = s;
-  cudaLaunchAttribute attr[1];
-  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
-  attr[0].val.programmaticStreamSerializationAllowed = 1;
-  cfg.attrs = attr;
-  cfg.numAttrs = 1;
-  return cudaLaunchKernelEx(&cfg, kern, a.tmA, a.tmB, a.tmA2, a.tmB2, a.M, a.N, a.kb_main,
-                            a.k_ext, static_cast<__nv_bfloat16 *>(a.out), a.ldo, a.dev_status);
+  return a.b_mn ? launch_variant<true, 256>(a, num_sms, s) : launch_variant<false, 256>(a, num_sms, s);
 }
 
 }  // namespace lora
