@@ -58,11 +58,14 @@ def kernel_work(kind, M, d_in, d_out, r):
                      e * (M * d_out + d_out * d_in + M * r + r * d_in + M * d_in)),
         "grad_a": (2 * M * d_in * r, e * (M * d_in + M * r + r * d_in)),
         "grad_b": (2 * M * d_out * r, e * (M * d_out + M * r + d_out * r)),
+        # s dY B and dY^T sH in one launch; dY counted once
+        "down_bwd_grad_b": (4 * M * d_out * r,
+                            e * (M * d_out + r * d_out + 2 * M * r + d_out * r)),
     }[kind]
 
 
 BOUND = {"prep": "hbm", "down_fwd": "hbm", "down_bwd": "hbm", "grad_a": "hbm",
-         "grad_b": "hbm", "main_fwd": "tensor", "main_bwd": "tensor"}
+         "grad_b": "hbm", "down_bwd_grad_b": "hbm", "main_fwd": "tensor", "main_bwd": "tensor"}
 
 
 def load_peaks():

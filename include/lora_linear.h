@@ -190,7 +190,8 @@ typedef enum {
     LORA_K_DOWN_BWD = 3,  /* s dY B              (skinny, HBM-bound)         */
     LORA_K_MAIN_BWD = 4,  /* [dY|sdYB][W;A]      (K-extended GEMM)           */
     LORA_K_GRAD_A = 5,    /* dA = (s dY B)^T X   (skinny split-K)            */
-    LORA_K_GRAD_B = 6     /* dB = dY^T (s X A^T) (skinny split-K)            */
+    LORA_K_GRAD_B = 6,    /* dB = dY^T (s X A^T) (skinny split-K)            */
+    LORA_K_DOWN_BWD_GRAD_B = 7  /* s dY B and dB in one launch (both read dY) */
 } lora_kernel_kind_t;
 
 /*

@@ -15,7 +15,8 @@ LIB_PATH = os.path.join(HERE, "liblora_linear.so")
 LORA_OK, LORA_ERR_INVALID_ARG, LORA_ERR_UNSUPPORTED, LORA_ERR_WORKSPACE, \
     LORA_ERR_CUDA, LORA_ERR_TIMEOUT = range(6)
 LORA_BF16, LORA_FP32 = 0, 1
-KERNEL_KINDS = ["prep", "down_fwd", "main_fwd", "down_bwd", "main_bwd", "grad_a", "grad_b"]
+KERNEL_KINDS = ["prep", "down_fwd", "main_fwd", "down_bwd", "main_bwd", "grad_a", "grad_b",
+                "down_bwd_grad_b"]
 
 _vp, _i64, _sz = ctypes.c_void_p, ctypes.c_int64, ctypes.c_size_t
 _int, _f32 = ctypes.c_int, ctypes.c_float

@@ -30,16 +30,18 @@ int main_gemm_pick_bn(int M, int N, int num_sms);
 cudaError_t launch_main_gemm(const MainGemmArgs &a, int num_sms, cudaStream_t s);
 
 // ---- skinny tensor-core pass with cluster split-K -------------------------
-//   acc[row, j] = sum_k A(row, k) B(j, k),  row < rows, j < RP (RP = N of the MMA)
+//   acc[row, j] = sum_k A(row, k) B(j, k),  row < rows, j < RP (RP = r_pad)
 //   out0[row * ld0 + j] = bf16(scale * acc)  for j < n0   (row-major, optional)
 //   out1[j * ld1 + row] = bf16(scale * acc)  for j < n1   (transposed, optional)
 // A is K-major [rows, K] (box 64 x 128) or, with a_mn, MN-major [K, rows]
-// (box 64 x 64); B is K-major [RP, K] (box 64 x RP).  The K range is split
-// over the CTAs of a cluster whose partial sums meet in distributed shared
-// memory and are added in cluster-rank order.
+// (box 64 x 64).  B is K-major [RP, K] (box 64 x RP) or, with b_mn,
+// MN-major [K, >= 1 columns] (box 64 x 64; columns past the tensor read as
+// zero and the MMA runs on whole 64-wide column blocks).  The K range is
+// split over the CTAs of a cluster whose partial sums meet in distributed
+// shared memory and are added in cluster-rank order.
 struct SkinnyArgs {
   CUtensorMap tmA, tmB;
-  bool a_mn = false;
+  bool a_mn = false, b_mn = false;
   int rows = 0, RP = 16, K = 0;
   float scale = 1.f;
   void *out0 = nullptr;
@@ -50,7 +52,8 @@ struct SkinnyArgs {
   int n1 = 0;
   unsigned *dev_status = nullptr;
 };
-cudaError_t launch_skinny(const SkinnyArgs &a, int num_sms, cudaStream_t s);
+// Runs one or two independent problems in one launch.
+cudaError_t launch_skinny(const SkinnyArgs *probs, int nprob, int num_sms, cudaStream_t s);
 int skinny_split(int rows, int K, int num_sms);
 
 // ---- fp32 CUDA-core GEMM (debug dtype) ------------------------------------

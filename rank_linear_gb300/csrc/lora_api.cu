@@ -56,6 +56,11 @@ lora_status_t device_info(DevInfo &out) {
   cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return fail(LORA_ERR_CUDA, "cudaGetDevice: %s", cudaGetErrorString(e));
   if (dev < 0 || dev >= kMaxDevices) return fail(LORA_ERR_UNSUPPORTED, "device index %d", dev);
+  // Make the device's primary context current on this host thread (a fresh
+  // thread, e.g. an autograd worker, may have none yet); the driver's
+  // tensor-map encoder needs it.
+  e = cudaSetDevice(dev);
+  if (e != cudaSuccess) return fail(LORA_ERR_CUDA, "cudaSetDevice: %s", cudaGetErrorString(e));
   std::lock_guard<std::mutex> lock(g_mtx);
   DevInfo &d = g_dev[dev];
   if (!d.init) {
@@ -255,7 +260,7 @@ lora_status_t down_fwd_bf16(const DevInfo &di, const Plan &P, const void *X, con
   f1.ld1 = P.Mp;
   f1.n1 = P.r_pad;
   f1.dev_status = di.status;
-  return run(LORA_K_DOWN_FWD, st, "s X A^T pass", [&] { return launch_skinny(f1, di.sms, st); });
+  return run(LORA_K_DOWN_FWD, st, "s X A^T pass", [&] { return launch_skinny(&f1, 1, di.sms, st); });
 }
 
 lora_status_t fwd_bf16(const void *X, const void *W, const void *A, const void *B, float alpha,
@@ -306,18 +311,24 @@ lora_status_t bwd_bf16(const void *dY, const void *X, const void *W, const void 
     saved = re;
   }
   const void *sHt = static_cast<const uint8_t *>(saved) + P.sHt_off;
-  void *Bt = at(ws, P.bt_off);
   void *sG = at(ws, P.sg_off);
   void *sGt = at(ws, P.sgt_off);
 
-  LORA_TRY(run(LORA_K_PREP, st, "transpose B", [&] {
-    return launch_transpose_pad_bf16(B, static_cast<int>(d_out), r, P.r_pad, Bt, st);
-  }));
-
-  // sG = s dY B, and its transpose
-  SkinnyArgs b1;
+  // sG = s dY B (and its transpose), and dB = dY^T sH: one launch, both read dY
+  SkinnyArgs g[2];
+  SkinnyArgs &b1 = g[0];
   LORA_TRY(tmap(&b1.tmA, dY, d_out, M, d_out * 2, 64, 128, "dY"));
-  LORA_TRY(tmap(&b1.tmB, Bt, d_out, P.r_pad, d_out * 2, 64, P.r_pad, "B^T"));
+  if (r % 8 == 0) {  // B [d_out, r] read directly as an MN-major operand
+    LORA_TRY(tmap(&b1.tmB, B, r, d_out, int64_t(r) * 2, 64, 64, "B (MN-major)"));
+    b1.b_mn = true;
+  } else {  // B's row pitch is not a multiple of 16 bytes: transpose it first
+    void *Bt = at(ws, P.bt_off);
+    LORA_TRY(run(LORA_K_PREP, st, "transpose B", [&] {
+      return launch_transpose_pad_bf16(B, static_cast<int>(d_out), r, P.r_pad, Bt, st);
+    }));
+    LORA_TRY(tmap(&b1.tmB, Bt, d_out, P.r_pad, d_out * 2, 64, P.r_pad, "B^T"));
+    b1.b_mn = false;
+  }
   b1.a_mn = false;
   b1.rows = static_cast<int>(M);
   b1.RP = P.r_pad;
@@ -330,10 +341,8 @@ lora_status_t bwd_bf16(const void *dY, const void *X, const void *W, const void 
   b1.ld1 = P.Mp;
   b1.n1 = P.r_pad;
   b1.dev_status = di.status;
-  LORA_TRY(run(LORA_K_DOWN_BWD, st, "s dY B pass", [&] { return launch_skinny(b1, di.sms, st); }));
 
-  // dB = dY^T sH   (rows = d_out, K = tokens)
-  SkinnyArgs b4;
+  SkinnyArgs &b4 = g[1];  // dB = dY^T sH   (rows = d_out, K = tokens)
   LORA_TRY(tmap(&b4.tmA, dY, d_out, M, d_out * 2, 64, 64, "dY^T"));
   LORA_TRY(tmap(&b4.tmB, sHt, M, P.r_pad, P.Mp * 2, 64, P.r_pad, "sH^T"));
   b4.a_mn = true;
@@ -345,7 +354,8 @@ lora_status_t bwd_bf16(const void *dY, const void *X, const void *W, const void 
   b4.ld0 = r;
   b4.n0 = r;
   b4.dev_status = di.status;
-  LORA_TRY(run(LORA_K_GRAD_B, st, "dB pass", [&] { return launch_skinny(b4, di.sms, st); }));
+  LORA_TRY(run(LORA_K_DOWN_BWD_GRAD_B, st, "s dY B and dB pass",
+               [&] { return launch_skinny(g, 2, di.sms, st); }));
 
   // dX = [dY | sG] . [W ; A]
   if (dX != nullptr) {
@@ -379,7 +389,7 @@ lora_status_t bwd_bf16(const void *dY, const void *X, const void *W, const void 
   b3.ld1 = d_in;
   b3.n1 = r;
   b3.dev_status = di.status;
-  return run(LORA_K_GRAD_A, st, "dA pass", [&] { return launch_skinny(b3, di.sms, st); });
+  return run(LORA_K_GRAD_A, st, "dA pass", [&] { return launch_skinny(&b3, 1, di.sms, st); });
 }
 
 // ---------------------------------------------------------------- fp32 path

@@ -4,7 +4,8 @@
 // LoRA", §5.3 have one side of width r and are bound by the HBM read of the
 // wide operand:
 //     forward   sH  = s X A^T           rows = tokens, K = d_in   (A K-major)
-//     backward  sG  = s dY B            rows = tokens, K = d_out  (A K-major)
+//     backward  sG  = s dY B            rows = tokens, K = d_out  (A K-major,
+//                                                                   B MN-major)
 //               dA^T = X^T sG           rows = d_in,   K = tokens (A MN-major)
 //               dB   = dY^T sH          rows = d_out,  K = tokens (A MN-major)
 // (the last two are the dL/dA and dL/dB of the fused backward's gradient
@@ -16,7 +17,9 @@
 // shared memory, and after a cluster barrier CTA c adds rows
 // [c*128/S, (c+1)*128/S) of all S partials in rank order through
 // distributed shared memory.  The order is fixed, so results are bitwise
-// reproducible and no partials touch HBM.
+// reproducible and no partials touch HBM.  One launch may carry two
+// independent problems (e.g. s dY B and dY^T sH, which both stream dY):
+// the first CTAs of the grid work on problem 0, the rest on problem 1.
 #include <cuda_bf16.h>
 
 #include "internal.h"
@@ -40,6 +43,29 @@ struct __align__(8) SkinnyTail {
   int abort_flag;
 };
 
+// Per-problem scalars (the tensor maps travel as separate kernel arguments).
+struct Prob {
+  int rows = 0, K = 0;
+  int num_kb = 0, kb_per = 0, ctas = 0;
+  int a_mn = 0, b_mn = 0;
+  int RP = 16;   // N of the MMA
+  int RK = 16;   // accumulator columns kept (<= RP, multiple of 16)
+  float scale = 1.f;
+  __nv_bfloat16 *out0 = nullptr;
+  int64_t ld0 = 0;
+  int n0 = 0;
+  __nv_bfloat16 *out1 = nullptr;
+  int64_t ld1 = 0;
+  int n1 = 0;
+};
+
+struct Params {
+  Prob p[2];
+  int nprob = 1;
+  int S = 1;
+  unsigned *dev_status = nullptr;
+};
+
 struct SkinnyLayout {
   int stages;
   uint32_t b_bytes, pipe_bytes, red_bytes, region_bytes;
@@ -47,7 +73,7 @@ struct SkinnyLayout {
   uint32_t tmem_cols;
 };
 
-__host__ __device__ inline SkinnyLayout skinny_layout(int RP) {
+__host__ __device__ inline SkinnyLayout skinny_layout(int RP, int RK) {
   SkinnyLayout L;
   L.b_bytes = static_cast<uint32_t>(RP) * BK * 2;
   const uint32_t stage_bytes = A_BYTES + L.b_bytes;
@@ -55,7 +81,7 @@ __host__ __device__ inline SkinnyLayout skinny_layout(int RP) {
   st = st < 2 ? 2 : (st > MAX_STAGES ? MAX_STAGES : st);
   L.stages = st;
   L.pipe_bytes = st * stage_bytes;
-  L.red_bytes = BM * (RP + 4) * 4;  // fp32 partial, row pitch RP + 4 floats
+  L.red_bytes = BM * (RK + 4) * 4;  // fp32 partial, row pitch RK + 4 floats
   L.region_bytes = L.pipe_bytes > L.red_bytes ? L.pipe_bytes : L.red_bytes;
   L.smem_bytes = 1024 + L.region_bytes + sizeof(SkinnyTail);
   uint32_t c = 32;
@@ -64,14 +90,22 @@ __host__ __device__ inline SkinnyLayout skinny_layout(int RP) {
   return L;
 }
 
-template <bool A_MN>
 __global__ void __launch_bounds__(NUM_THREADS, 1)
-    k_skinny(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
-             int rows, int RP, int num_kb, int kb_per, int S, float scale,
-             __nv_bfloat16 *__restrict__ out0, int64_t ld0, int n0,
-             __nv_bfloat16 *__restrict__ out1, int64_t ld1, int n1, unsigned *dev_status) {
+    k_skinny(const __grid_constant__ CUtensorMap tmA0, const __grid_constant__ CUtensorMap tmB0,
+             const __grid_constant__ CUtensorMap tmA1, const __grid_constant__ CUtensorMap tmB1,
+             const __grid_constant__ Params P) {
+  const int S = P.S;
+  const int which = (P.nprob > 1 && static_cast<int>(blockIdx.x) >= P.p[0].ctas) ? 1 : 0;
+  const Prob &pr = P.p[which];
+  const CUtensorMap *tmA = which ? &tmA1 : &tmA0;
+  const CUtensorMap *tmB = which ? &tmB1 : &tmB0;
+  const int block = static_cast<int>(blockIdx.x) - (which ? P.p[0].ctas : 0);
+  const int RP = pr.RP, RK = pr.RK;
+  const bool a_mn = pr.a_mn != 0, b_mn = pr.b_mn != 0;
+  unsigned *dev_status = P.dev_status;
+
   extern __shared__ uint8_t smem_raw[];
-  const SkinnyLayout L = skinny_layout(RP);
+  const SkinnyLayout L = skinny_layout(RP, RK);
   const uint32_t raw = smem_u32(smem_raw);
   const uint32_t base = (raw + 1023u) & ~1023u;
   uint8_t *base_ptr = smem_raw + (base - raw);
@@ -80,13 +114,13 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
   const uint32_t sA = base;
   const uint32_t sB = base + L.stages * A_BYTES;
   const int STAGES = L.stages;
-  const int pitch = RP + 4;
+  const int pitch = RK + 4;
 
   const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
   const int rank = static_cast<int>(cluster_ctarank());
-  const int m0 = (blockIdx.x / S) * BM;
-  const int kb_begin = rank * kb_per;
-  const int kb_end = min(num_kb, kb_begin + kb_per);
+  const int m0 = (block / S) * BM;
+  const int kb_begin = rank * pr.kb_per;
+  const int kb_end = min(pr.num_kb, kb_begin + pr.kb_per);
   const bool has_k = kb_end > kb_begin;
   volatile int *abort_flag = &tail->abort_flag;
 
@@ -99,8 +133,8 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     mbar_init(smem_u32(&tail->drain), 1);
     tail->abort_flag = 0;
     fence_barrier_init();
-    tma_prefetch(&tmA);
-    tma_prefetch(&tmB);
+    tma_prefetch(tmA);
+    tma_prefetch(tmB);
   }
   // Only this CTA's shared memory is touched above; global data and TMEM
   // are used only after the preceding kernel has finished.
@@ -132,13 +166,18 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         const uint32_t full = smem_u32(&tail->full[stage]);
         mbar_expect_tx(full, tx);
         const int k0 = kb * BK;
-        if (A_MN) {  // A^T stored [K][rows]: two 64-wide boxes of rows
-          tma_load_2d(sA + stage * A_BYTES, &tmA, full, m0, k0);
-          tma_load_2d(sA + stage * A_BYTES + 8192u, &tmA, full, m0 + 64, k0);
+        const uint32_t a_dst = sA + stage * A_BYTES, b_dst = sB + stage * L.b_bytes;
+        if (a_mn) {  // A^T stored [K][rows]: two 64-wide boxes of rows
+          tma_load_2d(a_dst, tmA, full, m0, k0);
+          tma_load_2d(a_dst + 8192u, tmA, full, m0 + 64, k0);
         } else {
-          tma_load_2d(sA + stage * A_BYTES, &tmA, full, k0, m0);
+          tma_load_2d(a_dst, tmA, full, k0, m0);
         }
-        tma_load_2d(sB + stage * L.b_bytes, &tmB, full, k0, 0);
+        if (b_mn) {  // B stored [K][N]: RP/64 boxes of 64 columns
+          for (int j = 0; j < RP / 64; ++j) tma_load_2d(b_dst + j * 8192u, tmB, full, 64 * j, k0);
+        } else {
+          tma_load_2d(b_dst, tmB, full, k0, 0);
+        }
         issued[stage] += 1;
         if (++stage == STAGES) {
           stage = 0;
@@ -153,7 +192,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
   } else if (warp == 1) {
     // ------------------------------------------------------ MMA issuer
     if (lane == 0) {
-      const uint32_t idesc = idesc_bf16(BM, static_cast<uint32_t>(RP), A_MN, false);
+      const uint32_t idesc = idesc_bf16(BM, static_cast<uint32_t>(RP), a_mn, b_mn);
       int stage = 0;
       uint32_t phase = 0;
       bool ok = true;
@@ -166,9 +205,10 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         const uint32_t a0 = sA + stage * A_BYTES, b0 = sB + stage * L.b_bytes;
 #pragma unroll
         for (int kk = 0; kk < BK / 16; ++kk) {
-          const uint64_t ad = A_MN ? sdesc_sw128(a0 + kk * 2048, 8192, 1024)
+          const uint64_t ad = a_mn ? sdesc_sw128(a0 + kk * 2048, 8192, 1024)
                                    : sdesc_sw128(a0 + kk * 32, 16, 1024);
-          const uint64_t bd = sdesc_sw128(b0 + kk * 32, 16, 1024);
+          const uint64_t bd = b_mn ? sdesc_sw128(b0 + kk * 2048, 8192, 1024)
+                                   : sdesc_sw128(b0 + kk * 32, 16, 1024);
           tc_mma_bf16(tmem_base, ad, bd, idesc, (kb > kb_begin || kk > 0) ? 1u : 0u);
         }
         tc_commit(smem_u32(&tail->empty[stage]));
@@ -194,7 +234,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
       const int rl = q * 32 + lane;
       float4 *dst = reinterpret_cast<float4 *>(red + rl * pitch);
       const uint32_t taddr = tmem_base + (static_cast<uint32_t>(q * 32) << 16);
-      for (int c = 0; c < RP / 16; ++c) {
+      for (int c = 0; c < RK / 16; ++c) {
         float v[16];
         tmem_ld_16cols(taddr + c * 16, v);
         if (!has_k) {
@@ -213,9 +253,9 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
   cluster_sync();  // every CTA's partial is in its shared memory
   const int R = BM / S;
   const int r_lo = rank * R;
-  const int c4n = RP / 4;
+  const int c4n = RK / 4;
   const uint32_t red_addr = smem_u32(red);
-  const bool vec0 = (ld0 % 4 == 0) && (n0 % 4 == 0);
+  const bool vec0 = (pr.ld0 % 4 == 0) && (pr.n0 % 4 == 0);
   for (int e = threadIdx.x; e < R * c4n; e += NUM_THREADS) {
     const int rl = r_lo + e / c4n;
     const int c4 = e % c4n;
@@ -228,16 +268,16 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
       acc.z += v.z;
       acc.w += v.w;
     }
-    acc.x *= scale;
-    acc.y *= scale;
-    acc.z *= scale;
-    acc.w *= scale;
+    acc.x *= pr.scale;
+    acc.y *= pr.scale;
+    acc.z *= pr.scale;
+    acc.w *= pr.scale;
     *reinterpret_cast<float4 *>(red + rl * pitch + c4 * 4) = acc;  // own slice only
     const int row = m0 + rl;
-    if (out0 != nullptr && row < rows) {
+    if (pr.out0 != nullptr && row < pr.rows) {
       const int c = c4 * 4;
-      __nv_bfloat16 *o = out0 + static_cast<int64_t>(row) * ld0 + c;
-      if (vec0 && c + 4 <= n0) {
+      __nv_bfloat16 *o = pr.out0 + static_cast<int64_t>(row) * pr.ld0 + c;
+      if (vec0 && c + 4 <= pr.n0) {
         __nv_bfloat162 lo = __floats2bfloat162_rn(acc.x, acc.y);
         __nv_bfloat162 hi = __floats2bfloat162_rn(acc.z, acc.w);
         uint2 pk;
@@ -247,19 +287,19 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
       } else {
         const float vv[4] = {acc.x, acc.y, acc.z, acc.w};
         for (int i = 0; i < 4; ++i)
-          if (c + i < n0) o[i] = __float2bfloat16_rn(vv[i]);
+          if (c + i < pr.n0) o[i] = __float2bfloat16_rn(vv[i]);
       }
     }
   }
   cluster_sync();  // peers are done reading this CTA's shared memory
 
-  if (out1 != nullptr) {  // transposed copy: consecutive threads, consecutive rows
-    for (int e = threadIdx.x; e < R * n1; e += NUM_THREADS) {
+  if (pr.out1 != nullptr) {  // transposed copy: consecutive threads, consecutive rows
+    for (int e = threadIdx.x; e < R * pr.n1; e += NUM_THREADS) {
       const int j = e / R;
       const int rl = r_lo + e % R;
       const int row = m0 + rl;
-      if (row < rows)
-        out1[static_cast<int64_t>(j) * ld1 + row] = __float2bfloat16_rn(red[rl * pitch + j]);
+      if (row < pr.rows)
+        pr.out1[static_cast<int64_t>(j) * pr.ld1 + row] = __float2bfloat16_rn(red[rl * pitch + j]);
     }
   }
 
@@ -269,6 +309,27 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     tc_fence_after();
     tmem_dealloc(tmem_base, L.tmem_cols);
   }
+}
+
+Prob to_prob(const SkinnyArgs &a, int S) {
+  Prob p;
+  p.rows = a.rows;
+  p.K = a.K;
+  p.num_kb = (a.K + BK - 1) / BK;
+  p.kb_per = (p.num_kb + S - 1) / S;
+  p.ctas = ((a.rows + BM - 1) / BM) * S;
+  p.a_mn = a.a_mn ? 1 : 0;
+  p.b_mn = a.b_mn ? 1 : 0;
+  p.RK = a.RP;
+  p.RP = a.b_mn ? (a.RP + 63) / 64 * 64 : a.RP;  // MN-major B: whole 64-wide atoms
+  p.scale = a.scale;
+  p.out0 = static_cast<__nv_bfloat16 *>(a.out0);
+  p.ld0 = a.ld0;
+  p.n0 = a.n0;
+  p.out1 = static_cast<__nv_bfloat16 *>(a.out1);
+  p.ld1 = a.ld1;
+  p.n1 = a.n1;
+  return p;
 }
 
 }  // namespace
@@ -283,21 +344,40 @@ int skinny_split(int rows, int K, int num_sms) {
   return S;
 }
 
-cudaError_t launch_skinny(const SkinnyArgs &a, int num_sms, cudaStream_t s) {
-  if (a.rows <= 0) return cudaSuccess;
-  const SkinnyLayout L = skinny_layout(a.RP);
-  const int mt = (a.rows + BM - 1) / BM;
-  const int num_kb = (a.K + BK - 1) / BK;
-  const int S = skinny_split(a.rows, a.K, num_sms);
-  const int kb_per = (num_kb + S - 1) / S;
-  auto kern = a.a_mn ? k_skinny<true> : k_skinny<false>;
-  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                       static_cast<int>(L.smem_bytes));
+cudaError_t launch_skinny(const SkinnyArgs *probs, int nprob, int num_sms, cudaStream_t s) {
+  Params P;
+  P.nprob = 0;
+  const SkinnyArgs *use[2] = {nullptr, nullptr};
+  for (int i = 0; i < nprob; ++i)
+    if (probs[i].rows > 0) use[P.nprob++] = &probs[i];
+  if (P.nprob == 0) return cudaSuccess;
+  // one cluster size for the whole launch: the smaller of the problems' own
+  int S = 8;
+  int total_rows_ctas = 0;
+  for (int i = 0; i < P.nprob; ++i) {
+    const int rows_all = use[i]->rows;
+    const int si = skinny_split(rows_all, use[i]->K, num_sms);
+    S = si < S ? si : S;
+    total_rows_ctas += (rows_all + BM - 1) / BM;
+  }
+  (void)total_rows_ctas;
+  P.S = S;
+  size_t smem = 0;
+  unsigned grid = 0;
+  for (int i = 0; i < P.nprob; ++i) {
+    P.p[i] = to_prob(*use[i], S);
+    const SkinnyLayout L = skinny_layout(P.p[i].RP, P.p[i].RK);
+    smem = L.smem_bytes > smem ? L.smem_bytes : smem;
+    grid += static_cast<unsigned>(P.p[i].ctas);
+  }
+  P.dev_status = use[0]->dev_status;
+  cudaError_t e = cudaFuncSetAttribute(k_skinny, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                       static_cast<int>(smem));
   if (e != cudaSuccess) return e;
   cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = dim3(static_cast<unsigned>(mt * S), 1, 1);
+  cfg.gridDim = dim3(grid, 1, 1);
   cfg.blockDim = dim3(NUM_THREADS, 1, 1);
-  cfg.dynamicSmemBytes = L.smem_bytes;
+  cfg.dynamicSmemBytes = smem;
   cfg.stream = s;
   cudaLaunchAttribute attr[2];
   attr[0].id = cudaLaunchAttributeClusterDimension;
@@ -308,9 +388,9 @@ cudaError_t launch_skinny(const SkinnyArgs &a, int num_sms, cudaStream_t s) {
   attr[1].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 2;
-  return cudaLaunchKernelEx(&cfg, kern, a.tmA, a.tmB, a.rows, a.RP, num_kb, kb_per, S, a.scale,
-                            static_cast<__nv_bfloat16 *>(a.out0), a.ld0, a.n0,
-                            static_cast<__nv_bfloat16 *>(a.out1), a.ld1, a.n1, a.dev_status);
+  const CUtensorMap &a1 = P.nprob > 1 ? use[1]->tmA : use[0]->tmA;
+  const CUtensorMap &b1 = P.nprob > 1 ? use[1]->tmB : use[0]->tmB;
+  return cudaLaunchKernelEx(&cfg, k_skinny, use[0]->tmA, use[0]->tmB, a1, b1, P);
 }
 
 }  // namespace lora

@@ -197,9 +197,9 @@ def test_timing_hook_records_every_launch():
     used = L.lora_timing_used()
     L.lora_set_timing_events(None, None, 0)
     torch.cuda.synchronize()
-    assert used == rl.launch_count() - n0 == 7
+    assert used == rl.launch_count() - n0 == 5
     assert [_lib.KERNEL_KINDS[k] for k in kinds[:used]] == [
-        "down_fwd", "main_fwd", "prep", "down_bwd", "grad_b", "main_bwd", "grad_a"]
+        "down_fwd", "main_fwd", "down_bwd_grad_b", "main_bwd", "grad_a"]
     for j in range(used):
         assert evs[2 * j].elapsed_time(evs[2 * j + 1]) > 0
 
