@@ -23,10 +23,26 @@ struct MainGemmArgs {
   int64_t ldo = 0;  // row pitch of out, elements
   bool b_mn = false;
   int bn = 256;     // pair-tile width
+  // Split of the last, partial wave (see main_gemm_split): its split_rem
+  // tiles are computed as split_k K-ranges each, on different pairs, whose
+  // fp32 partials meet in `partials`; `counters` (2 * split_rem words) must
+  // be zero when the kernel starts.
+  int split_k = 1, split_rem = 0;
+  float *partials = nullptr;
+  unsigned *counters = nullptr;
   unsigned *dev_status = nullptr;
 };
 constexpr int kMainBM = 128, kMainBK = 64;
 int main_gemm_pick_bn(int M, int N, int num_sms);
+// Number of CTA pairs the main GEMM runs on (resident clusters of two).
+int main_gemm_pairs(bool b_mn, int num_sms);
+struct MainSplit {
+  int k = 1, rem = 0;
+  size_t partial_bytes = 0, counter_bytes = 0;
+};
+// Tail split for an M x N output on `pairs` CTA pairs: the last wave's rem
+// tiles are split two ways (K ranges) when 2 * rem <= pairs.
+MainSplit main_gemm_split(int M, int N, int pairs);
 cudaError_t launch_main_gemm(const MainGemmArgs &a, int num_sms, cudaStream_t s);
 
 // ---- skinny tensor-core pass with cluster split-K -------------------------
@@ -40,6 +56,10 @@ cudaError_t launch_main_gemm(const MainGemmArgs &a, int num_sms, cudaStream_t s)
 // split over the CTAs of a cluster whose partial sums meet in distributed
 // shared memory and are added in cluster-rank order.
 struct SkinnyArgs {
+  // optional: zero `zero_words` 32-bit words at `zero_ptr` (the next main
+  // GEMM's split counters) once the preceding kernel has finished
+  unsigned *zero_ptr = nullptr;
+  int zero_words = 0;
   CUtensorMap tmA, tmB;
   bool a_mn = false, b_mn = false;
   int rows = 0, RP = 16, K = 0;

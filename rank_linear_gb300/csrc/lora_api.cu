@@ -151,6 +151,8 @@ lora_status_t run(lora_kernel_kind_t kind, cudaStream_t s, const char *what, F &
 int64_t rup(int64_t x, int64_t m) { return (x + m - 1) / m * m; }
 
 // Byte layout of the saved buffer and of the workspace for one shape.
+// The main GEMMs' tail-split region is optional: fwd_ws_min / bwd_ws_min
+// leave it out, fwd_ws / bwd_ws include it (when the shape splits at all).
 struct Plan {
   int r_pad = 0;     // bf16: r rounded up to 16 (K step of the MMA)
   int64_t Mp = 0;    // bf16: M rounded up to 8 (16-byte pitch of the transposed copies)
@@ -158,11 +160,13 @@ struct Plan {
   size_t sHt_off = 0;
   // workspace offsets
   size_t bpad_off = 0, bt_off = 0, sg_off = 0, sgt_off = 0, resaved_off = 0;
-  size_t fwd_ws = 0, bwd_ws = 0;
+  size_t fsplit_off = 0, fcnt_off = 0, bsplit_off = 0, bcnt_off = 0;
+  MainSplit fsplit, bsplit;
+  size_t fwd_ws = 0, bwd_ws = 0, fwd_ws_min = 0, bwd_ws_min = 0;
 };
 
-Plan make_plan(int64_t M, int64_t d_in, int64_t d_out, int r, lora_dtype_t dt) {
-  (void)d_in;
+// pairs: CTA pairs of the main GEMM on the target device (0: no tail split).
+Plan make_plan(int64_t M, int64_t d_in, int64_t d_out, int r, lora_dtype_t dt, int pairs = 0) {
   Plan P;
   if (dt == LORA_BF16) {
     P.r_pad = static_cast<int>(rup(r, 16));
@@ -170,17 +174,33 @@ Plan make_plan(int64_t M, int64_t d_in, int64_t d_out, int r, lora_dtype_t dt) {
     const size_t sH = size_t(M) * P.r_pad * 2;
     P.sHt_off = rup(sH, 256);
     P.saved = M > 0 ? P.sHt_off + size_t(P.r_pad) * P.Mp * 2 : 0;
-    P.fwd_ws = (r % 8) ? rup(size_t(d_out) * P.r_pad * 2, 256) : 0;
-    size_t off = 0;
+    // forward: [B padded (r % 8 != 0)] [split partials] [split counters]
+    size_t off = (r % 8) ? rup(size_t(d_out) * P.r_pad * 2, 256) : 0;
+    P.fwd_ws_min = off;
+    if (pairs > 0 && M > 0) P.fsplit = main_gemm_split(int(M), int(d_out), pairs);
+    P.fsplit_off = off;
+    off += rup(P.fsplit.partial_bytes, 256);
+    P.fcnt_off = off;
+    off += rup(P.fsplit.counter_bytes, 256);
+    P.fwd_ws = P.fsplit.k > 1 ? off : P.fwd_ws_min;
+    // backward: [B^T] [sG] [sG^T] [split partials] [split counters] [recomputed saved]
+    off = 0;
     P.bt_off = off;
     off += rup(size_t(P.r_pad) * d_out * 2, 256);
     P.sg_off = off;
     off += rup(size_t(M) * P.r_pad * 2, 256);
     P.sgt_off = off;
     off += rup(size_t(P.r_pad) * P.Mp * 2, 256);
+    const size_t base_end = off;
+    if (pairs > 0 && M > 0) P.bsplit = main_gemm_split(int(M), int(d_in), pairs);
+    P.bsplit_off = off;
+    off += rup(P.bsplit.partial_bytes, 256);
+    P.bcnt_off = off;
+    off += rup(P.bsplit.counter_bytes, 256);
     P.resaved_off = off;
     off += rup(P.saved, 256);
     P.bwd_ws = M > 0 ? off : 0;
+    P.bwd_ws_min = M > 0 ? base_end : 0;  // with a saved buffer and no tail split
   } else {
     P.r_pad = r;
     P.Mp = M;
@@ -189,6 +209,7 @@ Plan make_plan(int64_t M, int64_t d_in, int64_t d_out, int r, lora_dtype_t dt) {
     P.sg_off = 0;
     P.resaved_off = rup(size_t(M) * r * 4, 256);
     P.bwd_ws = M > 0 ? P.resaved_off + rup(P.saved, 256) : 0;
+    P.bwd_ws_min = M > 0 ? P.resaved_off : 0;
   }
   return P;
 }
@@ -244,8 +265,10 @@ uint8_t *at(void *base, size_t off) { return static_cast<uint8_t *>(base) + off;
 // sH = s X A^T into saved (row-major [M][r_pad]) and its transpose.
 lora_status_t down_fwd_bf16(const DevInfo &di, const Plan &P, const void *X, const void *A,
                             float s, int r, int64_t M, int64_t d_in, void *saved,
-                            cudaStream_t st) {
+                            cudaStream_t st, unsigned *zero_ptr = nullptr, int zero_words = 0) {
   SkinnyArgs f1;
+  f1.zero_ptr = zero_ptr;
+  f1.zero_words = zero_words;
   LORA_TRY(tmap(&f1.tmA, X, d_in, M, d_in * 2, 64, 128, "X"));
   LORA_TRY(tmap(&f1.tmB, A, d_in, r, d_in * 2, 64, P.r_pad, "A"));
   f1.a_mn = false;
@@ -265,10 +288,13 @@ lora_status_t down_fwd_bf16(const DevInfo &di, const Plan &P, const void *X, con
 
 lora_status_t fwd_bf16(const void *X, const void *W, const void *A, const void *B, float alpha,
                        int r, int64_t M, int64_t d_in, int64_t d_out, void *Y, void *saved,
-                       void *ws, cudaStream_t st) {
+                       void *ws, size_t ws_bytes, cudaStream_t st) {
   DevInfo di;
   LORA_TRY(device_info(di));
-  const Plan P = make_plan(M, d_in, d_out, r, LORA_BF16);
+  Plan P = make_plan(M, d_in, d_out, r, LORA_BF16, main_gemm_pairs(false, di.sms));
+  const bool split = P.fsplit.k > 1 && ws != nullptr && ws_bytes >= P.fwd_ws;
+  if (!split) P = make_plan(M, d_in, d_out, r, LORA_BF16);  // layout without the split region
+  unsigned *counters = split ? reinterpret_cast<unsigned *>(at(ws, P.fcnt_off)) : nullptr;
   const float s = alpha / static_cast<float>(r);
   const void *Bsrc = B;
   int64_t b_inner = r;
@@ -280,8 +306,15 @@ lora_status_t fwd_bf16(const void *X, const void *W, const void *A, const void *
     Bsrc = Bp;
     b_inner = P.r_pad;
   }
-  LORA_TRY(down_fwd_bf16(di, P, X, A, s, r, M, d_in, saved, st));
+  LORA_TRY(down_fwd_bf16(di, P, X, A, s, r, M, d_in, saved, st, counters,
+                         split ? 2 * P.fsplit.rem : 0));
   MainGemmArgs f2;
+  if (split) {
+    f2.split_k = P.fsplit.k;
+    f2.split_rem = P.fsplit.rem;
+    f2.partials = reinterpret_cast<float *>(at(ws, P.fsplit_off));
+    f2.counters = counters;
+  }
   f2.bn = main_gemm_pick_bn(static_cast<int>(M), static_cast<int>(d_out), di.sms);
   LORA_TRY(tmap(&f2.tmA, X, d_in, M, d_in * 2, 64, 128, "X"));
   LORA_TRY(tmap(&f2.tmB, W, d_in, d_out, d_in * 2, 64, f2.bn / 2, "W"));
@@ -300,10 +333,17 @@ lora_status_t fwd_bf16(const void *X, const void *W, const void *A, const void *
 
 lora_status_t bwd_bf16(const void *dY, const void *X, const void *W, const void *A, const void *B,
                        const void *saved, float alpha, int r, int64_t M, int64_t d_in,
-                       int64_t d_out, void *dX, void *dA, void *dB, void *ws, cudaStream_t st) {
+                       int64_t d_out, void *dX, void *dA, void *dB, void *ws, size_t ws_bytes,
+                       cudaStream_t st) {
   DevInfo di;
   LORA_TRY(device_info(di));
-  const Plan P = make_plan(M, d_in, d_out, r, LORA_BF16);
+  Plan P = make_plan(M, d_in, d_out, r, LORA_BF16, main_gemm_pairs(true, di.sms));
+  // tail split of the dX GEMM only if the workspace holds its region (it sits
+  // before the recompute room, so a saved buffer lets a shorter one suffice)
+  const bool split = dX != nullptr && P.bsplit.k > 1 && ws != nullptr &&
+                     ws_bytes >= (saved != nullptr ? P.resaved_off : P.bwd_ws);
+  if (!split) P = make_plan(M, d_in, d_out, r, LORA_BF16);  // layout without the split region
+  unsigned *counters = split ? reinterpret_cast<unsigned *>(at(ws, P.bcnt_off)) : nullptr;
   const float s = alpha / static_cast<float>(r);
   if (saved == nullptr) {  // recompute s X A^T into the workspace
     void *re = at(ws, P.resaved_off);
@@ -341,6 +381,8 @@ lora_status_t bwd_bf16(const void *dY, const void *X, const void *W, const void 
   b1.ld1 = P.Mp;
   b1.n1 = P.r_pad;
   b1.dev_status = di.status;
+  b1.zero_ptr = counters;  // the dX GEMM's split counters
+  b1.zero_words = split ? 2 * P.bsplit.rem : 0;
 
   SkinnyArgs &b4 = g[1];  // dB = dY^T sH   (rows = d_out, K = tokens)
   LORA_TRY(tmap(&b4.tmA, dY, d_out, M, d_out * 2, 64, 64, "dY^T"));
@@ -373,6 +415,12 @@ lora_status_t bwd_bf16(const void *dY, const void *X, const void *W, const void 
     b2.ldo = d_in;
     b2.b_mn = true;
     b2.dev_status = di.status;
+    if (split) {
+      b2.split_k = P.bsplit.k;
+      b2.split_rem = P.bsplit.rem;
+      b2.partials = reinterpret_cast<float *>(at(ws, P.bsplit_off));
+      b2.counters = counters;
+    }
     LORA_TRY(run(LORA_K_MAIN_BWD, st, "dX GEMM", [&] { return launch_main_gemm(b2, di.sms, st); }));
   }
 
@@ -558,7 +606,20 @@ size_t lora_linear_workspace_bytes(int64_t M, int64_t d_in, int64_t d_out, int r
   if (M < 0 || d_in < 1 || d_out < 1 || r < 1 || r > 256 ||
       (dtype != LORA_BF16 && dtype != LORA_FP32))
     return 0;
-  const Plan P = make_plan(M, d_in, d_out, r, dtype);
+  // sized for the current device (its number of main-GEMM CTA pairs); with
+  // no usable device, for a GB300's 76 pairs
+  int pairs = 76;
+  if (dtype == LORA_BF16) {
+    int dev = 0, sms = 0, major = 0, minor = 0;
+    if (cudaGetDevice(&dev) == cudaSuccess &&
+        cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) == cudaSuccess &&
+        cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev) == cudaSuccess &&
+        cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev) == cudaSuccess &&
+        major == 10 && minor == 3)
+      pairs = main_gemm_pairs(false, sms);
+    cudaGetLastError();
+  }
+  const Plan P = make_plan(M, d_in, d_out, r, dtype, pairs);
   return P.fwd_ws > P.bwd_ws ? P.fwd_ws : P.bwd_ws;
 }
 
@@ -576,10 +637,11 @@ lora_status_t lora_linear_fwd(const void *X, const void *W, const void *A, const
   LORA_TRY(check_ptr(Y, "Y", empty));
   LORA_TRY(check_ptr(saved, "saved", empty));
   const Plan P = make_plan(M, d_in, d_out, r, dtype);
-  LORA_TRY(check_ws(workspace, workspace_bytes, P.fwd_ws));
+  LORA_TRY(check_ws(workspace, workspace_bytes, P.fwd_ws_min));
   if (empty) return LORA_OK;
   cudaStream_t st = static_cast<cudaStream_t>(stream);
-  if (dtype == LORA_BF16) return fwd_bf16(X, W, A, B, alpha, r, M, d_in, d_out, Y, saved, workspace, st);
+  if (dtype == LORA_BF16)
+    return fwd_bf16(X, W, A, B, alpha, r, M, d_in, d_out, Y, saved, workspace, workspace_bytes, st);
   return fwd_f32(X, W, A, B, alpha, r, M, d_in, d_out, Y, saved, st);
 }
 
@@ -600,8 +662,7 @@ lora_status_t lora_linear_bwd(const void *dY, const void *X, const void *W, cons
   LORA_TRY(check_ptr(dA, "dA"));
   LORA_TRY(check_ptr(dB, "dB"));
   const Plan P = make_plan(M, d_in, d_out, r, dtype);
-  size_t need = P.bwd_ws;
-  if (saved != nullptr) need = need > P.resaved_off ? P.resaved_off : need;  // no recompute room
+  size_t need = saved != nullptr ? P.bwd_ws_min : P.bwd_ws;  // recompute room if no saved
   if (empty) need = 0;
   LORA_TRY(check_ws(workspace, workspace_bytes, need));
   cudaStream_t st = static_cast<cudaStream_t>(stream);
@@ -613,7 +674,8 @@ lora_status_t lora_linear_bwd(const void *dY, const void *X, const void *W, cons
     return LORA_OK;
   }
   if (dtype == LORA_BF16)
-    return bwd_bf16(dY, X, W, A, B, saved, alpha, r, M, d_in, d_out, dX, dA, dB, workspace, st);
+    return bwd_bf16(dY, X, W, A, B, saved, alpha, r, M, d_in, d_out, dX, dA, dB, workspace,
+                    workspace_bytes, st);
   return bwd_f32(dY, X, W, A, B, saved, alpha, r, M, d_in, d_out, dX, dA, dB, workspace, st);
 }
 
@@ -635,8 +697,7 @@ lora_status_t lora_linear_bwd_noalloc(const void *dY, const void *X, const void 
   LORA_TRY(check_ptr(dA, "dA"));
   LORA_TRY(check_ptr(dB, "dB"));
   const Plan P = make_plan(M, d_in, d_out, r, dtype);
-  size_t need = P.bwd_ws;
-  if (saved != nullptr) need = need > P.resaved_off ? P.resaved_off : need;
+  size_t need = saved != nullptr ? P.bwd_ws_min : P.bwd_ws;
   if (empty) need = 0;
   if (need > LORA_NOALLOC_SCRATCH_BYTES)
     return fail(LORA_ERR_UNSUPPORTED,

@@ -23,6 +23,14 @@
 // releases each stage to both CTAs with a multicast commit; warps 2-5 of
 // each CTA drain their half of the accumulator (tcgen05.ld -> bf16 ->
 // 16-byte global stores) while the next tile's main loop runs.
+//
+// Tail split: when the last wave would leave at least half the pairs idle
+// (rem tiles on P >= 2 rem pairs), those rem tiles are computed as two
+// K-ranges each, on two different pairs.  Each range's CTA writes its fp32
+// partial to `partials` (column-major, so a warp's stores coalesce) and
+// counts itself in; the CTA that arrives second adds the other partial to
+// its own, still in TMEM, and writes the bf16 tile.  fp32 addition of two
+// terms is commutative, so the result does not depend on who is second.
 #include <cuda_bf16.h>
 
 #include "internal.h"
@@ -58,13 +66,36 @@ struct __align__(8) MainTail {
   uint64_t tfull[2];        // each CTA: an accumulator is complete
   uint64_t tempty[2];       // even CTA: both CTAs drained an accumulator
   uint64_t drain;
+  uint64_t ebar;            // each CTA: the four epilogue warps meet (tail split)
   uint32_t tmem_base;
   int abort_flag;
+  int split_last;
 };
 
 template <int BN>
 constexpr size_t smem_bytes() {
   return 1024 + size_t(Geo<BN>::STAGES) * Geo<BN>::STAGE_BYTES + sizeof(MainTail<Geo<BN>::STAGES>);
+}
+
+// Work item -> tile and K-block range.  Items below split_first are whole
+// tiles; the rest are range `chunk` of split tile `rel` (tile split_first+rel).
+__device__ __forceinline__ void item_range(int item, int split_first, int split_k, int split_rem,
+                                           int kb_total, int &tile, int &kb_lo, int &kb_hi,
+                                           int &chunk, int &rel) {
+  if (item < split_first) {
+    tile = item;
+    kb_lo = 0;
+    kb_hi = kb_total;
+    chunk = 0;
+    rel = 0;
+  } else {
+    const int u = item - split_first;
+    rel = u % split_rem;
+    chunk = u / split_rem;
+    tile = split_first + rel;
+    kb_lo = chunk * kb_total / split_k;
+    kb_hi = (chunk + 1) * kb_total / split_k;
+  }
 }
 
 // Pair-tile order: groups of GROUP_M m-pairs; within a group the m-pair
@@ -84,11 +115,12 @@ __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
   return *reinterpret_cast<uint32_t *>(&v);
 }
 
-template <bool B_MN, int BN>
+template <bool B_MN, int BN, bool SPLIT>
 __global__ void __launch_bounds__(NUM_THREADS, 1)
     k_main_gemm(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                 const __grid_constant__ CUtensorMap tmA2, const __grid_constant__ CUtensorMap tmB2,
                 int M, int N, int kb_main, int k_ext, __nv_bfloat16 *__restrict__ out, int64_t ldo,
+                int split_k, int split_rem, float *__restrict__ partials, unsigned *counters,
                 unsigned *dev_status) {
   using G = Geo<BN>;
   constexpr int STAGES = G::STAGES;
@@ -110,6 +142,14 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
   const int m_pairs = (m_tiles + 1) / 2;
   const int num_tiles = m_pairs * n_tiles;
   const int kb_total = kb_main + (k_ext + BK - 1) / BK;
+  // work items: whole tiles [0, split_first), then split_k ranges of each of
+  // the last split_rem tiles
+  if (!SPLIT) {  // the lean instantiation runs whole tiles only
+    split_k = 1;
+    split_rem = 0;
+  }
+  const int split_first = num_tiles - split_rem;
+  const int num_items = split_first + split_k * split_rem;
   volatile int *abort_flag = &tail->abort_flag;
 
   if (threadIdx.x == 0) {
@@ -122,6 +162,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
       mbar_init(smem_u32(&tail->tempty[a]), EPI_ARRIVALS);
     }
     mbar_init(smem_u32(&tail->drain), 1);
+    mbar_init(smem_u32(&tail->ebar), 4);
     tail->abort_flag = 0;
     fence_barrier_init();
     tma_prefetch(&tmA);
@@ -131,9 +172,13 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
   }
   // Both CTAs' barriers exist before either signals the other's.
   cluster_sync();
-  // Everything above touches only shared memory; inputs, outputs and TMEM
-  // are used only after the preceding kernel has finished.
-  griddep_wait();
+  // Programmatic dependent launch.  The preceding kernel in the stream (the
+  // skinny pass producing sH or sG) waited for its own predecessor before
+  // letting this grid start, so everything this kernel reads except the
+  // low-rank operand of the K extension is already final, and nothing this
+  // kernel writes is read by it.  Only the producer waits, right before its
+  // first load of the extension; the main K segment overlaps the tail of
+  // the preceding kernel.
   griddep_launch_dependents();
   if (warp == 1) {
     tmem_alloc_pair(smem_u32(&tail->tmem_base), TMEM_COLS);
@@ -152,12 +197,15 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
       int stage = 0;
       uint32_t phase = 0;
       bool ok = true;
-      for (int tile = pair_id; tile < num_tiles && ok; tile += num_pairs) {
+      bool dep_done = false;
+      for (int item = pair_id; item < num_items && ok; item += num_pairs) {
+        int tile, kb_lo, kb_hi, chunk, rel;
+        item_range(item, split_first, split_k, split_rem, kb_total, tile, kb_lo, kb_hi, chunk, rel);
         int mp, nb;
         tile_coords(tile, m_pairs, n_tiles, mp, nb);
         const int m0 = (2 * mp + q) * BM;
         const int n0 = nb * BN + q * (BN / 2);  // this CTA's half of the B tile
-        for (int kb = 0; kb < kb_total; ++kb) {
+        for (int kb = kb_lo; kb < kb_hi; ++kb) {
           if (!mbar_wait(smem_u32(&tail->empty[stage]), phase ^ 1u, abort_flag, dev_status)) {
             ok = false;
             break;
@@ -166,6 +214,10 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
           const uint32_t full = dsmem_map(full_local, 0);  // the even CTA's barrier
           if (leader) mbar_expect_tx(full_local, PAIR_TX);
           const bool ext = kb >= kb_main;
+          if (ext && !dep_done) {  // sH / sG come from the preceding kernel
+            griddep_wait();
+            dep_done = true;
+          }
           const CUtensorMap *ta = ext ? &tmA2 : &tmA;
           const CUtensorMap *tb = ext ? &tmB2 : &tmB;
           const int k0 = (ext ? kb - kb_main : kb) * BK;
@@ -204,7 +256,9 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
       uint32_t phase = 0;
       bool ok = true;
       int t = 0;
-      for (int tile = pair_id; tile < num_tiles && ok; tile += num_pairs, ++t) {
+      for (int item = pair_id; item < num_items && ok; item += num_pairs, ++t) {
+        int tile, kb_lo, kb_hi, chunk, rel;
+        item_range(item, split_first, split_k, split_rem, kb_total, tile, kb_lo, kb_hi, chunk, rel);
         const int acc = t & 1;
         const uint32_t use = static_cast<uint32_t>(t >> 1);
         if (!mbar_wait(smem_u32(&tail->tempty[acc]), (use & 1u) ^ 1u, abort_flag, dev_status)) {
@@ -213,7 +267,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         }
         tc_fence_after();
         const uint32_t d = tmem_base + acc * BN;
-        for (int kb = 0; kb < kb_total; ++kb) {
+        for (int kb = kb_lo; kb < kb_hi; ++kb) {
           if (!mbar_wait(smem_u32(&tail->full[stage]), phase, abort_flag, dev_status)) {
             ok = false;
             break;
@@ -225,7 +279,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
             const uint64_t ad = sdesc_sw128(a0 + kk * 32, 16, 1024);
             const uint64_t bd = B_MN ? sdesc_sw128(b0 + kk * 2048, 8192, 1024)
                                      : sdesc_sw128(b0 + kk * 32, 16, 1024);
-            tc_mma_bf16_pair(d, ad, bd, idesc, (kb | kk) != 0 ? 1u : 0u);
+            tc_mma_bf16_pair(d, ad, bd, idesc, (kb > kb_lo || kk != 0) ? 1u : 0u);
           }
           tc_commit_pair_mc(smem_u32(&tail->empty[stage]), PAIR_MASK);  // free in both CTAs
           if (++stage == STAGES) {
@@ -244,8 +298,23 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
   } else {
     // ------------------------------------------------------ epilogue (both CTAs)
     const int qd = warp & 3;  // TMEM lane quadrant this warp may access
+    const int et = threadIdx.x - 64;  // 0..127 across the four epilogue warps
+    int *last_flag = &tail->split_last;
+    bool dep_done = false;
+    uint32_t eph = 0;  // phase of ebar (the same sequence in every epilogue thread)
+    // Bounded barrier among the four epilogue warps; false if it gave up.
+    auto epi_sync = [&]() -> bool {
+      __syncwarp();
+      if (lane == 0) mbar_arrive(smem_u32(&tail->ebar));
+      const bool okw = mbar_wait(smem_u32(&tail->ebar), eph, abort_flag, dev_status);
+      eph ^= 1u;
+      return __all_sync(0xffffffffu, okw);
+    };
     int t = 0;
-    for (int tile = pair_id; tile < num_tiles; tile += num_pairs, ++t) {
+    for (int item = pair_id; item < num_items; item += num_pairs, ++t) {
+      int tile, kb_lo, kb_hi, chunk, rel;
+      item_range(item, split_first, split_k, split_rem, kb_total, tile, kb_lo, kb_hi, chunk, rel);
+      const bool split = SPLIT && item >= split_first;
       const int acc = t & 1;
       const uint32_t use = static_cast<uint32_t>(t >> 1);
       int mp, nb;
@@ -253,32 +322,94 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
       const bool got = mbar_wait(smem_u32(&tail->tfull[acc]), use & 1u, abort_flag, dev_status);
       if (!__all_sync(0xffffffffu, got)) break;
       tc_fence_after();
-      const int row = (2 * mp + q) * BM + qd * 32 + lane;
+      const int rl = qd * 32 + lane;  // row within this CTA's 128
+      const int row = (2 * mp + q) * BM + rl;
       const uint32_t taddr = tmem_base + (static_cast<uint32_t>(qd * 32) << 16) + acc * BN;
       __nv_bfloat16 *orow = out + static_cast<int64_t>(row) * ldo;
+      if (!SPLIT || !split) {
+#pragma unroll 1
+        for (int c = 0; c < BN / 32; ++c) {
+          float v[32];
+          tmem_ld_32cols(taddr + c * 32, v);
+          const int col0 = nb * BN + c * 32;
+          if (row < M) {
+#pragma unroll
+            for (int g = 0; g < 4; ++g) {
+              const int col = col0 + g * 8;
+              if (col < N) {  // N is a multiple of 8: a group is all in or all out
+                uint4 pk;
+                pk.x = pack_bf16x2(v[g * 8 + 0], v[g * 8 + 1]);
+                pk.y = pack_bf16x2(v[g * 8 + 2], v[g * 8 + 3]);
+                pk.z = pack_bf16x2(v[g * 8 + 4], v[g * 8 + 5]);
+                pk.w = pack_bf16x2(v[g * 8 + 6], v[g * 8 + 7]);
+                *reinterpret_cast<uint4 *>(orow + col) = pk;
+              }
+            }
+          }
+        }
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive_cluster(dsmem_map(smem_u32(&tail->tempty[acc]), 0));
+        continue;
+      }
+      if constexpr (SPLIT) {
+
+      // ---- tail-split item (the last item of this pair): write the partial
+      // [col][row] fp32, count in; the second to arrive adds the other one.
+      // The accumulator is released only at the end (no item follows).
+      float *slot_mine = partials + static_cast<size_t>((rel * 2 + chunk) * 2 + q) * BM * BN;
+      float *slot_other = partials + static_cast<size_t>((rel * 2 + (chunk ^ 1)) * 2 + q) * BM * BN;
 #pragma unroll 1
       for (int c = 0; c < BN / 32; ++c) {
         float v[32];
         tmem_ld_32cols(taddr + c * 32, v);
-        const int col0 = nb * BN + c * 32;
-        if (row < M) {
 #pragma unroll
-          for (int g = 0; g < 4; ++g) {
-            const int col = col0 + g * 8;
-            if (col < N) {  // N is a multiple of 8: a group is all in or all out
-              uint4 pk;
-              pk.x = pack_bf16x2(v[g * 8 + 0], v[g * 8 + 1]);
-              pk.y = pack_bf16x2(v[g * 8 + 2], v[g * 8 + 3]);
-              pk.z = pack_bf16x2(v[g * 8 + 4], v[g * 8 + 5]);
-              pk.w = pack_bf16x2(v[g * 8 + 6], v[g * 8 + 7]);
-              *reinterpret_cast<uint4 *>(orow + col) = pk;
+        for (int i = 0; i < 32; ++i) slot_mine[(c * 32 + i) * BM + rl] = v[i];
+      }
+      if (!dep_done) {  // the counters were zeroed by the preceding kernel
+        griddep_wait();
+        dep_done = true;
+      }
+      __threadfence();            // this thread's partial is visible GPU-wide
+      bool sync_ok = epi_sync();  // ... and so are the other 127 threads'
+      if (sync_ok && et == 0) {
+        const unsigned prev = atomicAdd(&counters[rel * 2 + q], 1u);
+        *last_flag = (prev == 1u) ? 1 : 0;
+      }
+      sync_ok = sync_ok && epi_sync();
+      const bool last = sync_ok && *reinterpret_cast<volatile int *>(last_flag) != 0;
+      if (last) {
+        __threadfence();
+#pragma unroll 1
+        for (int c = 0; c < BN / 32; ++c) {
+          float o[32];
+#pragma unroll
+          for (int i = 0; i < 32; ++i) o[i] = __ldcg(slot_other + (c * 32 + i) * BM + rl);
+          float v[32];
+          tmem_ld_32cols(taddr + c * 32, v);
+          const int col0 = nb * BN + c * 32;
+          if (row < M) {
+#pragma unroll
+            for (int g = 0; g < 4; ++g) {
+              const int col = col0 + g * 8;
+              if (col < N) {
+                uint4 pk;
+                pk.x = pack_bf16x2(v[g * 8 + 0] + o[g * 8 + 0], v[g * 8 + 1] + o[g * 8 + 1]);
+                pk.y = pack_bf16x2(v[g * 8 + 2] + o[g * 8 + 2], v[g * 8 + 3] + o[g * 8 + 3]);
+                pk.z = pack_bf16x2(v[g * 8 + 4] + o[g * 8 + 4], v[g * 8 + 5] + o[g * 8 + 5]);
+                pk.w = pack_bf16x2(v[g * 8 + 6] + o[g * 8 + 6], v[g * 8 + 7] + o[g * 8 + 7]);
+                *reinterpret_cast<uint4 *>(orow + col) = pk;
+              }
             }
           }
         }
       }
+      if (sync_ok) sync_ok = epi_sync();  // the flag word is free again
       tc_fence_before();
       __syncwarp();
       if (lane == 0) mbar_arrive_cluster(dsmem_map(smem_u32(&tail->tempty[acc]), 0));
+      if (!sync_ok) break;
+      }  // SPLIT
     }
   }
 
@@ -294,9 +425,9 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
   }
 }
 
-template <bool B_MN, int BN>
+template <bool B_MN, int BN, bool SPLIT>
 constexpr auto kernel_of() {
-  return &k_main_gemm<B_MN, BN>;
+  return &k_main_gemm<B_MN, BN, SPLIT>;
 }
 
 int g_max_clusters[64][2] = {};
@@ -322,7 +453,8 @@ int max_clusters(int num_sms) {
     cfg.attrs = attr;
     cfg.numAttrs = 1;
     int c = 0;
-    if (cudaOccupancyMaxActiveClusters(&c, kernel_of<B_MN, BN>(), &cfg) != cudaSuccess || c < 1) {
+    if (cudaOccupancyMaxActiveClusters(&c, kernel_of<B_MN, BN, false>(), &cfg) != cudaSuccess ||
+        c < 1) {
       cudaGetLastError();  // clear; fall back to one cluster per SM pair
       c = num_sms / CLUSTER;
     }
@@ -331,12 +463,12 @@ int max_clusters(int num_sms) {
   return n;
 }
 
-template <bool B_MN, int BN>
+template <bool B_MN, int BN, bool SPLIT>
 cudaError_t launch_variant(const MainGemmArgs &a, int num_sms, cudaStream_t s) {
   const int m_tiles = (a.M + BM - 1) / BM, n_tiles = (a.N + BN - 1) / BN;
   const int tiles = ((m_tiles + 1) / 2) * n_tiles;  // pair tiles
   if (tiles == 0) return cudaSuccess;
-  auto kern = kernel_of<B_MN, BN>();
+  auto kern = kernel_of<B_MN, BN, SPLIT>();
   constexpr size_t smem = smem_bytes<BN>();
   cudaError_t e =
       cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));
@@ -358,17 +490,47 @@ cudaError_t launch_variant(const MainGemmArgs &a, int num_sms, cudaStream_t s) {
   cfg.attrs = attr;
   cfg.numAttrs = 2;
   return cudaLaunchKernelEx(&cfg, kern, a.tmA, a.tmB, a.tmA2, a.tmB2, a.M, a.N, a.kb_main,
-                            a.k_ext, static_cast<__nv_bfloat16 *>(a.out), a.ldo, a.dev_status);
+                            a.k_ext, static_cast<__nv_bfloat16 *>(a.out), a.ldo, a.split_k,
+                            a.split_rem, a.partials, a.counters, a.dev_status);
 }
 
 }  // namespace
+
+int main_gemm_pairs(bool b_mn, int num_sms) {
+  // the shared-memory attribute must be set before the occupancy query
+  auto kern = b_mn ? kernel_of<true, 256, false>() : kernel_of<false, 256, false>();
+  cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                       static_cast<int>(smem_bytes<256>()));
+  return b_mn ? max_clusters<true, 256>(num_sms) : max_clusters<false, 256>(num_sms);
+}
+
+MainSplit main_gemm_split(int M, int N, int pairs) {
+  MainSplit sp;
+  if (pairs < 2) return sp;
+  const int m_pairs = ((M + BM - 1) / BM + 1) / 2;
+  const int tiles = m_pairs * ((N + 255) / 256);
+  const int rem = tiles % pairs;
+  if (tiles <= pairs || rem == 0) return sp;  // one partial wave only, or none
+  if (2 * rem > pairs) return sp;  // splitting would not shorten the last wave
+  const int k = 2;
+  sp.k = k;
+  sp.rem = rem;
+  sp.partial_bytes = static_cast<size_t>(rem) * k * 2 * BM * 256 * sizeof(float);
+  sp.counter_bytes = static_cast<size_t>(rem) * 2 * sizeof(unsigned);
+  return sp;
+}
 
 // Pair-tile width.  256 is the only width built: 128-wide pair tiles ran at
 // well under half the tensor rate of 256-wide ones on GB300.
 int main_gemm_pick_bn(int, int, int) { return 256; }
 
 cudaError_t launch_main_gemm(const MainGemmArgs &a, int num_sms, cudaStream_t s) {
-  return a.b_mn ? launch_variant<true, 256>(a, num_sms, s) : launch_variant<false, 256>(a, num_sms, s);
+  const bool split = a.split_k > 1 && a.split_rem > 0;
+  if (a.b_mn)
+    return split ? launch_variant<true, 256, true>(a, num_sms, s)
+                 : launch_variant<true, 256, false>(a, num_sms, s);
+  return split ? launch_variant<false, 256, true>(a, num_sms, s)
+               : launch_variant<false, 256, false>(a, num_sms, s);
 }
 
 }  // namespace lora

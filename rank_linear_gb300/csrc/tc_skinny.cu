@@ -13,10 +13,11 @@
 //
 // One CTA owns 128 output rows and one slice of K.  The S CTAs that share
 // the rows form a thread-block cluster: each accumulates its slice with
-// tcgen05.mma (M = 128, N = RP) into TMEM, stages the fp32 partial in its
-// shared memory, and after a cluster barrier CTA c adds rows
-// [c*128/S, (c+1)*128/S) of all S partials in rank order through
-// distributed shared memory.  The order is fixed, so results are bitwise
+// tcgen05.mma (M = 128, N = RP) into TMEM; CTA c then adds rows
+// [c*128/S, (c+1)*128/S) of all S fp32 partials in rank order.  Narrow
+// accumulators (RP <= 64) are pushed into the owning CTA's staging area over
+// distributed shared memory before one cluster barrier; wide ones stay in
+// each CTA's shared memory and are pulled after the barrier.  The order is fixed, so results are bitwise
 // reproducible and no partials touch HBM.  One launch may carry two
 // independent problems (e.g. s dY B and dY^T sH, which both stream dY):
 // the first CTAs of the grid work on problem 0, the rest on problem 1.
@@ -63,12 +64,15 @@ struct Params {
   Prob p[2];
   int nprob = 1;
   int S = 1;
+  unsigned *zero_ptr = nullptr;  // words zeroed by CTA 0 for the next kernel
+  int zero_words = 0;
   unsigned *dev_status = nullptr;
 };
 
 struct SkinnyLayout {
   int stages;
-  uint32_t b_bytes, pipe_bytes, red_bytes, region_bytes;
+  bool push;      // partials pushed into a dedicated staging area (1 barrier)
+  uint32_t b_bytes, pipe_bytes, red_bytes, region_bytes, red_off;
   size_t smem_bytes;
   uint32_t tmem_cols;
 };
@@ -77,12 +81,23 @@ __host__ __device__ inline SkinnyLayout skinny_layout(int RP, int RK) {
   SkinnyLayout L;
   L.b_bytes = static_cast<uint32_t>(RP) * BK * 2;
   const uint32_t stage_bytes = A_BYTES + L.b_bytes;
-  int st = static_cast<int>(kSmemBudget / stage_bytes);
+  L.red_bytes = BM * (RK + 4) * 4;  // fp32 partials, row pitch RK + 4 floats
+  // Narrow accumulators get a staging area of their own, so peers can push
+  // their partials into it while this CTA's pipeline is still running;
+  // wide ones overlay the pipeline buffers and are pulled after a barrier.
+  L.push = RK <= 64;
+  const size_t budget = L.push ? kSmemBudget + 10 * 1024 - L.red_bytes : kSmemBudget;
+  int st = static_cast<int>(budget / stage_bytes);
   st = st < 2 ? 2 : (st > MAX_STAGES ? MAX_STAGES : st);
   L.stages = st;
   L.pipe_bytes = st * stage_bytes;
-  L.red_bytes = BM * (RK + 4) * 4;  // fp32 partial, row pitch RK + 4 floats
-  L.region_bytes = L.pipe_bytes > L.red_bytes ? L.pipe_bytes : L.red_bytes;
+  if (L.push) {
+    L.red_off = L.pipe_bytes;
+    L.region_bytes = L.pipe_bytes + L.red_bytes;
+  } else {
+    L.red_off = 0;
+    L.region_bytes = L.pipe_bytes > L.red_bytes ? L.pipe_bytes : L.red_bytes;
+  }
   L.smem_bytes = 1024 + L.region_bytes + sizeof(SkinnyTail);
   uint32_t c = 32;
   while (c < static_cast<uint32_t>(RP)) c <<= 1;
@@ -110,7 +125,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
   const uint32_t base = (raw + 1023u) & ~1023u;
   uint8_t *base_ptr = smem_raw + (base - raw);
   SkinnyTail *tail = reinterpret_cast<SkinnyTail *>(base_ptr + L.region_bytes);
-  float *red = reinterpret_cast<float *>(base_ptr);  // reuses the pipeline buffers
+  float *red = reinterpret_cast<float *>(base_ptr + L.red_off);
   const uint32_t sA = base;
   const uint32_t sB = base + L.stages * A_BYTES;
   const int STAGES = L.stages;
@@ -140,6 +155,8 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
   // are used only after the preceding kernel has finished.
   griddep_wait();
   griddep_launch_dependents();
+  if (blockIdx.x == 0 && P.zero_ptr != nullptr)
+    for (int i = threadIdx.x; i < P.zero_words; i += NUM_THREADS) P.zero_ptr[i] = 0u;
   if (warp == 1) {
     tmem_alloc(smem_u32(&tail->tmem_base), L.tmem_cols);
     tmem_relinquish();
@@ -225,14 +242,25 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
       }
     }
   } else {
-    // ------------------------------------------------------ TMEM -> smem partial
+    // ------------------------------------------------------ TMEM -> staging
+    // push: row rl of this CTA's partial belongs to CTA rl / R (which reduces
+    // rows [c*R, (c+1)*R)) and is stored there, in slice `rank`.
+    // pull: the partial stays in this CTA's (overlaid) staging area.
     const int q = warp & 3;
     const bool got = mbar_wait(smem_u32(&tail->tfull), 0, abort_flag, dev_status);
     if (__all_sync(0xffffffffu, got)) {
       tc_fence_after();
-      fence_proxy_async_smem();  // smem last read by the tensor cores is rewritten below
       const int rl = q * 32 + lane;
-      float4 *dst = reinterpret_cast<float4 *>(red + rl * pitch);
+      const int R = BM / S;
+      uint32_t dst;
+      if (L.push) {
+        const int slot = rank * R + rl % R;
+        dst = dsmem_map(smem_u32(red) + static_cast<uint32_t>(slot * pitch) * 4u,
+                        static_cast<uint32_t>(rl / R));
+      } else {
+        fence_proxy_async_smem();  // smem last read by the tensor cores is rewritten
+        dst = smem_u32(red) + static_cast<uint32_t>(rl * pitch) * 4u;
+      }
       const uint32_t taddr = tmem_base + (static_cast<uint32_t>(q * 32) << 16);
       for (int c = 0; c < RK / 16; ++c) {
         float v[16];
@@ -243,26 +271,32 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         }
 #pragma unroll
         for (int i = 0; i < 4; ++i)
-          dst[c * 4 + i] = make_float4(v[4 * i], v[4 * i + 1], v[4 * i + 2], v[4 * i + 3]);
+          dsmem_st_f4(dst + (c * 16 + 4 * i) * 4u,
+                      make_float4(v[4 * i], v[4 * i + 1], v[4 * i + 2], v[4 * i + 3]));
       }
     }
   }
 
   // ------------------------------------------------------ cluster reduction
   __syncwarp();
-  cluster_sync();  // every CTA's partial is in its shared memory
+  cluster_sync();  // every partial is staged
   const int R = BM / S;
   const int r_lo = rank * R;
   const int c4n = RK / 4;
   const uint32_t red_addr = smem_u32(red);
   const bool vec0 = (pr.ld0 % 4 == 0) && (pr.n0 % 4 == 0);
   for (int e = threadIdx.x; e < R * c4n; e += NUM_THREADS) {
-    const int rl = r_lo + e / c4n;
+    const int rr = e / c4n;  // row within this CTA's slice
     const int c4 = e % c4n;
-    const uint32_t off = static_cast<uint32_t>((rl * pitch + c4 * 4) * 4);
     float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
-    for (int p = 0; p < S; ++p) {
-      const float4 v = dsmem_ld_f4(dsmem_map(red_addr + off, static_cast<uint32_t>(p)));
+    for (int p = 0; p < S; ++p) {  // partials added in cluster-rank order
+      float4 v;
+      if (L.push) {
+        v = *reinterpret_cast<const float4 *>(red + (p * R + rr) * pitch + c4 * 4);
+      } else {
+        const uint32_t off = static_cast<uint32_t>(((r_lo + rr) * pitch + c4 * 4) * 4);
+        v = dsmem_ld_f4(dsmem_map(red_addr + off, static_cast<uint32_t>(p)));
+      }
       acc.x += v.x;
       acc.y += v.y;
       acc.z += v.z;
@@ -272,8 +306,11 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     acc.y *= pr.scale;
     acc.z *= pr.scale;
     acc.w *= pr.scale;
-    *reinterpret_cast<float4 *>(red + rl * pitch + c4 * 4) = acc;  // own slice only
-    const int row = m0 + rl;
+    // the result replaces a row only this thread reads: row rr of slice 0
+    // (push) or this CTA's own row r_lo + rr (pull)
+    const int keep = L.push ? rr : r_lo + rr;
+    *reinterpret_cast<float4 *>(red + keep * pitch + c4 * 4) = acc;
+    const int row = m0 + r_lo + rr;
     if (pr.out0 != nullptr && row < pr.rows) {
       const int c = c4 * 4;
       __nv_bfloat16 *o = pr.out0 + static_cast<int64_t>(row) * pr.ld0 + c;
@@ -291,15 +328,19 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
       }
     }
   }
-  cluster_sync();  // peers are done reading this CTA's shared memory
+  // pull: peers must finish reading this CTA's staging area before it is
+  // reused or the CTA exits; push: only local data is read after the barrier
+  if (!L.push) cluster_sync();
+  __syncthreads();
 
   if (pr.out1 != nullptr) {  // transposed copy: consecutive threads, consecutive rows
     for (int e = threadIdx.x; e < R * pr.n1; e += NUM_THREADS) {
       const int j = e / R;
-      const int rl = r_lo + e % R;
-      const int row = m0 + rl;
+      const int rr = e % R;
+      const int row = m0 + r_lo + rr;
+      const int keep = L.push ? rr : r_lo + rr;
       if (row < pr.rows)
-        pr.out1[static_cast<int64_t>(j) * pr.ld1 + row] = __float2bfloat16_rn(red[rl * pitch + j]);
+        pr.out1[static_cast<int64_t>(j) * pr.ld1 + row] = __float2bfloat16_rn(red[keep * pitch + j]);
     }
   }
 
@@ -371,6 +412,11 @@ cudaError_t launch_skinny(const SkinnyArgs *probs, int nprob, int num_sms, cudaS
     grid += static_cast<unsigned>(P.p[i].ctas);
   }
   P.dev_status = use[0]->dev_status;
+  for (int i = 0; i < nprob; ++i)
+    if (probs[i].zero_ptr != nullptr) {
+      P.zero_ptr = probs[i].zero_ptr;
+      P.zero_words = probs[i].zero_words;
+    }
   cudaError_t e = cudaFuncSetAttribute(k_skinny, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                        static_cast<int>(smem));
   if (e != cudaSuccess) return e;

@@ -46,8 +46,15 @@ def test_sizes():
     assert L.lora_linear_saved_bytes(64, 8, _lib.LORA_FP32) == 64 * 8 * 4
     assert L.lora_linear_saved_bytes(64, 0, _lib.LORA_BF16) == 0
     ws = L.lora_linear_workspace_bytes(4096, 4096, 4096, 16, _lib.LORA_BF16)
-    # B^T [16, 4096] + sG [4096, 16] + sG^T [16, 4096] + room for a recomputed saved buffer
-    assert ws == 3 * 4096 * 16 * 2 + 4096 * 16 * 2 * 2
+    # B^T [16, 4096] + sG [4096, 16] + sG^T [16, 4096] + the dX GEMM's tail split
+    # (no GPU here: sized for 76 CTA pairs; 256 pair tiles leave 28 in the last
+    # wave, split 2 ways: 28 x 2 ranges x 2 CTAs x 128 x 256 fp32, and 2 x 28
+    # counters) + room for a recomputed saved buffer
+    split = 28 * 2 * 2 * 128 * 256 * 4 + 256
+    assert ws == 3 * 4096 * 16 * 2 + split + 4096 * 16 * 2 * 2
+    # shapes whose last wave is nearly full are not split
+    ws2 = L.lora_linear_workspace_bytes(8192, 4096, 14336, 16, _lib.LORA_BF16)
+    assert ws2 == 16 * 14336 * 2 + 2 * 8192 * 16 * 2 + 8192 * 16 * 2 * 2
     assert L.lora_linear_workspace_bytes(0, 64, 64, 16, _lib.LORA_BF16) == 0
 
 

@@ -209,3 +209,36 @@ def test_timing_hook_rejects_uncreated_events():
     from rank_linear_gb300 import _lib
     arr = (ctypes.c_void_p * 2)(None, None)
     assert _lib.lib().lora_set_timing_events(arr, None, 1) == _lib.LORA_ERR_INVALID_ARG
+
+
+def test_tail_split_path():
+    """M = d_in = d_out = 4096: the main GEMMs' last wave is split across CTA
+    pairs (given the full workspace).  The split results are bitwise
+    repeatable, agree with the unsplit ones (minimal workspace) and with the
+    oracle on sampled rows."""
+    M = d = 4096
+    r, alpha = 16, 16.0
+    t = make_inputs(M, d, d, r, "bf16", seed=12, device=DEV)
+    X, W, A, B, dY = t["X"], t["W"], t["A"], t["B"], t["dY"]
+    full = torch.empty(rl.workspace_bytes(M, d, d, r, torch.bfloat16), dtype=torch.uint8,
+                       device=DEV)
+    minimal = torch.empty(3 * 16 * 4096 * 2, dtype=torch.uint8, device=DEV)  # B^T, sG, sG^T
+    assert full.numel() > minimal.numel()
+
+    def run(ws):
+        Y, saved = rl.forward(X, W, A, B, alpha, workspace=ws)
+        dX, dA, dB = rl.backward(dY, X, W, A, B, alpha, saved, workspace=ws)
+        torch.cuda.synchronize()
+        rl.device_status()
+        return Y, dX, dA, dB
+
+    s1, s2, u = run(full), run(full), run(minimal)
+    for a, b in zip(s1, s2):
+        assert torch.equal(a, b)
+    for a, b in zip(s1, u):
+        assert rel_err(a, b.double().cpu().numpy()) <= 4e-3
+    host = {k: v.cpu() for k, v in t.items()}
+    S = oracle.Sampled(host["X"], host["W"], host["A"], host["B"], host["dY"], alpha)
+    rows = np.array([0, 2047, 3071, 3584, 4095])  # include rows of the split tiles
+    assert rel_err(s1[0][rows], S.y_rows(rows)) <= TOL["bf16"]
+    assert rel_err(s1[1][rows], S.dx_rows(rows)) <= TOL["bf16"]
