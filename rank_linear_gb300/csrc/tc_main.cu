@@ -72,9 +72,16 @@ struct __align__(8) MainTail {
   int split_last;
 };
 
+// Epilogue staging: per epilogue warp, one 32 x 32 bf16 chunk with rows
+// padded to 80 bytes (conflict-free 16-byte writes).
+constexpr uint32_t EPI_PITCH = 80;
+constexpr uint32_t EPI_WARP_BYTES = 32 * EPI_PITCH;
+constexpr uint32_t EPI_BYTES = 4 * EPI_WARP_BYTES;
+
 template <int BN>
 constexpr size_t smem_bytes() {
-  return 1024 + size_t(Geo<BN>::STAGES) * Geo<BN>::STAGE_BYTES + sizeof(MainTail<Geo<BN>::STAGES>);
+  return 1024 + size_t(Geo<BN>::STAGES) * Geo<BN>::STAGE_BYTES + EPI_BYTES +
+         sizeof(MainTail<Geo<BN>::STAGES>);
 }
 
 // Work item -> tile and K-block range.  Items below split_first are whole
@@ -115,6 +122,29 @@ __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
   return *reinterpret_cast<uint32_t *>(&v);
 }
 
+// Writes a warp's 32 x 32 bf16 chunk (lane = row, pk = its 32 columns) to
+// out rows row0.. and columns col0.. through the warp's staging buffer, so
+// that each global store instruction covers 8 rows x 64 contiguous bytes.
+__device__ __forceinline__ void store_chunk(const uint32_t (&pk)[16], uint8_t *stage, int lane,
+                                           __nv_bfloat16 *out, int64_t ldo, int row0, int col0,
+                                           int M, int N) {
+  uint4 *my = reinterpret_cast<uint4 *>(stage + lane * EPI_PITCH);
+#pragma unroll
+  for (int i = 0; i < 4; ++i) my[i] = make_uint4(pk[4 * i], pk[4 * i + 1], pk[4 * i + 2], pk[4 * i + 3]);
+  __syncwarp();
+  const int seg = lane & 3;  // 16-byte segment (8 columns) of a row
+  const int col = col0 + seg * 8;
+#pragma unroll
+  for (int j = 0; j < 4; ++j) {
+    const int r = 8 * j + (lane >> 2);
+    const uint4 v = *reinterpret_cast<const uint4 *>(stage + r * EPI_PITCH + seg * 16);
+    const int row = row0 + r;
+    if (row < M && col < N)  // N is a multiple of 8: a segment is all in or all out
+      *reinterpret_cast<uint4 *>(out + static_cast<int64_t>(row) * ldo + col) = v;
+  }
+  __syncwarp();
+}
+
 template <bool B_MN, int BN, bool SPLIT>
 __global__ void __launch_bounds__(NUM_THREADS, 1)
     k_main_gemm(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
@@ -129,8 +159,8 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
   extern __shared__ uint8_t smem_raw[];
   const uint32_t raw = smem_u32(smem_raw);
   const uint32_t base = (raw + 1023u) & ~1023u;  // 128-B swizzle atoms need 1 KB alignment
-  auto *tail =
-      reinterpret_cast<MainTail<STAGES> *>(smem_raw + (base - raw) + STAGES * STAGE_BYTES);
+  uint8_t *epi_stage = smem_raw + (base - raw) + STAGES * STAGE_BYTES;
+  auto *tail = reinterpret_cast<MainTail<STAGES> *>(epi_stage + EPI_BYTES);
   const uint32_t sA = base;
   const uint32_t sB = base + STAGES * A_BYTES;
 
@@ -325,27 +355,17 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
       const int rl = qd * 32 + lane;  // row within this CTA's 128
       const int row = (2 * mp + q) * BM + rl;
       const uint32_t taddr = tmem_base + (static_cast<uint32_t>(qd * 32) << 16) + acc * BN;
-      __nv_bfloat16 *orow = out + static_cast<int64_t>(row) * ldo;
+      uint8_t *stage = epi_stage + qd * EPI_WARP_BYTES;
+      const int row0 = (2 * mp + q) * BM + qd * 32;
       if (!SPLIT || !split) {
 #pragma unroll 1
         for (int c = 0; c < BN / 32; ++c) {
           float v[32];
           tmem_ld_32cols(taddr + c * 32, v);
-          const int col0 = nb * BN + c * 32;
-          if (row < M) {
+          uint32_t pk[16];
 #pragma unroll
-            for (int g = 0; g < 4; ++g) {
-              const int col = col0 + g * 8;
-              if (col < N) {  // N is a multiple of 8: a group is all in or all out
-                uint4 pk;
-                pk.x = pack_bf16x2(v[g * 8 + 0], v[g * 8 + 1]);
-                pk.y = pack_bf16x2(v[g * 8 + 2], v[g * 8 + 3]);
-                pk.z = pack_bf16x2(v[g * 8 + 4], v[g * 8 + 5]);
-                pk.w = pack_bf16x2(v[g * 8 + 6], v[g * 8 + 7]);
-                *reinterpret_cast<uint4 *>(orow + col) = pk;
-              }
-            }
-          }
+          for (int i = 0; i < 16; ++i) pk[i] = pack_bf16x2(v[2 * i], v[2 * i + 1]);
+          store_chunk(pk, stage, lane, out, ldo, row0, nb * BN + c * 32, M, N);
         }
         tc_fence_before();
         __syncwarp();
@@ -387,21 +407,11 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
           for (int i = 0; i < 32; ++i) o[i] = __ldcg(slot_other + (c * 32 + i) * BM + rl);
           float v[32];
           tmem_ld_32cols(taddr + c * 32, v);
-          const int col0 = nb * BN + c * 32;
-          if (row < M) {
+          uint32_t pk[16];
 #pragma unroll
-            for (int g = 0; g < 4; ++g) {
-              const int col = col0 + g * 8;
-              if (col < N) {
-                uint4 pk;
-                pk.x = pack_bf16x2(v[g * 8 + 0] + o[g * 8 + 0], v[g * 8 + 1] + o[g * 8 + 1]);
-                pk.y = pack_bf16x2(v[g * 8 + 2] + o[g * 8 + 2], v[g * 8 + 3] + o[g * 8 + 3]);
-                pk.z = pack_bf16x2(v[g * 8 + 4] + o[g * 8 + 4], v[g * 8 + 5] + o[g * 8 + 5]);
-                pk.w = pack_bf16x2(v[g * 8 + 6] + o[g * 8 + 6], v[g * 8 + 7] + o[g * 8 + 7]);
-                *reinterpret_cast<uint4 *>(orow + col) = pk;
-              }
-            }
-          }
+          for (int i = 0; i < 16; ++i)
+            pk[i] = pack_bf16x2(v[2 * i] + o[2 * i], v[2 * i + 1] + o[2 * i + 1]);
+          store_chunk(pk, stage, lane, out, ldo, row0, nb * BN + c * 32, M, N);
         }
       }
       if (sync_ok) sync_ok = epi_sync();  // the flag word is free again
