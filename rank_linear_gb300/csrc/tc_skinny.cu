@@ -375,14 +375,31 @@ Prob to_prob(const SkinnyArgs &a, int S) {
 
 }  // namespace
 
-// Cluster size: enough CTAs to keep every SM streaming (about two per SM),
-// while each CTA keeps at least four K blocks.
+// Cluster size for a launch of `total_mt` 128-row tiles (summed over its
+// problems) whose longest problem has `max_kb` K blocks: the S in
+// {1, 2, 4, 8} minimising  waves(S) x (t_kb * ceil(max_kb / S) + t_cta),
+// where waves counts two CTAs per SM, t_kb ~ 0.15 us is the time of one K
+// block of a CTA with every slot streaming and t_cta ~ 4 us is a CTA's fixed
+// cost (start-up latency and the cluster reduction).  Ties go to fewer CTAs.
+int skinny_split_launch(int total_mt, int max_kb, int num_sms) {
+  const int slots = 2 * num_sms;
+  const double t_kb = 0.15, t_cta = 4.0;
+  int best = 1;
+  double best_cost = 1e300;
+  for (int S = 1; S <= 8; S *= 2) {
+    if (S > 1 && max_kb < 2 * S) break;  // keep at least two K blocks per CTA
+    const double waves = static_cast<double>((total_mt * S + slots - 1) / slots);
+    const double cost = waves * (t_kb * ((max_kb + S - 1) / S) + t_cta);
+    if (cost < best_cost - 1e-9) {
+      best_cost = cost;
+      best = S;
+    }
+  }
+  return best;
+}
+
 int skinny_split(int rows, int K, int num_sms) {
-  const int mt = (rows + BM - 1) / BM;
-  const int nkb = (K + BK - 1) / BK;
-  int S = 1;
-  while (S < 8 && mt * S < 2 * num_sms && nkb >= 8 * S) S *= 2;
-  return S;
+  return skinny_split_launch((rows + BM - 1) / BM, (K + BK - 1) / BK, num_sms);
 }
 
 cudaError_t launch_skinny(const SkinnyArgs *probs, int nprob, int num_sms, cudaStream_t s) {
@@ -392,16 +409,14 @@ cudaError_t launch_skinny(const SkinnyArgs *probs, int nprob, int num_sms, cudaS
   for (int i = 0; i < nprob; ++i)
     if (probs[i].rows > 0) use[P.nprob++] = &probs[i];
   if (P.nprob == 0) return cudaSuccess;
-  // one cluster size for the whole launch: the smaller of the problems' own
-  int S = 8;
-  int total_rows_ctas = 0;
+  // one cluster size for the whole launch
+  int total_mt = 0, max_kb = 0;
   for (int i = 0; i < P.nprob; ++i) {
-    const int rows_all = use[i]->rows;
-    const int si = skinny_split(rows_all, use[i]->K, num_sms);
-    S = si < S ? si : S;
-    total_rows_ctas += (rows_all + BM - 1) / BM;
+    total_mt += (use[i]->rows + BM - 1) / BM;
+    const int kb = (use[i]->K + BK - 1) / BK;
+    max_kb = kb > max_kb ? kb : max_kb;
   }
-  (void)total_rows_ctas;
+  const int S = skinny_split_launch(total_mt, max_kb, num_sms);
   P.S = S;
   size_t smem = 0;
   unsigned grid = 0;
