@@ -282,6 +282,11 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     // ------------------------------------------------------ MMA issuer (even CTA)
     if (leader && lane == 0) {
       constexpr uint32_t idesc = idesc_bf16(CLUSTER * BM, BN, false, B_MN);
+      // per 16-wide K step: 32 B along a K-major row, or two 1 KB MN-major
+      // swizzle atoms (descriptor units of 16 B)
+      constexpr uint64_t A_STEP = 32 >> 4, B_STEP = B_MN ? (2048 >> 4) : (32 >> 4);
+      const uint64_t a_desc0 = sdesc_sw128(sA, 16, 1024);
+      const uint64_t b_desc0 = B_MN ? sdesc_sw128(sB, 8192, 1024) : sdesc_sw128(sB, 16, 1024);
       int stage = 0;
       uint32_t phase = 0;
       bool ok = true;
@@ -297,24 +302,39 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         }
         tc_fence_after();
         const uint32_t d = tmem_base + acc * BN;
+        // Descriptors of the current stage, advanced by addition: the
+        // start-address field is the low 14 bits (address / 16) and every
+        // stage lies below 256 KB, so the sums never carry out of it.
+        // Between two MMAs the issuing thread runs as few instructions as
+        // possible: anything longer than the tensor pipe's short queue
+        // shows up as idle tensor cycles.
+        uint64_t ad = a_desc0 + stage * (A_BYTES >> 4);
+        uint64_t bd = b_desc0 + stage * (B_BYTES >> 4);
+        uint32_t accum = 0;
         for (int kb = kb_lo; kb < kb_hi; ++kb) {
           if (!mbar_wait(smem_u32(&tail->full[stage]), phase, abort_flag, dev_status)) {
             ok = false;
             break;
           }
           tc_fence_after();
-          const int nk = kb < kb_main ? BK / 16 : min(BK / 16, (k_ext - (kb - kb_main) * BK) / 16);
-          const uint32_t a0 = sA + stage * A_BYTES, b0 = sB + stage * B_BYTES;
-          for (int kk = 0; kk < nk; ++kk) {
-            const uint64_t ad = sdesc_sw128(a0 + kk * 32, 16, 1024);
-            const uint64_t bd = B_MN ? sdesc_sw128(b0 + kk * 2048, 8192, 1024)
-                                     : sdesc_sw128(b0 + kk * 32, 16, 1024);
-            tc_mma_bf16_pair(d, ad, bd, idesc, (kb > kb_lo || kk != 0) ? 1u : 0u);
+          if (kb < kb_main) {
+#pragma unroll
+            for (int kk = 0; kk < BK / 16; ++kk)
+              tc_mma_bf16_pair(d, ad + kk * A_STEP, bd + kk * B_STEP, idesc, kk ? 1u : accum);
+          } else {
+            const int nk = min(BK / 16, (k_ext - (kb - kb_main) * BK) / 16);
+            for (int kk = 0; kk < nk; ++kk)
+              tc_mma_bf16_pair(d, ad + kk * A_STEP, bd + kk * B_STEP, idesc, kk ? 1u : accum);
           }
+          accum = 1u;
           tc_commit_pair_mc(smem_u32(&tail->empty[stage]), PAIR_MASK);  // free in both CTAs
+          ad += A_BYTES >> 4;
+          bd += B_BYTES >> 4;
           if (++stage == STAGES) {
             stage = 0;
             phase ^= 1u;
+            ad = a_desc0;
+            bd = b_desc0;
           }
         }
         if (!ok) break;
@@ -353,7 +373,6 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
       if (!__all_sync(0xffffffffu, got)) break;
       tc_fence_after();
       const int rl = qd * 32 + lane;  // row within this CTA's 128
-      const int row = (2 * mp + q) * BM + rl;
       const uint32_t taddr = tmem_base + (static_cast<uint32_t>(qd * 32) << 16) + acc * BN;
       uint8_t *stage = epi_stage + qd * EPI_WARP_BYTES;
       const int row0 = (2 * mp + q) * BM + qd * 32;
