@@ -118,6 +118,21 @@ __device__ __forceinline__ void tma_load_2d_mc(uint32_t dst, const CUtensorMap *
       "l"(reinterpret_cast<uint64_t>(tm)), "r"(bar), "r"(x), "r"(y), "h"(cta_mask)
       : "memory");
 }
+// Untiled bulk copy of `bytes` from global memory into this CTA's shared
+// memory, counted on `bar`: both addresses 16-byte aligned, bytes a multiple
+// of 16.
+__device__ __forceinline__ void bulk_load(uint32_t dst, const void *src, uint32_t bytes,
+                                          uint32_t bar) {
+  asm volatile(
+      "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(dst),
+      "l"(reinterpret_cast<uint64_t>(src)), "r"(bytes), "r"(bar)
+      : "memory");
+}
+// Orders this thread's earlier generic-proxy accesses of global memory
+// (e.g. an acquiring atomic) before its later async-proxy (bulk copy) ones.
+__device__ __forceinline__ void fence_proxy_async_global() {
+  asm volatile("fence.proxy.async.global;" ::: "memory");
+}
 // 2-D tiled load into this CTA's shared memory whose completion is counted
 // on an mbarrier that may live in the peer CTA of a CTA pair (`bar` is a
 // shared::cluster address, e.g. from dsmem_map).

@@ -67,6 +67,7 @@ struct __align__(8) MainTail {
   uint64_t tempty[2];       // even CTA: both CTAs drained an accumulator
   uint64_t drain;
   uint64_t ebar;            // each CTA: the four epilogue warps meet (tail split)
+  uint64_t fix;             // each CTA: the other K range's partial landed (tail split)
   uint32_t tmem_base;
   int abort_flag;
   int split_last;
@@ -193,6 +194,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     }
     mbar_init(smem_u32(&tail->drain), 1);
     mbar_init(smem_u32(&tail->ebar), 4);
+    mbar_init(smem_u32(&tail->fix), 1);
     tail->abort_flag = 0;
     fence_barrier_init();
     tma_prefetch(&tmA);
@@ -418,12 +420,32 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
       sync_ok = sync_ok && epi_sync();
       const bool last = sync_ok && *reinterpret_cast<volatile int *>(last_flag) != 0;
       if (last) {
-        __threadfence();
+        // The other range's partial (BM x BN fp32, column-major) comes in
+        // with bulk copies on one barrier, into the stage ring: a split item
+        // is its pair's last, so the ring's loads have all been consumed by
+        // the MMAs that completed this accumulator.  One round trip instead
+        // of a dependent chain of global loads per column block.
+        constexpr uint32_t PART_BYTES = BM * BN * 4, PIECE = 16384;
+        static_assert(PART_BYTES <= STAGES * STAGE_BYTES, "partial must fit the stage ring");
+        const uint32_t fix = smem_u32(&tail->fix);
+        if (et == 0) {
+          __threadfence();             // acquire: the other range's partial is final
+          fence_proxy_async_global();  // ... and ordered before the bulk reads
+          mbar_expect_tx(fix, PART_BYTES);
+          for (uint32_t o = 0; o < PART_BYTES; o += PIECE)
+            bulk_load(base + o, reinterpret_cast<const uint8_t *>(slot_other) + o, PIECE, fix);
+        }
+        const bool landed = mbar_wait(fix, 0, abort_flag, dev_status);
+        if (!__all_sync(0xffffffffu, landed)) {
+          if (et == 0) mbar_wait_drain(fix, 0);  // the copies in flight land first
+          break;
+        }
+        const float *part = reinterpret_cast<const float *>(smem_raw + (base - raw));
 #pragma unroll 1
         for (int c = 0; c < BN / 32; ++c) {
           float o[32];
 #pragma unroll
-          for (int i = 0; i < 32; ++i) o[i] = __ldcg(slot_other + (c * 32 + i) * BM + rl);
+          for (int i = 0; i < 32; ++i) o[i] = part[(c * 32 + i) * BM + rl];
           float v[32];
           tmem_ld_32cols(taddr + c * 32, v);
           uint32_t pk[16];
