@@ -402,49 +402,81 @@ def run_ours(args, w):
 
 
 def run_e2e(args, w, t, tdt, dev, stream, world):
-    """Same metric through the C ABI with pinned host buffers: every step
-    copies the inputs in and the results (Y, dX, dA, dB) out."""
+    """Same metric through the public API with pinned host buffers: every step
+    copies its inputs (X, W, A, B, dY) in and its results (Y, dX, dA, dB) out,
+    inside the timed region.  Steps are pipelined the way a training loop
+    would be: two device buffer sets, uploads on one stream, the layer on the
+    launching stream, downloads on a third, so that step i+1's upload and
+    step i-1's download overlap step i's kernels."""
     import torch
     import rank_linear_gb300 as rl
     M, d_in, d_out, r, alpha = w.M, w.d_in, w.d_out, w.r, w.alpha
     h_in = {k: v.cpu().pin_memory() for k, v in t.items()}
-    d_in_t = {k: torch.empty_like(v) for k, v in t.items()}
     outs = {"Y": (M, d_out), "dX": (M, d_in), "dA": (r, d_in), "dB": (d_out, r)}
-    d_out_t = {k: torch.empty(s, dtype=tdt, device=dev) for k, s in outs.items()}
-    h_out = {k: torch.empty(s, dtype=tdt).pin_memory() for k, s in outs.items()}
+    nbuf = 2
+    d_in_t = [{k: torch.empty_like(v) for k, v in t.items()} for _ in range(nbuf)]
+    d_out_t = [{k: torch.empty(s, dtype=tdt, device=dev) for k, s in outs.items()}
+               for _ in range(nbuf)]
+    h_out = [{k: torch.empty(s, dtype=tdt).pin_memory() for k, s in outs.items()}
+             for _ in range(nbuf)]
     saved = torch.empty(max(1, rl.saved_bytes(M, r, tdt)), dtype=torch.uint8, device=dev)
     ws = torch.empty(max(1, rl.workspace_bytes(M, d_in, d_out, r, tdt)), dtype=torch.uint8,
                      device=dev)
+    s_up = torch.cuda.Stream(device=dev)
+    s_down = torch.cuda.Stream(device=dev)
+    ev = lambda: torch.cuda.Event()
+    up_done = [ev() for _ in range(nbuf)]
+    comp_done = [ev() for _ in range(nbuf)]
+    down_done = [ev() for _ in range(nbuf)]
+    for b in range(nbuf):  # every buffer starts free
+        comp_done[b].record(stream)
+        down_done[b].record(stream)
 
-    def step():
-        for k in h_in:
-            d_in_t[k].copy_(h_in[k], non_blocking=True)
-        g = d_in_t
-        rl.forward(g["X"], g["W"], g["A"], g["B"], alpha, Y=d_out_t["Y"], saved=saved,
+    def step(i):
+        b = i % nbuf
+        din, dout, hout = d_in_t[b], d_out_t[b], h_out[b]
+        s_up.wait_event(comp_done[b])  # step i-2 has finished reading din
+        with torch.cuda.stream(s_up):
+            for k in h_in:
+                din[k].copy_(h_in[k], non_blocking=True)
+        up_done[b].record(s_up)
+        stream.wait_event(up_done[b])
+        stream.wait_event(down_done[b])  # step i-2's results have left dout
+        rl.forward(din["X"], din["W"], din["A"], din["B"], alpha, Y=dout["Y"], saved=saved,
                    workspace=ws, stream=stream)
-        rl.backward(g["dY"], g["X"], g["W"], g["A"], g["B"], alpha, saved, dX=d_out_t["dX"],
-                    dA=d_out_t["dA"], dB=d_out_t["dB"], workspace=ws, stream=stream)
-        for k in h_out:
-            h_out[k].copy_(d_out_t[k], non_blocking=True)
+        rl.backward(din["dY"], din["X"], din["W"], din["A"], din["B"], alpha, saved,
+                    dX=dout["dX"], dA=dout["dA"], dB=dout["dB"], workspace=ws, stream=stream)
+        comp_done[b].record(stream)
+        s_down.wait_event(comp_done[b])
+        with torch.cuda.stream(s_down):
+            for k in hout:
+                hout[k].copy_(dout[k], non_blocking=True)
+        down_done[b].record(s_down)
 
-    for _ in range(max(1, args.warmup)):
-        step()
+    for i in range(max(nbuf, args.warmup)):
+        step(i)
     torch.cuda.synchronize()
     n = max(3, min(args.steps, 50))
     e0 = torch.cuda.Event(enable_timing=True)
     e1 = torch.cuda.Event(enable_timing=True)
     barrier(world)
-    e0.record(stream)
-    for _ in range(n):
-        step()
+    e0.record(stream)  # before the first upload; everything after depends on it
+    s_up.wait_event(e0)
+    s_down.wait_event(e0)
+    for i in range(n):
+        step(i)
+    stream.wait_stream(s_down)  # e1 follows the last download
     e1.record(stream)
     torch.cuda.synchronize()
     sec = max_over_ranks(e0.elapsed_time(e1) / 1e3, world, dev)
     bi = sum(v.numel() * v.element_size() for v in h_in.values())
-    bo = sum(v.numel() * v.element_size() for v in h_out.values())
+    bo = sum(v.numel() * v.element_size() for v in h_out[0].values())
     return {"value": world * step_flops(M, d_in, d_out, r) * n / sec / 1e12, "unit": "TFLOP/s",
             "h2d_bytes_per_step": bi, "d2h_bytes_per_step": bo, "steps": n,
-            "inputs": "X, W, A, B, dY copied in; Y, dX, dA, dB copied out (pinned host)"}
+            "inputs": "X, W, A, B, dY copied in; Y, dX, dA, dB copied out (pinned host), "
+                      "every step; uploads, kernels and downloads on three streams with two "
+                      "device buffer sets (step i+1's upload and step i-1's download overlap "
+                      "step i's kernels)"}
 
 
 def main(argv=None):
