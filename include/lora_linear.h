@@ -206,6 +206,20 @@ lora_status_t lora_set_timing_events(void *const *events, int *kinds,
                                      int n_pairs);
 int lora_timing_used(void);
 
+/*
+ * Test hook for the bounded device-side waits (the pages have no
+ * counterpart; it exists so that the timeout path can be exercised without
+ * faulting or hanging a GPU).  The next n bf16 backward dA passes (the last
+ * launch of lora_linear_bwd) launched by this process (any thread) leave
+ * the first pipeline stage of their first CTA unfilled.  That CTA's MMA
+ * wait then runs out after the wait limit (about 2 s), the kernel leaves
+ * through its abort path (no fault, no hang), the caller's next
+ * lora_device_status() returns LORA_ERR_TIMEOUT, and dA of that call is
+ * undefined (dX and dB are complete).  n = 0 cancels.  Returns
+ * LORA_ERR_INVALID_ARG for n < 0.
+ */
+lora_status_t lora_debug_withhold_arrive(int n);
+
 #ifdef __cplusplus
 }
 #endif

@@ -35,6 +35,7 @@ SIGNATURES = {
     "lora_device_status": ([_int], _int),
     "lora_launch_count": ([], ctypes.c_uint64),
     "lora_set_timing_events": ([ctypes.POINTER(_vp), ctypes.POINTER(_int), _int], _int),
+    "lora_debug_withhold_arrive": ([_int], _int),
     "lora_timing_used": ([], _int),
 }
 

@@ -71,6 +71,9 @@ struct SkinnyArgs {
   int64_t ld1 = 0;
   int n1 = 0;
   unsigned *dev_status = nullptr;
+  // Test hook of the bounded waits: the first CTA's producer leaves its
+  // first stage unfilled, so that CTA's MMA wait runs out (problem 0 only).
+  int withhold_first_stage = 0;
 };
 // Runs one or two independent problems in one launch.
 cudaError_t launch_skinny(const SkinnyArgs *probs, int nprob, int num_sms, cudaStream_t s);

@@ -30,6 +30,8 @@ struct TimingHook {
 };
 thread_local TimingHook t_hook;
 std::atomic<uint64_t> g_launches{0};
+// backward dA passes still to launch with a withheld stage (test hook)
+std::atomic<int> g_withhold{0};
 
 lora_status_t fail(lora_status_t st, const char *fmt, ...) {
   char buf[512];
@@ -437,6 +439,10 @@ lora_status_t bwd_bf16(const void *dY, const void *X, const void *W, const void 
   b3.ld1 = d_in;
   b3.n1 = r;
   b3.dev_status = di.status;
+  int pending = g_withhold.load();  // test hook of the bounded waits
+  while (pending > 0 && !g_withhold.compare_exchange_weak(pending, pending - 1)) {
+  }
+  b3.withhold_first_stage = pending > 0 ? 1 : 0;
   return run(LORA_K_GRAD_A, st, "dA pass", [&] { return launch_skinny(&b3, 1, di.sms, st); });
 }
 
@@ -760,5 +766,12 @@ lora_status_t lora_set_timing_events(void *const *events, int *kinds, int n_pair
 }
 
 int lora_timing_used(void) { return t_hook.used; }
+
+lora_status_t lora_debug_withhold_arrive(int n) {
+  t_err.clear();
+  if (n < 0) return fail(LORA_ERR_INVALID_ARG, "n = %d is negative", n);
+  g_withhold.store(n);
+  return LORA_OK;
+}
 
 }  // extern "C"

@@ -268,16 +268,31 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
           }
         }
       }
+      bool clean = ok;
       if (ok) {
         // The pair MMAs have released every stage this CTA filled: no commit
-        // is still on its way to this CTA's barriers.
+        // is still on its way to this CTA's barriers, and no copy in flight.
         for (int s = 0; s < STAGES; ++s)
           if (issued[s] && !mbar_wait(smem_u32(&tail->empty[s]), (issued[s] - 1u) & 1u,
-                                      abort_flag, dev_status))
+                                      abort_flag, dev_status)) {
+            clean = false;
             break;
-      } else if (leader) {  // let the pair's copies in flight land before exiting
-        for (int s = 0; s < STAGES; ++s)
-          if (issued[s]) mbar_wait_drain(smem_u32(&tail->full[s]), (issued[s] - 1u) & 1u);
+          }
+      }
+      if (!clean) {  // aborting: let the pair's copies in flight land before exiting
+        if (leader) {
+          // a phase the even CTA armed completes when both CTAs' bytes landed
+          for (int s = 0; s < STAGES; ++s)
+            if (issued[s]) mbar_wait_drain(smem_u32(&tail->full[s]), (issued[s] - 1u) & 1u);
+        } else {
+          // The odd CTA's copies complete on the even CTA's barriers, which it
+          // cannot poll; one it issued for a phase the even CTA never armed
+          // is not covered above.  A copy lands within microseconds: wait
+          // 100 us before leaving.
+          const uint64_t t0 = globaltimer_ns();
+          while (globaltimer_ns() - t0 < 100000ull) {
+          }
+        }
       }
     }
   } else if (warp == 1) {

@@ -67,6 +67,7 @@ struct Params {
   unsigned *zero_ptr = nullptr;  // words zeroed by CTA 0 for the next kernel
   int zero_words = 0;
   unsigned *dev_status = nullptr;
+  int withhold = 0;  // test hook: CTA 0 never fills its first stage
 };
 
 struct SkinnyLayout {
@@ -180,6 +181,15 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
           ok = false;
           break;
         }
+        if (P.withhold && blockIdx.x == 0 && kb == kb_begin) {
+          // test hook: this stage is never filled, so the MMA thread's wait
+          // for it runs out and the CTA leaves through its abort path
+          if (++stage == STAGES) {
+            stage = 0;
+            phase ^= 1u;
+          }
+          continue;
+        }
         const uint32_t full = smem_u32(&tail->full[stage]);
         mbar_expect_tx(full, tx);
         const int k0 = kb * BK;
@@ -201,6 +211,10 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
           phase ^= 1u;
         }
       }
+      // Stay until the MMAs have consumed every stage (their final commit).
+      // If that wait gives up, the CTA is aborting and copies this thread
+      // issued may still be in flight: let them land before the CTA exits.
+      if (ok) ok = mbar_wait(smem_u32(&tail->tfull), 0, abort_flag, dev_status);
       if (!ok) {
         for (int s = 0; s < STAGES; ++s)
           if (issued[s]) mbar_wait_drain(smem_u32(&tail->full[s]), (issued[s] - 1u) & 1u);
@@ -427,6 +441,7 @@ cudaError_t launch_skinny(const SkinnyArgs *probs, int nprob, int num_sms, cudaS
     grid += static_cast<unsigned>(P.p[i].ctas);
   }
   P.dev_status = use[0]->dev_status;
+  P.withhold = use[0]->withhold_first_stage;
   for (int i = 0; i < nprob; ++i)
     if (probs[i].zero_ptr != nullptr) {
       P.zero_ptr = probs[i].zero_ptr;

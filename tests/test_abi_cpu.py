@@ -124,6 +124,11 @@ def test_timing_hook_set_and_clear():
     assert L.lora_timing_used() == 0
 
 
+def test_withhold_hook_arguments():
+    assert L.lora_debug_withhold_arrive(-1) == _lib.LORA_ERR_INVALID_ARG
+    assert L.lora_debug_withhold_arrive(0) == _lib.LORA_OK
+
+
 def test_product_path_needs_the_library(monkeypatch, tmp_path):
     """Without the built library the Python layer raises; it has no fallback."""
     monkeypatch.setattr(_lib, "_lib", None)
