@@ -31,6 +31,20 @@ struct MainGemmArgs {
   float *partials = nullptr;
   unsigned *counters = nullptr;
   unsigned *dev_status = nullptr;
+  // Gated (SwiGLU) pair: the pair's even CTA multiplies by B = tmB and
+  // B2 = tmB2 (gate projection), the odd CTA by tmB3 and tmB4 (up
+  // projection), whose extension columns are read ext_shift columns earlier
+  // (K coordinate k - ext_shift) so that they meet the second half of the
+  // extension A = [sH_g | sH_u].  A pair tile is 256 rows x 128 columns of
+  // both projections; out = silu(gate) * up, aux0 = gate, aux1 = up (bf16,
+  // row pitch ldo; aux0/aux1 may be null).  N counts output columns.
+  bool gated = false;
+  CUtensorMap tmB3, tmB4;
+  int ext_shift = 0;
+  void *aux0 = nullptr, *aux1 = nullptr;
+  // Second B segment of the main K range (not gated): K blocks >= kb_switch
+  // read B from tmB3 at K coordinate (kb - kb_switch) * 64.  -1: none.
+  int kb_switch = -1;
 };
 constexpr int kMainBM = 128, kMainBK = 64;
 int main_gemm_pick_bn(int M, int N, int num_sms);
@@ -41,7 +55,8 @@ struct MainSplit {
   size_t partial_bytes = 0, counter_bytes = 0;
 };
 // Tail split for an M x N output on `pairs` CTA pairs: the last wave's rem
-// tiles are split two ways (K ranges) when 2 * rem <= pairs.
+// tiles are split two ways (K ranges) when 2 * rem <= pairs.  For the gated
+// pair pass N = 2 x roundup(output columns, 128) (tiles of 128 columns).
 MainSplit main_gemm_split(int M, int N, int pairs);
 cudaError_t launch_main_gemm(const MainGemmArgs &a, int num_sms, cudaStream_t s);
 
@@ -103,5 +118,12 @@ cudaError_t launch_transpose_pad_bf16(const void *B, int d_out, int r, int r_pad
 // Bp[o * r_pad + j] = (j < r) ? B[o * r + j] : 0     for j < r_pad
 cudaError_t launch_pad_cols_bf16(const void *B, int d_out, int r, int r_pad, void *Bp,
                                  cudaStream_t s);
+// SwiGLU backward, elementwise: D = [dH * up * silu'(gate) | dH * silu(gate)]
+// ([M][2 half] bf16, columns [d_ff, half) of each half zero).
+cudaError_t launch_swiglu_grad_bf16(const void *dH, const void *gate, const void *up, int64_t M,
+                                    int d_ff, int half, void *D, int num_sms, cudaStream_t s);
+// dst [2 r_pad][d_in] = [Ag (r rows) ; 0 ; Au (r rows) ; 0].
+cudaError_t launch_stack_rows_bf16(const void *Ag, const void *Au, int r, int r_pad, int64_t d_in,
+                                   void *dst, cudaStream_t s);
 
 }  // namespace lora

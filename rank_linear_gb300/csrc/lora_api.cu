@@ -13,6 +13,7 @@
 
 #include "internal.h"
 #include "lora_linear.h"
+#include "lora_swiglu.h"
 #include "ptx.cuh"
 
 namespace lora {
@@ -561,6 +562,284 @@ lora_status_t bwd_f32(const void *dY, const void *X, const void *W, const void *
   return gemm32(LORA_K_GRAD_A, "dA pass (fp32)", b3, st);
 }
 
+// ---------------------------------------------------------------- SwiGLU pair
+// Byte layout of the gated pair's saved buffer and workspace (bf16).
+struct SwPlan {
+  int r_pad = 0;
+  int64_t Mp = 0, half = 0;  // half: d_ff rounded up to 64 (a column block of D)
+  size_t gate_off = 0, up_off = 0, sh_off = 0, sht_off[2] = {0, 0}, saved = 0;
+  size_t bpad_off[2] = {0, 0}, fsplit_off = 0, fcnt_off = 0, fwd_ws = 0, fwd_ws_min = 0;
+  size_t d_off = 0, sg_off = 0, sgt_off[2] = {0, 0}, agu_off = 0, bt_off[2] = {0, 0};
+  size_t bsplit_off = 0, bcnt_off = 0, bwd_ws = 0, bwd_ws_min = 0;
+  MainSplit fsplit, bsplit;
+};
+
+SwPlan make_sw_plan(int64_t M, int64_t d_in, int64_t d_ff, int r, int pairs_f, int pairs_b) {
+  SwPlan P;
+  P.r_pad = static_cast<int>(rup(r, 16));
+  P.Mp = rup(M, 8);
+  P.half = rup(d_ff, 64);
+  const size_t act = rup(size_t(M) * d_ff * 2, 256);
+  const size_t tr = rup(size_t(P.r_pad) * P.Mp * 2, 256);
+  // saved: [gate] [up] [sH_g | sH_u] [sH_g^T] [sH_u^T]
+  size_t off = 0;
+  P.gate_off = off;
+  off += act;
+  P.up_off = off;
+  off += act;
+  P.sh_off = off;
+  off += rup(size_t(M) * 2 * P.r_pad * 2, 256);
+  for (int p = 0; p < 2; ++p) {
+    P.sht_off[p] = off;
+    off += tr;
+  }
+  P.saved = M > 0 ? off : 0;
+  // forward workspace: [Bg, Bu padded (r % 8 != 0)] [split partials] [counters]
+  off = 0;
+  for (int p = 0; p < 2; ++p) {
+    P.bpad_off[p] = off;
+    if (r % 8) off += rup(size_t(d_ff) * P.r_pad * 2, 256);
+  }
+  P.fwd_ws_min = off;
+  if (pairs_f > 0 && M > 0) P.fsplit = main_gemm_split(int(M), int(2 * rup(d_ff, 128)), pairs_f);
+  P.fsplit_off = off;
+  off += rup(P.fsplit.partial_bytes, 256);
+  P.fcnt_off = off;
+  off += rup(P.fsplit.counter_bytes, 256);
+  P.fwd_ws = M > 0 ? (P.fsplit.k > 1 ? off : P.fwd_ws_min) : 0;
+  // backward workspace: [D = d_gate | d_up] [sG_g | sG_u] [sG_g^T] [sG_u^T]
+  // [Ag ; Au] [Bg^T, Bu^T (r % 8 != 0)] [split partials] [counters]
+  off = 0;
+  P.d_off = off;
+  off += rup(size_t(M) * 2 * P.half * 2, 256);
+  P.sg_off = off;
+  off += rup(size_t(M) * 2 * P.r_pad * 2, 256);
+  for (int p = 0; p < 2; ++p) {
+    P.sgt_off[p] = off;
+    off += tr;
+  }
+  P.agu_off = off;
+  off += rup(size_t(2) * P.r_pad * d_in * 2, 256);
+  for (int p = 0; p < 2; ++p) {
+    P.bt_off[p] = off;
+    if (r % 8) off += rup(size_t(P.r_pad) * d_ff * 2, 256);
+  }
+  P.bwd_ws_min = M > 0 ? off : 0;
+  if (pairs_b > 0 && M > 0) P.bsplit = main_gemm_split(int(M), int(d_in), pairs_b);
+  P.bsplit_off = off;
+  off += rup(P.bsplit.partial_bytes, 256);
+  P.bcnt_off = off;
+  off += rup(P.bsplit.counter_bytes, 256);
+  P.bwd_ws = M > 0 ? (P.bsplit.k > 1 ? off : P.bwd_ws_min) : 0;
+  return P;
+}
+
+lora_status_t sw_fwd_bf16(const void *X, const void *Wg, const void *Ag, const void *Bg,
+                          const void *Wu, const void *Au, const void *Bu, float alpha, int r,
+                          int64_t M, int64_t d_in, int64_t d_ff, void *H, void *saved, void *ws,
+                          size_t ws_bytes, cudaStream_t st) {
+  DevInfo di;
+  LORA_TRY(device_info(di));
+  SwPlan P = make_sw_plan(M, d_in, d_ff, r, main_gemm_pairs(false, di.sms), 0);
+  const bool split = P.fsplit.k > 1 && ws != nullptr && ws_bytes >= P.fwd_ws;
+  if (!split) P = make_sw_plan(M, d_in, d_ff, r, 0, 0);
+  unsigned *counters = split ? reinterpret_cast<unsigned *>(at(ws, P.fcnt_off)) : nullptr;
+  const float s = alpha / static_cast<float>(r);
+  const void *A2[2] = {Ag, Au};
+  const void *Bsrc[2] = {Bg, Bu};
+  int64_t b_inner = r;
+  if (r % 8 != 0) {  // B's row pitch is not a multiple of 16 bytes: pad it
+    for (int p = 0; p < 2; ++p) {
+      void *Bp = at(ws, P.bpad_off[p]);
+      const void *B = Bsrc[p];
+      LORA_TRY(run(LORA_K_PREP, st, "pad B", [&] {
+        return launch_pad_cols_bf16(B, static_cast<int>(d_ff), r, P.r_pad, Bp, st);
+      }));
+      Bsrc[p] = Bp;
+    }
+    b_inner = P.r_pad;
+  }
+  uint8_t *sh = static_cast<uint8_t *>(saved) + P.sh_off;
+  // [s X Ag^T | s X Au^T] (and transposes): one launch, both read X
+  SkinnyArgs f[2];
+  for (int p = 0; p < 2; ++p) {
+    LORA_TRY(tmap(&f[p].tmA, X, d_in, M, d_in * 2, 64, 128, "X"));
+    LORA_TRY(tmap(&f[p].tmB, A2[p], d_in, r, d_in * 2, 64, P.r_pad, p ? "Au" : "Ag"));
+    f[p].a_mn = false;
+    f[p].rows = static_cast<int>(M);
+    f[p].RP = P.r_pad;
+    f[p].K = static_cast<int>(d_in);
+    f[p].scale = s;
+    f[p].out0 = sh + size_t(p) * P.r_pad * 2;
+    f[p].ld0 = 2 * P.r_pad;
+    f[p].n0 = P.r_pad;
+    f[p].out1 = at(saved, P.sht_off[p]);
+    f[p].ld1 = P.Mp;
+    f[p].n1 = P.r_pad;
+    f[p].dev_status = di.status;
+  }
+  f[0].zero_ptr = counters;  // the gated GEMM's split counters
+  f[0].zero_words = split ? 2 * P.fsplit.rem : 0;
+  LORA_TRY(run(LORA_K_DOWN_FWD, st, "s X A^T passes (gate, up)",
+               [&] { return launch_skinny(f, 2, di.sms, st); }));
+
+  MainGemmArgs g;
+  g.gated = true;
+  g.bn = 256;
+  LORA_TRY(tmap(&g.tmA, X, d_in, M, d_in * 2, 64, 128, "X"));
+  LORA_TRY(tmap(&g.tmB, Wg, d_in, d_ff, d_in * 2, 64, 128, "Wg"));
+  LORA_TRY(tmap(&g.tmB3, Wu, d_in, d_ff, d_in * 2, 64, 128, "Wu"));
+  LORA_TRY(tmap(&g.tmA2, sh, 2 * P.r_pad, M, 2 * P.r_pad * 2, 64, 128, "[sH_g | sH_u]"));
+  LORA_TRY(tmap(&g.tmB2, Bsrc[0], b_inner, d_ff, b_inner * 2, 64, 128, "Bg"));
+  LORA_TRY(tmap(&g.tmB4, Bsrc[1], b_inner, d_ff, b_inner * 2, 64, 128, "Bu"));
+  g.M = static_cast<int>(M);
+  g.N = static_cast<int>(d_ff);
+  g.kb_main = static_cast<int>((d_in + 63) / 64);
+  g.k_ext = 2 * P.r_pad;
+  g.ext_shift = P.r_pad;
+  g.out = H;
+  g.aux0 = at(saved, P.gate_off);
+  g.aux1 = at(saved, P.up_off);
+  g.ldo = d_ff;
+  g.b_mn = false;
+  g.dev_status = di.status;
+  if (split) {
+    g.split_k = P.fsplit.k;
+    g.split_rem = P.fsplit.rem;
+    g.partials = reinterpret_cast<float *>(at(ws, P.fsplit_off));
+    g.counters = counters;
+  }
+  return run(LORA_K_MAIN_FWD, st, "gated GEMM", [&] { return launch_main_gemm(g, di.sms, st); });
+}
+
+lora_status_t sw_bwd_bf16(const void *dH, const void *X, const void *Wg, const void *Ag,
+                          const void *Bg, const void *Wu, const void *Au, const void *Bu,
+                          const void *saved, float alpha, int r, int64_t M, int64_t d_in,
+                          int64_t d_ff, void *dX, void *dAg, void *dBg, void *dAu, void *dBu,
+                          void *ws, size_t ws_bytes, cudaStream_t st) {
+  DevInfo di;
+  LORA_TRY(device_info(di));
+  SwPlan P = make_sw_plan(M, d_in, d_ff, r, 0, main_gemm_pairs(true, di.sms));
+  const bool split = dX != nullptr && P.bsplit.k > 1 && ws != nullptr && ws_bytes >= P.bwd_ws;
+  if (!split) P = make_sw_plan(M, d_in, d_ff, r, 0, 0);
+  unsigned *counters = split ? reinterpret_cast<unsigned *>(at(ws, P.bcnt_off)) : nullptr;
+  const float s = alpha / static_cast<float>(r);
+  const uint8_t *sv = static_cast<const uint8_t *>(saved);
+  uint8_t *D = static_cast<uint8_t *>(at(ws, P.d_off));
+  uint8_t *sG = static_cast<uint8_t *>(at(ws, P.sg_off));
+  const int64_t half = P.half;
+
+  // D = [d_gate | d_up]
+  LORA_TRY(run(LORA_K_SWIGLU_GRAD, st, "SwiGLU backward (elementwise)", [&] {
+    return launch_swiglu_grad_bf16(dH, sv + P.gate_off, sv + P.up_off, M, static_cast<int>(d_ff),
+                                   static_cast<int>(half), D, di.sms, st);
+  }));
+
+  // per projection: s D_p B_p (and its transpose) and dB_p = D_p^T sH_p,
+  // one launch (both read D_p)
+  const void *Bs[2] = {Bg, Bu};
+  void *dBs[2] = {dBg, dBu};
+  for (int p = 0; p < 2; ++p) {
+    const uint8_t *Dp = D + size_t(p) * half * 2;
+    SkinnyArgs g[2];
+    SkinnyArgs &b1 = g[0];
+    LORA_TRY(tmap(&b1.tmA, Dp, d_ff, M, 2 * half * 2, 64, 128, p ? "d_up" : "d_gate"));
+    if (r % 8 == 0) {
+      LORA_TRY(tmap(&b1.tmB, Bs[p], r, d_ff, int64_t(r) * 2, 64, 64, "B (MN-major)"));
+      b1.b_mn = true;
+    } else {
+      void *Bt = at(ws, P.bt_off[p]);
+      const void *B = Bs[p];
+      LORA_TRY(run(LORA_K_PREP, st, "transpose B", [&] {
+        return launch_transpose_pad_bf16(B, static_cast<int>(d_ff), r, P.r_pad, Bt, st);
+      }));
+      LORA_TRY(tmap(&b1.tmB, Bt, d_ff, P.r_pad, d_ff * 2, 64, P.r_pad, "B^T"));
+      b1.b_mn = false;
+    }
+    b1.a_mn = false;
+    b1.rows = static_cast<int>(M);
+    b1.RP = P.r_pad;
+    b1.K = static_cast<int>(d_ff);
+    b1.scale = s;
+    b1.out0 = sG + size_t(p) * P.r_pad * 2;
+    b1.ld0 = 2 * P.r_pad;
+    b1.n0 = P.r_pad;
+    b1.out1 = at(ws, P.sgt_off[p]);
+    b1.ld1 = P.Mp;
+    b1.n1 = P.r_pad;
+    b1.dev_status = di.status;
+    if (p == 0) {
+      b1.zero_ptr = counters;  // the dX GEMM's split counters
+      b1.zero_words = split ? 2 * P.bsplit.rem : 0;
+    }
+    SkinnyArgs &b4 = g[1];
+    LORA_TRY(tmap(&b4.tmA, Dp, d_ff, M, 2 * half * 2, 64, 64, "D^T"));
+    LORA_TRY(tmap(&b4.tmB, sv + P.sht_off[p], M, P.r_pad, P.Mp * 2, 64, P.r_pad, "sH^T"));
+    b4.a_mn = true;
+    b4.rows = static_cast<int>(d_ff);
+    b4.RP = P.r_pad;
+    b4.K = static_cast<int>(M);
+    b4.scale = 1.f;
+    b4.out0 = dBs[p];
+    b4.ld0 = r;
+    b4.n0 = r;
+    b4.dev_status = di.status;
+    LORA_TRY(run(LORA_K_DOWN_BWD_GRAD_B, st, "s D B and dB pass",
+                 [&] { return launch_skinny(g, 2, di.sms, st); }));
+  }
+
+  // dX = [d_gate | d_up | sG_g | sG_u] . [Wg ; Wu ; Ag ; Au]
+  if (dX != nullptr) {
+    void *Agu = at(ws, P.agu_off);
+    LORA_TRY(run(LORA_K_PREP, st, "stack Ag, Au", [&] {
+      return launch_stack_rows_bf16(Ag, Au, r, P.r_pad, d_in, Agu, st);
+    }));
+    MainGemmArgs b2;
+    b2.bn = 256;
+    LORA_TRY(tmap(&b2.tmA, D, 2 * half, M, 2 * half * 2, 64, 128, "[d_gate | d_up]"));
+    LORA_TRY(tmap(&b2.tmB, Wg, d_in, d_ff, d_in * 2, 64, 64, "Wg (MN-major)"));
+    LORA_TRY(tmap(&b2.tmB3, Wu, d_in, d_ff, d_in * 2, 64, 64, "Wu (MN-major)"));
+    LORA_TRY(tmap(&b2.tmA2, sG, 2 * P.r_pad, M, 2 * P.r_pad * 2, 64, 128, "[sG_g | sG_u]"));
+    LORA_TRY(tmap(&b2.tmB2, Agu, d_in, 2 * P.r_pad, d_in * 2, 64, 64, "[Ag ; Au] (MN-major)"));
+    b2.M = static_cast<int>(M);
+    b2.N = static_cast<int>(d_in);
+    b2.kb_main = static_cast<int>(2 * half / 64);
+    b2.kb_switch = static_cast<int>(half / 64);
+    b2.k_ext = 2 * P.r_pad;
+    b2.out = dX;
+    b2.ldo = d_in;
+    b2.b_mn = true;
+    b2.dev_status = di.status;
+    if (split) {
+      b2.split_k = P.bsplit.k;
+      b2.split_rem = P.bsplit.rem;
+      b2.partials = reinterpret_cast<float *>(at(ws, P.bsplit_off));
+      b2.counters = counters;
+    }
+    LORA_TRY(run(LORA_K_MAIN_BWD, st, "gated dX GEMM",
+                 [&] { return launch_main_gemm(b2, di.sms, st); }));
+  }
+
+  // dA_p^T = X^T sG_p, written transposed into dA_p: one launch, both read X
+  SkinnyArgs a[2];
+  void *dAs[2] = {dAg, dAu};
+  for (int p = 0; p < 2; ++p) {
+    LORA_TRY(tmap(&a[p].tmA, X, d_in, M, d_in * 2, 64, 64, "X^T"));
+    LORA_TRY(tmap(&a[p].tmB, at(ws, P.sgt_off[p]), M, P.r_pad, P.Mp * 2, 64, P.r_pad, "sG^T"));
+    a[p].a_mn = true;
+    a[p].rows = static_cast<int>(d_in);
+    a[p].RP = P.r_pad;
+    a[p].K = static_cast<int>(M);
+    a[p].scale = 1.f;
+    a[p].out1 = dAs[p];
+    a[p].ld1 = d_in;
+    a[p].n1 = r;
+    a[p].dev_status = di.status;
+  }
+  return run(LORA_K_GRAD_A, st, "dA passes (gate, up)",
+             [&] { return launch_skinny(a, 2, di.sms, st); });
+}
+
 }  // namespace
 }  // namespace lora
 
@@ -766,6 +1045,104 @@ lora_status_t lora_set_timing_events(void *const *events, int *kinds, int n_pair
 }
 
 int lora_timing_used(void) { return t_hook.used; }
+
+// ---------------------------------------------------------------- SwiGLU pair
+static lora_status_t check_sw_shape(int r, int64_t M, int64_t d_in, int64_t d_ff,
+                                    lora_dtype_t dt, float alpha) {
+  if (dt == LORA_FP32) return fail(LORA_ERR_UNSUPPORTED, "the SwiGLU pair is built for bf16 only");
+  LORA_TRY(check_shape(r, M, d_in, d_ff, dt, alpha));
+  // the gated GEMM's tiles are 128 output columns wide
+  const int64_t t = ((M + 127) / 128) * ((d_ff + 127) / 128);
+  if (t > INT32_MAX / 2) return fail(LORA_ERR_UNSUPPORTED, "too many output tiles");
+  return LORA_OK;
+}
+
+static int current_pairs(bool b_mn) {
+  int pairs = 76;  // a GB300's, when no usable device is current
+  int dev = 0, sms = 0, major = 0, minor = 0;
+  if (cudaGetDevice(&dev) == cudaSuccess &&
+      cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) == cudaSuccess &&
+      cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev) == cudaSuccess &&
+      cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev) == cudaSuccess &&
+      major == 10 && minor == 3)
+    pairs = main_gemm_pairs(b_mn, sms);
+  cudaGetLastError();
+  return pairs;
+}
+
+size_t lora_swiglu_saved_bytes(int64_t M, int64_t d_ff, int r) {
+  if (M < 0 || d_ff < 1 || r < 1 || r > 256) return 0;
+  return make_sw_plan(M, 1, d_ff, r, 0, 0).saved;
+}
+
+size_t lora_swiglu_workspace_bytes(int64_t M, int64_t d_in, int64_t d_ff, int r) {
+  if (M < 0 || d_in < 1 || d_ff < 1 || r < 1 || r > 256) return 0;
+  const SwPlan P = make_sw_plan(M, d_in, d_ff, r, current_pairs(false), current_pairs(true));
+  return P.fwd_ws > P.bwd_ws ? P.fwd_ws : P.bwd_ws;
+}
+
+lora_status_t lora_swiglu_fwd(const void *X, const void *Wg, const void *Ag, const void *Bg,
+                              const void *Wu, const void *Au, const void *Bu, float alpha,
+                              int r, int64_t M, int64_t d_in, int64_t d_ff, lora_dtype_t dtype,
+                              void *H, void *saved, void *workspace, size_t workspace_bytes,
+                              void *stream) {
+  t_err.clear();
+  LORA_TRY(check_sw_shape(r, M, d_in, d_ff, dtype, alpha));
+  const bool empty = M == 0;
+  LORA_TRY(check_ptr(X, "X", empty));
+  LORA_TRY(check_ptr(Wg, "Wg"));
+  LORA_TRY(check_ptr(Ag, "Ag"));
+  LORA_TRY(check_ptr(Bg, "Bg"));
+  LORA_TRY(check_ptr(Wu, "Wu"));
+  LORA_TRY(check_ptr(Au, "Au"));
+  LORA_TRY(check_ptr(Bu, "Bu"));
+  LORA_TRY(check_ptr(H, "H", empty));
+  LORA_TRY(check_ptr(saved, "saved", empty));
+  const SwPlan P = make_sw_plan(M, d_in, d_ff, r, 0, 0);
+  LORA_TRY(check_ws(workspace, workspace_bytes, P.fwd_ws_min));
+  if (empty) return LORA_OK;
+  return sw_fwd_bf16(X, Wg, Ag, Bg, Wu, Au, Bu, alpha, r, M, d_in, d_ff, H, saved, workspace,
+                     workspace_bytes, static_cast<cudaStream_t>(stream));
+}
+
+lora_status_t lora_swiglu_bwd(const void *dH, const void *X, const void *Wg, const void *Ag,
+                              const void *Bg, const void *Wu, const void *Au, const void *Bu,
+                              const void *saved, float alpha, int r, int64_t M, int64_t d_in,
+                              int64_t d_ff, lora_dtype_t dtype, void *dX, void *dAg, void *dBg,
+                              void *dAu, void *dBu, void *workspace, size_t workspace_bytes,
+                              void *stream) {
+  t_err.clear();
+  LORA_TRY(check_sw_shape(r, M, d_in, d_ff, dtype, alpha));
+  const bool empty = M == 0;
+  LORA_TRY(check_ptr(dH, "dH", empty));
+  LORA_TRY(check_ptr(X, "X", empty));
+  LORA_TRY(check_ptr(Wg, "Wg"));
+  LORA_TRY(check_ptr(Ag, "Ag"));
+  LORA_TRY(check_ptr(Bg, "Bg"));
+  LORA_TRY(check_ptr(Wu, "Wu"));
+  LORA_TRY(check_ptr(Au, "Au"));
+  LORA_TRY(check_ptr(Bu, "Bu"));
+  LORA_TRY(check_ptr(saved, "saved", empty));
+  LORA_TRY(check_ptr(dX, "dX", true));
+  LORA_TRY(check_ptr(dAg, "dAg"));
+  LORA_TRY(check_ptr(dBg, "dBg"));
+  LORA_TRY(check_ptr(dAu, "dAu"));
+  LORA_TRY(check_ptr(dBu, "dBu"));
+  const SwPlan P = make_sw_plan(M, d_in, d_ff, r, 0, 0);
+  LORA_TRY(check_ws(workspace, workspace_bytes, empty ? 0 : P.bwd_ws_min));
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  if (empty) {  // sums over zero tokens
+    cudaError_t e = cudaSuccess;
+    for (void *p : {dAg, dAu})
+      if (e == cudaSuccess) e = cudaMemsetAsync(p, 0, size_t(r) * d_in * 2, st);
+    for (void *p : {dBg, dBu})
+      if (e == cudaSuccess) e = cudaMemsetAsync(p, 0, size_t(d_ff) * r * 2, st);
+    if (e != cudaSuccess) return fail(LORA_ERR_CUDA, "zero dA/dB: %s", cudaGetErrorString(e));
+    return LORA_OK;
+  }
+  return sw_bwd_bf16(dH, X, Wg, Ag, Bg, Wu, Au, Bu, saved, alpha, r, M, d_in, d_ff, dX, dAg, dBg,
+                     dAu, dBu, workspace, workspace_bytes, st);
+}
 
 lora_status_t lora_debug_withhold_arrive(int n) {
   t_err.clear();

@@ -89,6 +89,72 @@ __global__ void k_pad_cols(const __nv_bfloat16 *__restrict__ B, int d_out, int r
   }
 }
 
+// SwiGLU backward, elementwise (ch05 "Acceleration principles: Triton kernels
+// and fused LoRA", §5.6; the derivative of silu(g) * u), 8 columns per
+// thread, fp32 arithmetic, one rounding to bf16:
+//   D[m][j]        = dH * u * silu'(g),  silu'(g) = sig(g) (1 + g (1 - sig(g)))
+//   D[m][half + j] = dH * silu(g),       silu(g) = g sig(g)
+// for j < d_ff, with D's row pitch 2 * half; columns [d_ff, half) of both
+// halves are written as zero.  d_ff and half are multiples of 8.
+__global__ void k_swiglu_grad(const __nv_bfloat16 *__restrict__ dH,
+                              const __nv_bfloat16 *__restrict__ gate,
+                              const __nv_bfloat16 *__restrict__ up, int64_t M, int d_ff,
+                              int half, __nv_bfloat16 *__restrict__ D) {
+  griddep_wait();
+  griddep_launch_dependents();
+  const int per_row = half / 8;
+  const int64_t total = M * per_row;
+  for (int64_t v = blockIdx.x * int64_t(blockDim.x) + threadIdx.x; v < total;
+       v += int64_t(gridDim.x) * blockDim.x) {
+    const int64_t m = v / per_row;
+    const int j = static_cast<int>(v % per_row) * 8;
+    uint4 dg = make_uint4(0u, 0u, 0u, 0u), du = dg;
+    if (j < d_ff) {
+      const int64_t src = m * d_ff + j;
+      const uint4 h4 = *reinterpret_cast<const uint4 *>(dH + src);
+      const uint4 g4 = *reinterpret_cast<const uint4 *>(gate + src);
+      const uint4 u4 = *reinterpret_cast<const uint4 *>(up + src);
+      const __nv_bfloat162 *h2 = reinterpret_cast<const __nv_bfloat162 *>(&h4);
+      const __nv_bfloat162 *g2 = reinterpret_cast<const __nv_bfloat162 *>(&g4);
+      const __nv_bfloat162 *u2 = reinterpret_cast<const __nv_bfloat162 *>(&u4);
+      __nv_bfloat162 *o_g = reinterpret_cast<__nv_bfloat162 *>(&dg);
+      __nv_bfloat162 *o_u = reinterpret_cast<__nv_bfloat162 *>(&du);
+#pragma unroll
+      for (int i = 0; i < 4; ++i) {
+        const float2 h = __bfloat1622float2(h2[i]);
+        const float2 g = __bfloat1622float2(g2[i]);
+        const float2 u = __bfloat1622float2(u2[i]);
+        const float s0 = 1.f / (1.f + expf(-g.x)), s1 = 1.f / (1.f + expf(-g.y));
+        o_g[i] = __floats2bfloat162_rn(h.x * u.x * s0 * (1.f + g.x * (1.f - s0)),
+                                       h.y * u.y * s1 * (1.f + g.y * (1.f - s1)));
+        o_u[i] = __floats2bfloat162_rn(h.x * g.x * s0, h.y * g.y * s1);
+      }
+    }
+    __nv_bfloat16 *row = D + m * 2 * int64_t(half);
+    *reinterpret_cast<uint4 *>(row + j) = dg;
+    *reinterpret_cast<uint4 *>(row + half + j) = du;
+  }
+}
+
+// dst [2 r_pad][d_in]: rows [0, r) = Ag, rows [r_pad, r_pad + r) = Au, the
+// other rows zero (the extension operand [Ag ; Au] of the gated dX GEMM).
+__global__ void k_stack_rows(const __nv_bfloat16 *__restrict__ Ag,
+                             const __nv_bfloat16 *__restrict__ Au, int r, int r_pad,
+                             int64_t d_in, __nv_bfloat16 *__restrict__ dst) {
+  griddep_wait();
+  griddep_launch_dependents();
+  const int64_t total = 2 * int64_t(r_pad) * d_in;
+  for (int64_t i = blockIdx.x * int64_t(blockDim.x) + threadIdx.x; i < total;
+       i += int64_t(gridDim.x) * blockDim.x) {
+    const int row = static_cast<int>(i / d_in);
+    const int64_t k = i % d_in;
+    __nv_bfloat16 v = __float2bfloat16_rn(0.f);
+    if (row < r) v = Ag[row * d_in + k];
+    else if (row >= r_pad && row < r_pad + r) v = Au[(row - r_pad) * d_in + k];
+    dst[i] = v;
+  }
+}
+
 // Launch with programmatic stream serialisation allowed (every kernel of the
 // library waits on griddep_wait before touching global memory).
 template <typename... KArgs, typename... Args>
@@ -108,6 +174,29 @@ cudaError_t launch_pdl(void (*kern)(KArgs...), dim3 grid, dim3 block, cudaStream
 }
 
 }  // namespace
+
+cudaError_t launch_swiglu_grad_bf16(const void *dH, const void *gate, const void *up, int64_t M,
+                                    int d_ff, int half, void *D, int num_sms, cudaStream_t s) {
+  if (M <= 0) return cudaSuccess;
+  const int64_t vecs = M * (half / 8);
+  const int64_t want = (vecs + 255) / 256;
+  const int blocks = static_cast<int>(want < 8LL * num_sms ? want : 8LL * num_sms);
+  return launch_pdl(k_swiglu_grad, dim3(blocks), dim3(256), s,
+                    static_cast<const __nv_bfloat16 *>(dH),
+                    static_cast<const __nv_bfloat16 *>(gate),
+                    static_cast<const __nv_bfloat16 *>(up), M, d_ff, half,
+                    static_cast<__nv_bfloat16 *>(D));
+}
+
+cudaError_t launch_stack_rows_bf16(const void *Ag, const void *Au, int r, int r_pad, int64_t d_in,
+                                   void *dst, cudaStream_t s) {
+  const int64_t total = 2 * int64_t(r_pad) * d_in;
+  const int blocks = static_cast<int>(total / 256 + 1 < 4096 ? total / 256 + 1 : 4096);
+  return launch_pdl(k_stack_rows, dim3(blocks), dim3(256), s,
+                    static_cast<const __nv_bfloat16 *>(Ag),
+                    static_cast<const __nv_bfloat16 *>(Au), r, r_pad, d_in,
+                    static_cast<__nv_bfloat16 *>(dst));
+}
 
 cudaError_t launch_f32_gemm(const F32GemmArgs &a, cudaStream_t s) {
   if (a.M <= 0 || a.N <= 0) return cudaSuccess;

@@ -146,13 +146,46 @@ __device__ __forceinline__ void store_chunk(const uint32_t (&pk)[16], uint8_t *s
   __syncwarp();
 }
 
-template <bool B_MN, int BN, bool SPLIT>
+// Gated (SwiGLU) epilogue of one 32-column chunk (ch05 "Acceleration
+// principles: Triton kernels and fused LoRA", §5.6: SiLU and the elementwise
+// product fused into the matmul epilogue): from fp32 gate g and up u, writes
+// bf16 silu(g) * u to out, and g and u themselves (kept for the backward) to
+// aux0 and aux1 (skipped when null).  silu(z) = z / (1 + e^-z).
+__device__ __forceinline__ void store_gated(const float (&g)[32], const float (&u)[32],
+                                           uint8_t *stage, int lane, __nv_bfloat16 *out,
+                                           __nv_bfloat16 *aux0, __nv_bfloat16 *aux1,
+                                           int64_t ldo, int row0, int col0, int M, int N) {
+  uint32_t pk[16];
+  if (aux0 != nullptr) {
+#pragma unroll
+    for (int i = 0; i < 16; ++i) pk[i] = pack_bf16x2(g[2 * i], g[2 * i + 1]);
+    store_chunk(pk, stage, lane, aux0, ldo, row0, col0, M, N);
+  }
+  if (aux1 != nullptr) {
+#pragma unroll
+    for (int i = 0; i < 16; ++i) pk[i] = pack_bf16x2(u[2 * i], u[2 * i + 1]);
+    store_chunk(pk, stage, lane, aux1, ldo, row0, col0, M, N);
+  }
+#pragma unroll
+  for (int i = 0; i < 16; ++i) {
+    const float h0 = g[2 * i] / (1.f + expf(-g[2 * i])) * u[2 * i];
+    const float h1 = g[2 * i + 1] / (1.f + expf(-g[2 * i + 1])) * u[2 * i + 1];
+    pk[i] = pack_bf16x2(h0, h1);
+  }
+  store_chunk(pk, stage, lane, out, ldo, row0, col0, M, N);
+}
+
+template <bool B_MN, int BN, bool SPLIT, bool GATED>
 __global__ void __launch_bounds__(NUM_THREADS, 1)
     k_main_gemm(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                 const __grid_constant__ CUtensorMap tmA2, const __grid_constant__ CUtensorMap tmB2,
-                int M, int N, int kb_main, int k_ext, __nv_bfloat16 *__restrict__ out, int64_t ldo,
-                int split_k, int split_rem, float *__restrict__ partials, unsigned *counters,
-                unsigned *dev_status) {
+                const __grid_constant__ CUtensorMap tmB3, const __grid_constant__ CUtensorMap tmB4,
+                int M, int N, int kb_main, int k_ext, int kb_switch, int ext_shift,
+                __nv_bfloat16 *__restrict__ out, __nv_bfloat16 *__restrict__ aux0,
+                __nv_bfloat16 *__restrict__ aux1, int64_t ldo, int split_k, int split_rem,
+                float *__restrict__ partials, unsigned *counters, unsigned *dev_status) {
+  static_assert(!(GATED && B_MN), "the gated pair reads K-major B");
+  constexpr int TN = GATED ? BN / 2 : BN;  // output columns per pair tile
   using G = Geo<BN>;
   constexpr int STAGES = G::STAGES;
   constexpr uint32_t B_BYTES = G::B_BYTES, STAGE_BYTES = G::STAGE_BYTES, PAIR_TX = G::PAIR_TX;
@@ -169,7 +202,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
   const int q = static_cast<int>(cluster_ctarank());  // 0: even (MMA-issuing) CTA, 1: odd
   const bool leader = q == 0;
   const int pair_id = blockIdx.x / CLUSTER, num_pairs = gridDim.x / CLUSTER;
-  const int m_tiles = (M + BM - 1) / BM, n_tiles = (N + BN - 1) / BN;
+  const int m_tiles = (M + BM - 1) / BM, n_tiles = (N + TN - 1) / TN;
   const int m_pairs = (m_tiles + 1) / 2;
   const int num_tiles = m_pairs * n_tiles;
   const int kb_total = kb_main + (k_ext + BK - 1) / BK;
@@ -236,7 +269,9 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         int mp, nb;
         tile_coords(tile, m_pairs, n_tiles, mp, nb);
         const int m0 = (2 * mp + q) * BM;
-        const int n0 = nb * BN + q * (BN / 2);  // this CTA's half of the B tile
+        // this CTA's half of the B tile: columns q*BN/2.. of the tile, or for
+        // the gated pair the same TN rows of its own projection
+        const int n0 = GATED ? nb * TN : nb * BN + q * (BN / 2);
         for (int kb = kb_lo; kb < kb_hi; ++kb) {
           if (!mbar_wait(smem_u32(&tail->empty[stage]), phase ^ 1u, abort_flag, dev_status)) {
             ok = false;
@@ -251,15 +286,30 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
             dep_done = true;
           }
           const CUtensorMap *ta = ext ? &tmA2 : &tmA;
-          const CUtensorMap *tb = ext ? &tmB2 : &tmB;
-          const int k0 = (ext ? kb - kb_main : kb) * BK;
+          const int k0 = (ext ? kb - kb_main : kb) * BK;  // K of A
+          // B: the odd CTA of the gated pair reads the up projection (its
+          // extension shifted so it meets the second half of [sH_g | sH_u]);
+          // otherwise the main segment switches to tmB3 at kb_switch
+          const CUtensorMap *tb;
+          int kB = k0;
+          if (ext) {
+            tb = (GATED && q) ? &tmB4 : &tmB2;
+            if (GATED && q) kB = k0 - ext_shift;
+          } else if (GATED) {
+            tb = q ? &tmB3 : &tmB;
+          } else if (kb >= kb_switch) {
+            tb = &tmB3;
+            kB = (kb - kb_switch) * BK;
+          } else {
+            tb = &tmB;
+          }
           tma_load_2d_pair(sA + stage * A_BYTES, ta, full, k0, m0);
           if (B_MN) {  // BN/128 boxes of [64 K x 64 N]
 #pragma unroll
             for (int j = 0; j < BN / 128; ++j)
-              tma_load_2d_pair(sB + stage * B_BYTES + j * 8192u, tb, full, n0 + 64 * j, k0);
+              tma_load_2d_pair(sB + stage * B_BYTES + j * 8192u, tb, full, n0 + 64 * j, kB);
           } else {  // BN/2 rows of [N x 64 K]
-            tma_load_2d_pair(sB + stage * B_BYTES, tb, full, k0, n0);
+            tma_load_2d_pair(sB + stage * B_BYTES, tb, full, kB, n0);
           }
           issued[stage] += 1;
           if (++stage == STAGES) {
@@ -394,14 +444,24 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
       uint8_t *stage = epi_stage + qd * EPI_WARP_BYTES;
       const int row0 = (2 * mp + q) * BM + qd * 32;
       if (!SPLIT || !split) {
+        if constexpr (GATED) {  // columns [0, TN) gate, [TN, 2 TN) up
 #pragma unroll 1
-        for (int c = 0; c < BN / 32; ++c) {
-          float v[32];
-          tmem_ld_32cols(taddr + c * 32, v);
-          uint32_t pk[16];
+          for (int c = 0; c < TN / 32; ++c) {
+            float g[32], u[32];
+            tmem_ld_32cols(taddr + c * 32, g);
+            tmem_ld_32cols(taddr + TN + c * 32, u);
+            store_gated(g, u, stage, lane, out, aux0, aux1, ldo, row0, nb * TN + c * 32, M, N);
+          }
+        } else {
+#pragma unroll 1
+          for (int c = 0; c < BN / 32; ++c) {
+            float v[32];
+            tmem_ld_32cols(taddr + c * 32, v);
+            uint32_t pk[16];
 #pragma unroll
-          for (int i = 0; i < 16; ++i) pk[i] = pack_bf16x2(v[2 * i], v[2 * i + 1]);
-          store_chunk(pk, stage, lane, out, ldo, row0, nb * BN + c * 32, M, N);
+            for (int i = 0; i < 16; ++i) pk[i] = pack_bf16x2(v[2 * i], v[2 * i + 1]);
+            store_chunk(pk, stage, lane, out, ldo, row0, nb * BN + c * 32, M, N);
+          }
         }
         tc_fence_before();
         __syncwarp();
@@ -456,18 +516,33 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
           break;
         }
         const float *part = reinterpret_cast<const float *>(smem_raw + (base - raw));
+        if constexpr (GATED) {
 #pragma unroll 1
-        for (int c = 0; c < BN / 32; ++c) {
-          float o[32];
+          for (int c = 0; c < TN / 32; ++c) {
+            float g[32], u[32];
+            tmem_ld_32cols(taddr + c * 32, g);
+            tmem_ld_32cols(taddr + TN + c * 32, u);
 #pragma unroll
-          for (int i = 0; i < 32; ++i) o[i] = part[(c * 32 + i) * BM + rl];
-          float v[32];
-          tmem_ld_32cols(taddr + c * 32, v);
-          uint32_t pk[16];
+            for (int i = 0; i < 32; ++i) {
+              g[i] += part[(c * 32 + i) * BM + rl];
+              u[i] += part[(TN + c * 32 + i) * BM + rl];
+            }
+            store_gated(g, u, stage, lane, out, aux0, aux1, ldo, row0, nb * TN + c * 32, M, N);
+          }
+        } else {
+#pragma unroll 1
+          for (int c = 0; c < BN / 32; ++c) {
+            float o[32];
 #pragma unroll
-          for (int i = 0; i < 16; ++i)
-            pk[i] = pack_bf16x2(v[2 * i] + o[2 * i], v[2 * i + 1] + o[2 * i + 1]);
-          store_chunk(pk, stage, lane, out, ldo, row0, nb * BN + c * 32, M, N);
+            for (int i = 0; i < 32; ++i) o[i] = part[(c * 32 + i) * BM + rl];
+            float v[32];
+            tmem_ld_32cols(taddr + c * 32, v);
+            uint32_t pk[16];
+#pragma unroll
+            for (int i = 0; i < 16; ++i)
+              pk[i] = pack_bf16x2(v[2 * i] + o[2 * i], v[2 * i + 1] + o[2 * i + 1]);
+            store_chunk(pk, stage, lane, out, ldo, row0, nb * BN + c * 32, M, N);
+          }
         }
       }
       if (sync_ok) sync_ok = epi_sync();  // the flag word is free again
@@ -491,9 +566,9 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
   }
 }
 
-template <bool B_MN, int BN, bool SPLIT>
+template <bool B_MN, int BN, bool SPLIT, bool GATED = false>
 constexpr auto kernel_of() {
-  return &k_main_gemm<B_MN, BN, SPLIT>;
+  return &k_main_gemm<B_MN, BN, SPLIT, GATED>;
 }
 
 int g_max_clusters[64][2] = {};
@@ -529,12 +604,13 @@ int max_clusters(int num_sms) {
   return n;
 }
 
-template <bool B_MN, int BN, bool SPLIT>
+template <bool B_MN, int BN, bool SPLIT, bool GATED>
 cudaError_t launch_variant(const MainGemmArgs &a, int num_sms, cudaStream_t s) {
-  const int m_tiles = (a.M + BM - 1) / BM, n_tiles = (a.N + BN - 1) / BN;
+  constexpr int TN = GATED ? BN / 2 : BN;
+  const int m_tiles = (a.M + BM - 1) / BM, n_tiles = (a.N + TN - 1) / TN;
   const int tiles = ((m_tiles + 1) / 2) * n_tiles;  // pair tiles
   if (tiles == 0) return cudaSuccess;
-  auto kern = kernel_of<B_MN, BN, SPLIT>();
+  auto kern = kernel_of<B_MN, BN, SPLIT, GATED>();
   constexpr size_t smem = smem_bytes<BN>();
   cudaError_t e =
       cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));
@@ -555,9 +631,16 @@ cudaError_t launch_variant(const MainGemmArgs &a, int num_sms, cudaStream_t s) {
   attr[1].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 2;
-  return cudaLaunchKernelEx(&cfg, kern, a.tmA, a.tmB, a.tmA2, a.tmB2, a.M, a.N, a.kb_main,
-                            a.k_ext, static_cast<__nv_bfloat16 *>(a.out), a.ldo, a.split_k,
-                            a.split_rem, a.partials, a.counters, a.dev_status);
+  // without a second B segment the switch point lies past every K block
+  const int kb_switch = a.kb_switch >= 0 ? a.kb_switch : (1 << 30);
+  const CUtensorMap &tmB3 = (GATED || a.kb_switch >= 0) ? a.tmB3 : a.tmB;
+  const CUtensorMap &tmB4 = GATED ? a.tmB4 : a.tmB2;
+  return cudaLaunchKernelEx(&cfg, kern, a.tmA, a.tmB, a.tmA2, a.tmB2, tmB3, tmB4, a.M, a.N,
+                            a.kb_main, a.k_ext, kb_switch, a.ext_shift,
+                            static_cast<__nv_bfloat16 *>(a.out),
+                            static_cast<__nv_bfloat16 *>(a.aux0),
+                            static_cast<__nv_bfloat16 *>(a.aux1), a.ldo, a.split_k, a.split_rem,
+                            a.partials, a.counters, a.dev_status);
 }
 
 }  // namespace
@@ -592,11 +675,16 @@ int main_gemm_pick_bn(int, int, int) { return 256; }
 
 cudaError_t launch_main_gemm(const MainGemmArgs &a, int num_sms, cudaStream_t s) {
   const bool split = a.split_k > 1 && a.split_rem > 0;
+  if (a.gated) {
+    if (a.b_mn) return cudaErrorInvalidValue;
+    return split ? launch_variant<false, 256, true, true>(a, num_sms, s)
+                 : launch_variant<false, 256, false, true>(a, num_sms, s);
+  }
   if (a.b_mn)
-    return split ? launch_variant<true, 256, true>(a, num_sms, s)
-                 : launch_variant<true, 256, false>(a, num_sms, s);
-  return split ? launch_variant<false, 256, true>(a, num_sms, s)
-               : launch_variant<false, 256, false>(a, num_sms, s);
+    return split ? launch_variant<true, 256, true, false>(a, num_sms, s)
+                 : launch_variant<true, 256, false, false>(a, num_sms, s);
+  return split ? launch_variant<false, 256, true, false>(a, num_sms, s)
+               : launch_variant<false, 256, false, false>(a, num_sms, s);
 }
 
 }  // namespace lora

@@ -146,3 +146,95 @@ def timing_events(n_pairs: int, stream=None):
 
 def launch_count() -> int:
     return int(_lib.lib().lora_launch_count())
+
+
+# ---------------------------------------------------------------- SwiGLU pair
+# H = silu(gate) * up with gate and up each a LoRA layer (ch05 "Acceleration
+# principles: Triton kernels and fused LoRA", §5.6 fused SwiGLU, over the
+# LoRA layer of §5.3); bf16 only.
+
+def swiglu_saved_bytes(M: int, d_ff: int, r: int) -> int:
+    return int(_lib.lib().lora_swiglu_saved_bytes(M, d_ff, r))
+
+
+def swiglu_workspace_bytes(M: int, d_in: int, d_ff: int, r: int) -> int:
+    return int(_lib.lib().lora_swiglu_workspace_bytes(M, d_in, d_ff, r))
+
+
+def swiglu_forward(X, Wg, Ag, Bg, Wu, Au, Bu, alpha: float, *, H=None, saved=None,
+                   workspace=None, stream=None):
+    """H = silu(gate) * up.  Returns (H, saved); saved holds gate and up."""
+    _check_dev(X, Wg, Ag, Bg, Wu, Au, Bu)
+    M, d_in = X.shape
+    d_ff, r = Bg.shape
+    dt = _dtype_code(X)
+    L = _lib.lib()
+    if H is None:
+        H = torch.empty(M, d_ff, dtype=X.dtype, device=X.device)
+    if saved is None:
+        saved = _buffer(L.lora_swiglu_saved_bytes(M, d_ff, r), X.device)
+    if workspace is None:
+        workspace = _buffer(L.lora_swiglu_workspace_bytes(M, d_in, d_ff, r), X.device)
+    st = L.lora_swiglu_fwd(_ptr(X), _ptr(Wg), _ptr(Ag), _ptr(Bg), _ptr(Wu), _ptr(Au), _ptr(Bu),
+                           float(alpha), r, M, d_in, d_ff, dt, _ptr(H), _ptr(saved),
+                           _ptr(workspace), workspace.numel(), _stream_ptr(stream))
+    _lib.check(st, "lora_swiglu_fwd")
+    return H, saved
+
+
+def swiglu_backward(dH, X, Wg, Ag, Bg, Wu, Au, Bu, alpha: float, saved, *, need_dX=True,
+                    dX=None, dAg=None, dBg=None, dAu=None, dBu=None, workspace=None,
+                    stream=None):
+    """Returns (dX or None, dAg, dBg, dAu, dBu) for the upstream gradient dH."""
+    _check_dev(dH, X, Wg, Ag, Bg, Wu, Au, Bu)
+    M, d_in = X.shape
+    d_ff, r = Bg.shape
+    dt = _dtype_code(X)
+    L = _lib.lib()
+    new = lambda *s: torch.empty(*s, dtype=X.dtype, device=X.device)
+    if need_dX and dX is None:
+        dX = new(M, d_in)
+    dAg = new(r, d_in) if dAg is None else dAg
+    dAu = new(r, d_in) if dAu is None else dAu
+    dBg = new(d_ff, r) if dBg is None else dBg
+    dBu = new(d_ff, r) if dBu is None else dBu
+    if workspace is None:
+        workspace = _buffer(L.lora_swiglu_workspace_bytes(M, d_in, d_ff, r), X.device)
+    st = L.lora_swiglu_bwd(_ptr(dH), _ptr(X), _ptr(Wg), _ptr(Ag), _ptr(Bg), _ptr(Wu), _ptr(Au),
+                           _ptr(Bu), _ptr(saved), float(alpha), r, M, d_in, d_ff, dt,
+                           _ptr(dX) if need_dX else None, _ptr(dAg), _ptr(dBg), _ptr(dAu),
+                           _ptr(dBu), _ptr(workspace), workspace.numel(), _stream_ptr(stream))
+    _lib.check(st, "lora_swiglu_bwd")
+    return (dX if need_dX else None), dAg, dBg, dAu, dBu
+
+
+class LoRASwiGLUFunction(torch.autograd.Function):
+    """Autograd function of the gated pair: saves gate, up and the low-rank
+    activations for the backward."""
+
+    @staticmethod
+    def forward(ctx, X, Wg, Ag, Bg, Wu, Au, Bu, alpha):
+        shape = X.shape
+        X2 = X.reshape(-1, shape[-1]).contiguous()
+        ws = [t.contiguous() for t in (Wg, Ag, Bg, Wu, Au, Bu)]
+        H, saved = swiglu_forward(X2, *ws, alpha)
+        ctx.save_for_backward(X2, *ws, saved)
+        ctx.alpha = alpha
+        ctx.x_shape = shape
+        return H.reshape(*shape[:-1], Wg.shape[0])
+
+    @staticmethod
+    def backward(ctx, dH):
+        X2, Wg, Ag, Bg, Wu, Au, Bu, saved = ctx.saved_tensors
+        dH2 = dH.reshape(-1, dH.shape[-1]).contiguous()
+        dX, dAg, dBg, dAu, dBu = swiglu_backward(dH2, X2, Wg, Ag, Bg, Wu, Au, Bu, ctx.alpha, saved,
+                                                 need_dX=ctx.needs_input_grad[0])
+        if dX is not None:
+            dX = dX.reshape(ctx.x_shape)
+        return dX, None, dAg, dBg, None, dAu, dBu, None
+
+
+def lora_swiglu(X, Wg, Ag, Bg, Wu, Au, Bu, alpha: float):
+    """silu(X Wg^T + s X Ag^T Bg^T) * (X Wu^T + s X Au^T Bu^T) with gradients for
+    X and the four adapter matrices (Wg, Wu frozen)."""
+    return LoRASwiGLUFunction.apply(X, Wg, Ag, Bg, Wu, Au, Bu, alpha)

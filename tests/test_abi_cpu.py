@@ -8,7 +8,8 @@ import pytest
 
 from rank_linear_gb300 import _lib, build
 
-HEADER = os.path.join(os.path.dirname(os.path.dirname(__file__)), "include", "lora_linear.h")
+INCLUDE = os.path.join(os.path.dirname(os.path.dirname(__file__)), "include")
+HEADERS = sorted(os.path.join(INCLUDE, f) for f in os.listdir(INCLUDE) if f.endswith(".h"))
 L = None
 
 
@@ -19,7 +20,7 @@ def setup_module():
 
 
 def declared_functions():
-    src = open(HEADER).read()
+    src = "".join(open(h).read() for h in HEADERS)
     src = re.sub(r"/\*.*?\*/", "", src, flags=re.S)
     return sorted(set(re.findall(r"\b(lora_\w+)\s*\(", src)))
 
@@ -122,6 +123,32 @@ def test_bwd_rejects(kw, code):
 def test_timing_hook_set_and_clear():
     assert L.lora_set_timing_events(None, None, 0) == _lib.LORA_OK
     assert L.lora_timing_used() == 0
+
+
+def test_swiglu_sizes_and_rejects():
+    M, d_in, d_ff, r = 300, 64, 200, 16
+    # gate, up [M, d_ff] + [sH_g | sH_u] [M, 32] + two transposes [16, 304], 256-byte granules
+    rup = lambda x: (x + 255) // 256 * 256
+    assert L.lora_swiglu_saved_bytes(M, d_ff, r) == (2 * rup(M * d_ff * 2) + rup(M * 32 * 2)
+                                                     + 2 * rup(16 * 304 * 2))
+    assert L.lora_swiglu_saved_bytes(0, d_ff, r) == 0
+    assert L.lora_swiglu_saved_bytes(M, d_ff, 0) == 0
+    assert L.lora_swiglu_workspace_bytes(M, d_in, d_ff, 300) == 0
+    fake = ctypes.c_void_p(4096)
+    args = lambda dt=_lib.LORA_BF16, r=16, d_ff=200: (fake,) * 7 + (
+        32.0, r, M, d_in, d_ff, dt, fake, fake, None, 0, None)
+    assert L.lora_swiglu_fwd(*args(dt=_lib.LORA_FP32)) == _lib.LORA_ERR_UNSUPPORTED
+    assert L.lora_swiglu_fwd(*args(r=0)) == _lib.LORA_ERR_INVALID_ARG
+    assert L.lora_swiglu_fwd(*args(d_ff=204)) == _lib.LORA_ERR_UNSUPPORTED
+    bad = list(args())
+    bad[1] = None  # Wg
+    assert L.lora_swiglu_fwd(*bad) == _lib.LORA_ERR_INVALID_ARG
+    # the backward needs the saved buffer and a workspace
+    bwd = (fake,) * 8 + (None, 32.0, 16, M, d_in, 200, _lib.LORA_BF16) + (fake,) * 5 + (
+        fake, 1 << 40, None)
+    assert L.lora_swiglu_bwd(*bwd) == _lib.LORA_ERR_INVALID_ARG
+    bwd = (fake,) * 9 + (32.0, 16, M, d_in, 200, _lib.LORA_BF16) + (fake,) * 5 + (None, 0, None)
+    assert L.lora_swiglu_bwd(*bwd) == _lib.LORA_ERR_WORKSPACE
 
 
 def test_withhold_hook_arguments():

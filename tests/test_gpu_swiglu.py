@@ -1,0 +1,168 @@
+"""The SwiGLU gate/up pair of LoRA layers on the GPU vs the fp64 oracle
+(needs a GB300).
+
+Metric per output tensor T: max|T_gpu - T_ref| / max|T_ref| <= 1e-2 (bf16).
+The gradients carry one rounding more than the plain layer's: d_gate and
+d_up are bf16 intermediates (from bf16-saved gate and up), and each gradient
+is a dot product over them.  Where that product cancels (one token, rank
+one), a gradient may instead meet the forward error bound of such a product,
+max|T_gpu - T_ref| <= 2^-7 max|T_abs|, T_abs being the same formula on
+absolute values (relative error <= 4 u per term, u = 2^-9).
+Small and ragged shapes are compared element by element; the full gate/up
+workload (Llama-3-8B MLP shape) on sampled token rows of H and dX (dA and dB
+depend on every row and are compared at the smaller sizes only).
+"""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from oracle import swiglu as osw
+import rank_linear_gb300 as rl
+from rank_linear_gb300.synth import make_inputs
+
+pytestmark = pytest.mark.gpu
+
+TOL = 1e-2
+DEV = "cuda:0"
+
+
+def rel_err(got, ref) -> float:
+    if isinstance(got, torch.Tensor):
+        got = got.detach().double().cpu().numpy()
+    den = np.abs(ref).max()
+    return float(np.abs(got - ref).max() / (den if den > 0 else 1.0))
+
+
+def make_pair(M, d_in, d_ff, r, seed):
+    """Gate and up projections drawn like the LoRA layer's inputs (two seeds)."""
+    g = make_inputs(M, d_in, d_ff, r, "bf16", seed=seed)
+    u = make_inputs(M, d_in, d_ff, r, "bf16", seed=seed + 1000)
+    # larger adapters than the init-like B ~ N(0, 0.02) so the low-rank term matters
+    return dict(X=g["X"], Wg=g["W"], Ag=g["A"], Bg=(g["B"].float() * 10).bfloat16(),
+                Wu=u["W"], Au=u["A"], Bu=(u["B"].float() * 10).bfloat16(), dH=g["dY"])
+
+
+def run_gpu(t, alpha, need_dX=True):
+    g = {k: v.to(DEV) for k, v in t.items()}
+    args = [g[k] for k in ("Wg", "Ag", "Bg", "Wu", "Au", "Bu")]
+    H, saved = rl.swiglu_forward(g["X"], *args, alpha)
+    grads = rl.swiglu_backward(g["dH"], g["X"], *args, alpha, saved, need_dX=need_dX)
+    torch.cuda.synchronize()
+    rl.device_status()
+    return (H,) + tuple(grads)
+
+
+def oracle_all(t, alpha):
+    args = [t[k] for k in ("X", "Wg", "Ag", "Bg", "Wu", "Au", "Bu")]
+    _, _, H = osw.forward(*args, alpha)
+    return (H,) + tuple(osw.backward(t["dH"], *args, alpha))
+
+
+def oracle_abs(t, alpha):
+    """dX, dAg, dBg, dAu, dBu computed on absolute values (error-bound scale)."""
+    args = [t[k] for k in ("X", "Wg", "Ag", "Bg", "Wu", "Au", "Bu")]
+    gate, up, _ = osw.forward(*args, alpha)
+    dH = np.abs(oracle._f64(t["dH"]))
+    d_gate = dH * np.abs(up) * np.abs(osw.silu_grad(gate))
+    d_up = dH * np.abs(osw.silu(gate))
+    a = {k: np.abs(oracle._f64(t[k])) for k in ("X", "Wg", "Ag", "Bg", "Wu", "Au", "Bu")}
+    dXg, dAg, dBg = oracle.backward(d_gate, a["X"], a["Wg"], a["Ag"], a["Bg"], alpha)
+    dXu, dAu, dBu = oracle.backward(d_up, a["X"], a["Wu"], a["Au"], a["Bu"], alpha)
+    return dXg + dXu, dAg, dBg, dAu, dBu
+
+
+def meets_bar(got, ref, ref_abs=None):
+    if isinstance(got, torch.Tensor):
+        got = got.detach().double().cpu().numpy()
+    err = float(np.abs(got - ref).max())
+    if err <= TOL * float(np.abs(ref).max()):
+        return True
+    return ref_abs is not None and err <= 2.0 ** -7 * float(np.abs(ref_abs).max())
+
+
+NAMES = ("H", "dX", "dAg", "dBg", "dAu", "dBu")
+
+# M, d_in, d_ff, r, alpha
+SMALL = [
+    (300, 392, 264, 16, 32.0),     # M, K and the gated columns ragged
+    (520, 520, 1000, 24, 48.0),    # r not a multiple of 16 (padded to 32)
+    (129, 136, 264, 12, 24.0),     # r not a multiple of 8 (B padded / transposed)
+    (1, 64, 64, 1, 2.0),           # one token, rank one
+    (256, 512, 384, 256, 512.0),   # maximum rank: extension K = 512
+    (64, 8, 8, 8, 16.0),           # K smaller than one block
+    (2048, 1536, 2560, 128, 256.0),  # gated GEMM's last wave split two ways
+    (1024, 5120, 1024, 16, 32.0),  # dX GEMM's last wave split two ways
+]
+
+
+@pytest.mark.parametrize("shape", SMALL, ids=lambda s: "x".join(map(str, s[:4])))
+def test_small_against_oracle(shape):
+    M, d_in, d_ff, r, alpha = shape
+    t = make_pair(M, d_in, d_ff, r, seed=sum(shape[:4]))
+    got = run_gpu(t, alpha)
+    ref = oracle_all(t, alpha)
+    bound = (None,) + oracle_abs(t, alpha)
+    errs = {n: rel_err(g, e) for n, g, e in zip(NAMES, got, ref)}
+    for n, g, e, b in zip(NAMES, got, ref, bound):
+        assert meets_bar(g, e, b), f"{n}: {errs[n]:.3e} ({errs})"
+
+
+def test_full_gate_up_sampled_rows():
+    # Llama-3-8B MLP gate/up shape: M = 8192 tokens, d_in = 4096, d_ff = 14336, r = 16
+    M, d_in, d_ff, r, alpha = 8192, 4096, 14336, 16, 32.0
+    t = make_pair(M, d_in, d_ff, r, seed=0)
+    H, dX, dAg, dBg, dAu, dBu = run_gpu(t, alpha)
+    smp = osw.SampledRows(*(t[k] for k in ("X", "Wg", "Ag", "Bg", "Wu", "Au", "Bu")), t["dH"],
+                          alpha)
+    rows = np.array([0, 1, 127, 128, 4095, 4096, 5000, 8191])
+    assert rel_err(H[rows], smp.h_rows(rows)) <= TOL
+    assert rel_err(dX[rows], smp.dx_rows(rows)) <= TOL
+    for g in (dAg, dBg, dAu, dBu):
+        assert torch.isfinite(g.float()).all()
+
+
+def test_deterministic():
+    t = make_pair(520, 520, 1000, 24, seed=5)
+    a = run_gpu(t, 48.0)
+    b = run_gpu(t, 48.0)
+    for x, y in zip(a, b):
+        assert torch.equal(x, y)
+
+
+def test_skip_dx_leaves_the_rest_unchanged():
+    t = make_pair(300, 392, 264, 16, seed=6)
+    full = run_gpu(t, 32.0)
+    part = run_gpu(t, 32.0, need_dX=False)
+    assert part[1] is None
+    for i in (0, 2, 3, 4, 5):
+        assert torch.equal(full[i], part[i])
+
+
+def test_autograd():
+    M, d_in, d_ff, r, alpha = 130, 128, 256, 8, 16.0
+    t = make_pair(M, d_in, d_ff, r, seed=7)
+    g = {k: v.to(DEV) for k, v in t.items()}
+    X = g["X"].clone().reshape(2, 65, d_in).requires_grad_(True)
+    params = {k: g[k].clone().requires_grad_(k in ("Ag", "Bg", "Au", "Bu"))
+              for k in ("Wg", "Ag", "Bg", "Wu", "Au", "Bu")}
+    H = rl.lora_swiglu(X, *(params[k] for k in ("Wg", "Ag", "Bg", "Wu", "Au", "Bu")), alpha)
+    H.backward(g["dH"].reshape(2, 65, d_ff))
+    ref = oracle_all(t, alpha)
+    assert rel_err(H.reshape(M, d_ff), ref[0]) <= TOL
+    assert rel_err(X.grad.reshape(M, d_in), ref[1]) <= TOL
+    for name, e in zip(("Ag", "Bg", "Au", "Bu"), ref[2:]):
+        assert rel_err(params[name].grad, e) <= TOL, name
+    assert params["Wg"].grad is None and params["Wu"].grad is None
+
+
+def test_empty_batch():
+    t = make_pair(0, 64, 64, 8, seed=8)
+    g = {k: v.to(DEV) for k, v in t.items()}
+    args = [g[k] for k in ("Wg", "Ag", "Bg", "Wu", "Au", "Bu")]
+    H, saved = rl.swiglu_forward(g["X"], *args, 16.0)
+    dX, dAg, dBg, dAu, dBu = rl.swiglu_backward(g["dH"], g["X"], *args, 16.0, saved)
+    torch.cuda.synchronize()
+    assert H.shape == (0, 64) and dX.shape == (0, 64)
+    for z in (dAg, dBg, dAu, dBu):
+        assert torch.count_nonzero(z) == 0
