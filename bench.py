@@ -64,7 +64,23 @@ def kernel_work(kind, M, d_in, d_out, r):
     }[kind]
 
 
-BOUND = {"prep": "hbm", "down_fwd": "hbm", "down_bwd": "hbm", "grad_a": "hbm",
+def kernel_work_swiglu(kind, M, d_in, d_ff, r):
+    """Algorithmic (flops, bytes) of one launch of the gated pair's kernels."""
+    e = 2
+    return {
+        "prep": (0, e * 4 * r * d_in),
+        "down_fwd": (4 * M * d_in * r, e * (M * d_in + 2 * r * d_in + 2 * M * r)),
+        "main_fwd": (4 * M * d_ff * (d_in + r),
+                     e * (M * d_in + 2 * d_ff * d_in + 2 * M * r + 2 * d_ff * r + 3 * M * d_ff)),
+        "swiglu_grad": (0, e * 5 * M * d_ff),
+        "down_bwd_grad_b": (4 * M * d_ff * r, e * (M * d_ff + r * d_ff + 2 * M * r + d_ff * r)),
+        "main_bwd": (4 * M * d_in * (d_ff + r),
+                     e * (2 * M * d_ff + 2 * d_ff * d_in + 2 * M * r + 2 * r * d_in + M * d_in)),
+        "grad_a": (4 * M * d_in * r, e * (M * d_in + 2 * M * r + 2 * r * d_in)),
+    }[kind]
+
+
+BOUND = {"prep": "hbm", "swiglu_grad": "hbm", "down_fwd": "hbm", "down_bwd": "hbm", "grad_a": "hbm",
          "grad_b": "hbm", "down_bwd_grad_b": "hbm", "main_fwd": "tensor", "main_bwd": "tensor"}
 
 
@@ -188,8 +204,20 @@ def barrier(world: int):
 
 
 # ---------------------------------------------------------------- CPU oracle
+def layer_flops(w, tokens):
+    """Algorithmic fwd+bwd FLOPs of the workload's layer on `tokens` tokens
+    (the gated pair is two LoRA layers; its SiLU is not counted)."""
+    return step_flops(tokens, w.d_in, w.d_out, w.r) * (2 if w.layer == "swiglu" else 1)
+
+
 def oracle_run(t, alpha):
     import oracle
+    if "Wu" in t:
+        from oracle import swiglu
+        args = [t[k] for k in ("X", "W", "A", "B", "Wu", "Au", "Bu")]
+        swiglu.forward(*args, alpha)
+        swiglu.backward(t["dY"], *args, alpha)
+        return
     oracle.forward(t["X"], t["W"], t["A"], t["B"], alpha)
     oracle.backward(t["dY"], t["X"], t["W"], t["A"], t["B"], alpha)
 
@@ -197,6 +225,9 @@ def oracle_run(t, alpha):
 def oracle_inputs(w, tokens):
     from rank_linear_gb300.synth import make_inputs
     t = make_inputs(tokens, w.d_in, w.d_out, w.r, w.dtype, seed=0)
+    if w.layer == "swiglu":
+        u = make_inputs(tokens, w.d_in, w.d_out, w.r, w.dtype, seed=1000, which="W,A,B")
+        t.update(Wu=u["W"], Au=u["A"], Bu=u["B"])
     import numpy as np
     return {k: np.ascontiguousarray(v.double().numpy()) for k, v in t.items()}
 
@@ -221,9 +252,9 @@ def cpu_baseline(w, budget_s=15.0):
     t0 = time.perf_counter()
     oracle_run(t, w.alpha)
     dt = time.perf_counter() - t0
-    return {"value": step_flops(tokens, w.d_in, w.d_out, w.r) / dt / 1e12, "unit": "TFLOP/s",
+    return {"value": layer_flops(w, tokens) / dt / 1e12, "unit": "TFLOP/s",
             "cores": oracle.threads(), "kind": "oracle",
-            "sample": f"one fp64 fwd+bwd of {tokens} of the {w.M} tokens "
+            "sample": f"one fp64 fwd+bwd ({w.layer} layer) of {tokens} of the {w.M} tokens "
                       f"({w.d_in}x{w.d_out}, r={w.r}); {dt:.2f} s"}
 
 
@@ -244,7 +275,7 @@ def run_reference(args, w):
         oracle_run(t, w.alpha)
         times.append(time.perf_counter() - t0)
     sec = sum(times)
-    value = step_flops(tokens, w.d_in, w.d_out, w.r) * args.steps / sec / 1e12
+    value = layer_flops(w, tokens) * args.steps / sec / 1e12
     line = {
         "impl": "reference", "metric": METRIC, "value": value, "unit": "TFLOP/s",
         "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
@@ -277,6 +308,7 @@ def run_ours(args, w):
     torch.cuda.set_device(dev)
     L = _lib.lib()
 
+    swiglu = w.layer == "swiglu"
     # CPU baseline first (rank 0, N = 1 only), before the GPU is busy
     cpu = cpu_baseline(w) if (rank == 0 and world == 1 and not args.no_cpu_baseline) else None
 
@@ -298,6 +330,23 @@ def run_ours(args, w):
         rl.forward(X, W, A, B, alpha, Y=Y, saved=saved, workspace=ws, stream=stream)
         rl.backward(dY, X, W, A, B, alpha, saved, dX=dX, dA=dA, dB=dB, workspace=ws,
                     stream=stream)
+
+    if swiglu:  # the gate/up pair: H = silu(gate) * up, d_out = FFN width
+        tu = make_inputs(M, d_in, d_out, r, w.dtype, seed=rank + 1000, device=dev,
+                         which="W,A,B")
+        Wu, Au, Bu = tu["W"], tu["A"], tu["B"]
+        dAu = torch.empty(r, d_in, dtype=tdt, device=dev)
+        dBu = torch.empty(d_out, r, dtype=tdt, device=dev)
+        saved = torch.empty(max(1, rl.swiglu_saved_bytes(M, d_out, r)), dtype=torch.uint8,
+                            device=dev)
+        ws = torch.empty(max(1, rl.swiglu_workspace_bytes(M, d_in, d_out, r)),
+                         dtype=torch.uint8, device=dev)
+
+        def step():
+            rl.swiglu_forward(X, W, A, B, Wu, Au, Bu, alpha, H=Y, saved=saved, workspace=ws,
+                              stream=stream)
+            rl.swiglu_backward(dY, X, W, A, B, Wu, Au, Bu, alpha, saved, dX=dX, dAg=dA,
+                               dBg=dB, dAu=dAu, dBu=dBu, workspace=ws, stream=stream)
 
     for _ in range(args.warmup):
         flush.zero_()
@@ -353,7 +402,7 @@ def run_ours(args, w):
 
     step_ms = [s.elapsed_time(e) for s, e in zip(s_ev, e_ev)]
     sec = max_over_ranks(sum(step_ms) / 1e3, world, dev)
-    flops = step_flops(M, d_in, d_out, r)
+    flops = step_flops(M, d_in, d_out, r) * (2 if swiglu else 1)
     value = world * flops * args.steps / sec / 1e12
 
     per_kind = {}
@@ -366,7 +415,7 @@ def run_ours(args, w):
     dom = max(per_kind, key=lambda k: sum(per_kind[k]))
 
     peaks = load_peaks()
-    fl, by = kernel_work(dom, M, d_in, d_out, r)
+    fl, by = (kernel_work_swiglu if swiglu else kernel_work)(dom, M, d_in, d_out, r)
     avg_s = sum(per_kind[dom]) / len(per_kind[dom]) / 1e3
     if BOUND[dom] == "tensor":
         ach, peak, unit = fl / avg_s / 1e12, peaks["bf16_tflops"], "TFLOP/s"
@@ -376,7 +425,7 @@ def run_ours(args, w):
                 "unit": unit, "frac": ach / peak, "peak_source": peaks["source"] + " (burst)",
                 "traffic": load_traffic(w.name, dom)}
 
-    e2e = None if args.no_e2e else run_e2e(args, w, t, tdt, dev, stream, world)
+    e2e = None if (args.no_e2e or swiglu) else run_e2e(args, w, t, tdt, dev, stream, world)
 
     if rank == 0:
         line = {
@@ -384,7 +433,8 @@ def run_ours(args, w):
             "steps": args.steps, "warmup": args.warmup,
             "ms_per_step": 1e3 * sec / args.steps, "higher_is_better": True,
             "scaling": "weak", "vs_baseline": None, "dtype": w.dtype, "data": "synthetic",
-            "config": {"workload": w.name, "M": M, "d_in": d_in, "d_out": d_out, "r": r,
+            "config": {"workload": w.name, "layer": w.layer, "M": M, "d_in": d_in,
+                       "d_out": d_out, "r": r,
                        "alpha": alpha, "l2": "flushed before every step (256 MiB write)",
                        "parallelism": "replicas" if world > 1 else "single GPU"},
             "pct_of_bf16_peak": 100.0 * value / world / peaks["bf16_tflops"],

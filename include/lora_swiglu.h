@@ -44,8 +44,10 @@ size_t lora_swiglu_workspace_bytes(int64_t M, int64_t d_in, int64_t d_ff, int r)
 
 /*
  * Forward: H = silu(gate) * up, with gate and up written to `saved` for the
- * backward.  Two launches: one skinny pass for [s X Ag^T | s X Au^T], then
- * one tensor-core GEMM whose CTA pairs compute 128 columns of the gate
+ * backward.  `saved` may be NULL (inference): then nothing is kept and the
+ * forward skips writing gate and up (a third less output traffic).  Two
+ * launches: one skinny pass for [s X Ag^T | s X Au^T], then one tensor-core
+ * GEMM whose CTA pairs compute 128 columns of the gate
  * projection (even CTA) and of the up projection (odd CTA) for the same
  * 256 rows, and apply silu(gate) * up in the epilogue.
  *   workspace   device scratch of lora_swiglu_workspace_bytes bytes.

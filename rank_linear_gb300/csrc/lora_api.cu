@@ -568,7 +568,8 @@ struct SwPlan {
   int r_pad = 0;
   int64_t Mp = 0, half = 0;  // half: d_ff rounded up to 64 (a column block of D)
   size_t gate_off = 0, up_off = 0, sh_off = 0, sht_off[2] = {0, 0}, saved = 0;
-  size_t bpad_off[2] = {0, 0}, fsplit_off = 0, fcnt_off = 0, fwd_ws = 0, fwd_ws_min = 0;
+  size_t bpad_off[2] = {0, 0}, shws_off = 0, fsplit_off = 0, fcnt_off = 0, fwd_ws = 0,
+         fwd_ws_min = 0;
   size_t d_off = 0, sg_off = 0, sgt_off[2] = {0, 0}, agu_off = 0, bt_off[2] = {0, 0};
   size_t bsplit_off = 0, bcnt_off = 0, bwd_ws = 0, bwd_ws_min = 0;
   MainSplit fsplit, bsplit;
@@ -594,13 +595,16 @@ SwPlan make_sw_plan(int64_t M, int64_t d_in, int64_t d_ff, int r, int pairs_f, i
     off += tr;
   }
   P.saved = M > 0 ? off : 0;
-  // forward workspace: [Bg, Bu padded (r % 8 != 0)] [split partials] [counters]
+  // forward workspace: [Bg, Bu padded (r % 8 != 0)] [sH_g | sH_u when nothing
+  // is saved] [split partials] [counters]
   off = 0;
   for (int p = 0; p < 2; ++p) {
     P.bpad_off[p] = off;
     if (r % 8) off += rup(size_t(d_ff) * P.r_pad * 2, 256);
   }
-  P.fwd_ws_min = off;
+  P.shws_off = off;
+  off += rup(size_t(M) * 2 * P.r_pad * 2, 256);
+  P.fwd_ws_min = M > 0 ? off : 0;
   if (pairs_f > 0 && M > 0) P.fsplit = main_gemm_split(int(M), int(2 * rup(d_ff, 128)), pairs_f);
   P.fsplit_off = off;
   off += rup(P.fsplit.partial_bytes, 256);
@@ -659,7 +663,10 @@ lora_status_t sw_fwd_bf16(const void *X, const void *Wg, const void *Ag, const v
     }
     b_inner = P.r_pad;
   }
-  uint8_t *sh = static_cast<uint8_t *>(saved) + P.sh_off;
+  // without a saved buffer (inference) the low-rank activations live in the
+  // workspace and neither their transposes nor gate and up are written
+  uint8_t *sh = saved != nullptr ? static_cast<uint8_t *>(saved) + P.sh_off
+                                 : static_cast<uint8_t *>(at(ws, P.shws_off));
   // [s X Ag^T | s X Au^T] (and transposes): one launch, both read X
   SkinnyArgs f[2];
   for (int p = 0; p < 2; ++p) {
@@ -673,7 +680,7 @@ lora_status_t sw_fwd_bf16(const void *X, const void *Wg, const void *Ag, const v
     f[p].out0 = sh + size_t(p) * P.r_pad * 2;
     f[p].ld0 = 2 * P.r_pad;
     f[p].n0 = P.r_pad;
-    f[p].out1 = at(saved, P.sht_off[p]);
+    f[p].out1 = saved != nullptr ? at(saved, P.sht_off[p]) : nullptr;
     f[p].ld1 = P.Mp;
     f[p].n1 = P.r_pad;
     f[p].dev_status = di.status;
@@ -698,8 +705,8 @@ lora_status_t sw_fwd_bf16(const void *X, const void *Wg, const void *Ag, const v
   g.k_ext = 2 * P.r_pad;
   g.ext_shift = P.r_pad;
   g.out = H;
-  g.aux0 = at(saved, P.gate_off);
-  g.aux1 = at(saved, P.up_off);
+  g.aux0 = saved != nullptr ? at(saved, P.gate_off) : nullptr;
+  g.aux1 = saved != nullptr ? at(saved, P.up_off) : nullptr;
   g.ldo = d_ff;
   g.b_mn = false;
   g.dev_status = di.status;
@@ -1097,7 +1104,7 @@ lora_status_t lora_swiglu_fwd(const void *X, const void *Wg, const void *Ag, con
   LORA_TRY(check_ptr(Au, "Au"));
   LORA_TRY(check_ptr(Bu, "Bu"));
   LORA_TRY(check_ptr(H, "H", empty));
-  LORA_TRY(check_ptr(saved, "saved", empty));
+  LORA_TRY(check_ptr(saved, "saved", true));
   const SwPlan P = make_sw_plan(M, d_in, d_ff, r, 0, 0);
   LORA_TRY(check_ws(workspace, workspace_bytes, P.fwd_ws_min));
   if (empty) return LORA_OK;

@@ -162,8 +162,9 @@ def swiglu_workspace_bytes(M: int, d_in: int, d_ff: int, r: int) -> int:
 
 
 def swiglu_forward(X, Wg, Ag, Bg, Wu, Au, Bu, alpha: float, *, H=None, saved=None,
-                   workspace=None, stream=None):
-    """H = silu(gate) * up.  Returns (H, saved); saved holds gate and up."""
+                   workspace=None, stream=None, keep=True):
+    """H = silu(gate) * up.  Returns (H, saved); saved holds gate and up for the
+    backward, or is None with keep=False (inference: nothing is kept)."""
     _check_dev(X, Wg, Ag, Bg, Wu, Au, Bu)
     M, d_in = X.shape
     d_ff, r = Bg.shape
@@ -171,7 +172,7 @@ def swiglu_forward(X, Wg, Ag, Bg, Wu, Au, Bu, alpha: float, *, H=None, saved=Non
     L = _lib.lib()
     if H is None:
         H = torch.empty(M, d_ff, dtype=X.dtype, device=X.device)
-    if saved is None:
+    if saved is None and keep:
         saved = _buffer(L.lora_swiglu_saved_bytes(M, d_ff, r), X.device)
     if workspace is None:
         workspace = _buffer(L.lora_swiglu_workspace_bytes(M, d_in, d_ff, r), X.device)

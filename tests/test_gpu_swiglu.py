@@ -122,6 +122,18 @@ def test_full_gate_up_sampled_rows():
         assert torch.isfinite(g.float()).all()
 
 
+def test_inference_forward_keeps_nothing_and_agrees():
+    t = make_pair(300, 392, 264, 16, seed=9)
+    g = {k: v.to(DEV) for k, v in t.items()}
+    args = [g[k] for k in ("Wg", "Ag", "Bg", "Wu", "Au", "Bu")]
+    H1, saved = rl.swiglu_forward(g["X"], *args, 32.0)
+    H2, none = rl.swiglu_forward(g["X"], *args, 32.0, keep=False)
+    torch.cuda.synchronize()
+    rl.device_status()
+    assert none is None and saved is not None
+    assert torch.equal(H1, H2)
+
+
 def test_deterministic():
     t = make_pair(520, 520, 1000, 24, seed=5)
     a = run_gpu(t, 48.0)
