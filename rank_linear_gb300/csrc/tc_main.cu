@@ -175,7 +175,7 @@ __device__ __forceinline__ void store_gated(const float (&g)[32], const float (&
   store_chunk(pk, stage, lane, out, ldo, row0, col0, M, N);
 }
 
-template <bool B_MN, int BN, bool SPLIT, bool GATED>
+template <bool B_MN, int BN, bool SPLIT, bool GATED, bool DUAL_B>
 __global__ void __launch_bounds__(NUM_THREADS, 1)
     k_main_gemm(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                 const __grid_constant__ CUtensorMap tmA2, const __grid_constant__ CUtensorMap tmB2,
@@ -290,18 +290,18 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
           // B: the odd CTA of the gated pair reads the up projection (its
           // extension shifted so it meets the second half of [sH_g | sH_u]);
           // otherwise the main segment switches to tmB3 at kb_switch
-          const CUtensorMap *tb;
+          const CUtensorMap *tb = ext ? &tmB2 : &tmB;
           int kB = k0;
-          if (ext) {
-            tb = (GATED && q) ? &tmB4 : &tmB2;
-            if (GATED && q) kB = k0 - ext_shift;
-          } else if (GATED) {
-            tb = q ? &tmB3 : &tmB;
-          } else if (kb >= kb_switch) {
-            tb = &tmB3;
-            kB = (kb - kb_switch) * BK;
-          } else {
-            tb = &tmB;
+          if constexpr (GATED) {
+            if (q) {
+              tb = ext ? &tmB4 : &tmB3;
+              if (ext) kB = k0 - ext_shift;
+            }
+          } else if constexpr (DUAL_B) {
+            if (!ext && kb >= kb_switch) {
+              tb = &tmB3;
+              kB = (kb - kb_switch) * BK;
+            }
           }
           tma_load_2d_pair(sA + stage * A_BYTES, ta, full, k0, m0);
           if (B_MN) {  // BN/128 boxes of [64 K x 64 N]
@@ -566,9 +566,9 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
   }
 }
 
-template <bool B_MN, int BN, bool SPLIT, bool GATED = false>
+template <bool B_MN, int BN, bool SPLIT, bool GATED = false, bool DUAL_B = false>
 constexpr auto kernel_of() {
-  return &k_main_gemm<B_MN, BN, SPLIT, GATED>;
+  return &k_main_gemm<B_MN, BN, SPLIT, GATED, DUAL_B>;
 }
 
 int g_max_clusters[64][2] = {};
@@ -604,13 +604,13 @@ int max_clusters(int num_sms) {
   return n;
 }
 
-template <bool B_MN, int BN, bool SPLIT, bool GATED>
+template <bool B_MN, int BN, bool SPLIT, bool GATED, bool DUAL_B>
 cudaError_t launch_variant(const MainGemmArgs &a, int num_sms, cudaStream_t s) {
   constexpr int TN = GATED ? BN / 2 : BN;
   const int m_tiles = (a.M + BM - 1) / BM, n_tiles = (a.N + TN - 1) / TN;
   const int tiles = ((m_tiles + 1) / 2) * n_tiles;  // pair tiles
   if (tiles == 0) return cudaSuccess;
-  auto kern = kernel_of<B_MN, BN, SPLIT, GATED>();
+  auto kern = kernel_of<B_MN, BN, SPLIT, GATED, DUAL_B>();
   constexpr size_t smem = smem_bytes<BN>();
   cudaError_t e =
       cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));
@@ -676,15 +676,20 @@ int main_gemm_pick_bn(int, int, int) { return 256; }
 cudaError_t launch_main_gemm(const MainGemmArgs &a, int num_sms, cudaStream_t s) {
   const bool split = a.split_k > 1 && a.split_rem > 0;
   if (a.gated) {
-    if (a.b_mn) return cudaErrorInvalidValue;
-    return split ? launch_variant<false, 256, true, true>(a, num_sms, s)
-                 : launch_variant<false, 256, false, true>(a, num_sms, s);
+    if (a.b_mn || a.kb_switch >= 0) return cudaErrorInvalidValue;
+    return split ? launch_variant<false, 256, true, true, false>(a, num_sms, s)
+                 : launch_variant<false, 256, false, true, false>(a, num_sms, s);
+  }
+  if (a.kb_switch >= 0) {  // the gated pair's dX GEMM: [Wg ; Wu], MN-major
+    if (!a.b_mn) return cudaErrorInvalidValue;
+    return split ? launch_variant<true, 256, true, false, true>(a, num_sms, s)
+                 : launch_variant<true, 256, false, false, true>(a, num_sms, s);
   }
   if (a.b_mn)
-    return split ? launch_variant<true, 256, true, false>(a, num_sms, s)
-                 : launch_variant<true, 256, false, false>(a, num_sms, s);
-  return split ? launch_variant<false, 256, true, false>(a, num_sms, s)
-               : launch_variant<false, 256, false, false>(a, num_sms, s);
+    return split ? launch_variant<true, 256, true, false, false>(a, num_sms, s)
+                 : launch_variant<true, 256, false, false, false>(a, num_sms, s);
+  return split ? launch_variant<false, 256, true, false, false>(a, num_sms, s)
+               : launch_variant<false, 256, false, false, false>(a, num_sms, s);
 }
 
 }  // namespace lora
