@@ -58,6 +58,8 @@ def kernel_work(kind, M, d_in, d_out, r):
                      e * (M * d_out + d_out * d_in + M * r + r * d_in + M * d_in)),
         "grad_a": (2 * M * d_in * r, e * (M * d_in + M * r + r * d_in)),
         "grad_b": (2 * M * d_out * r, e * (M * d_out + M * r + d_out * r)),
+        # e4m3 quantisation of X's rows (bf16 in, bytes and scales out)
+        "quant": (0, e * M * d_in + M * d_in + 4 * M),
         # s dY B and dY^T sH in one launch; dY counted once
         "down_bwd_grad_b": (4 * M * d_out * r,
                             e * (M * d_out + r * d_out + 2 * M * r + d_out * r)),
@@ -80,7 +82,7 @@ def kernel_work_swiglu(kind, M, d_in, d_ff, r):
     }[kind]
 
 
-BOUND = {"prep": "hbm", "swiglu_grad": "hbm", "down_fwd": "hbm", "down_bwd": "hbm", "grad_a": "hbm",
+BOUND = {"prep": "hbm", "swiglu_grad": "hbm", "quant": "hbm", "down_fwd": "hbm", "down_bwd": "hbm", "grad_a": "hbm",
          "grad_b": "hbm", "down_bwd_grad_b": "hbm", "main_fwd": "tensor", "main_bwd": "tensor"}
 
 
@@ -210,8 +212,13 @@ def layer_flops(w, tokens):
     return step_flops(tokens, w.d_in, w.d_out, w.r) * (2 if w.layer == "swiglu" else 1)
 
 
-def oracle_run(t, alpha):
+def oracle_run(t, alpha, layer="linear"):
     import oracle
+    if layer == "fp8":
+        from oracle import fp8
+        fp8.forward(t["X"], t["W"], t["A"], t["B"], alpha)
+        fp8.backward(t["dY"], t["X"], t["W"], t["A"], t["B"], alpha)
+        return
     if "Wu" in t:
         from oracle import swiglu
         args = [t[k] for k in ("X", "W", "A", "B", "Wu", "Au", "Bu")]
@@ -237,7 +244,7 @@ def oracle_sample_tokens(w, budget_s):
     budget_s seconds, from one calibration run on 8 tokens."""
     t = oracle_inputs(w, 8)
     t0 = time.perf_counter()
-    oracle_run(t, w.alpha)
+    oracle_run(t, w.alpha, w.layer)
     per_token = (time.perf_counter() - t0) / 8
     tokens = 8
     while tokens * 2 <= w.M and tokens * 2 * per_token <= budget_s:
@@ -250,7 +257,7 @@ def cpu_baseline(w, budget_s=15.0):
     tokens = oracle_sample_tokens(w, budget_s)
     t = oracle_inputs(w, tokens)
     t0 = time.perf_counter()
-    oracle_run(t, w.alpha)
+    oracle_run(t, w.alpha, w.layer)
     dt = time.perf_counter() - t0
     return {"value": layer_flops(w, tokens) / dt / 1e12, "unit": "TFLOP/s",
             "cores": oracle.threads(), "kind": "oracle",
@@ -268,11 +275,11 @@ def run_reference(args, w):
     tokens = oracle_sample_tokens(w, per_step)
     t = oracle_inputs(w, tokens)
     for _ in range(args.warmup):
-        oracle_run(t, w.alpha)
+        oracle_run(t, w.alpha, w.layer)
     times = []
     for _ in range(args.steps):
         t0 = time.perf_counter()
-        oracle_run(t, w.alpha)
+        oracle_run(t, w.alpha, w.layer)
         times.append(time.perf_counter() - t0)
     sec = sum(times)
     value = layer_flops(w, tokens) * args.steps / sec / 1e12
@@ -309,6 +316,7 @@ def run_ours(args, w):
     L = _lib.lib()
 
     swiglu = w.layer == "swiglu"
+    fp8 = w.layer == "fp8"
     # CPU baseline first (rank 0, N = 1 only), before the GPU is busy
     cpu = cpu_baseline(w) if (rank == 0 and world == 1 and not args.no_cpu_baseline) else None
 
@@ -330,6 +338,16 @@ def run_ours(args, w):
         rl.forward(X, W, A, B, alpha, Y=Y, saved=saved, workspace=ws, stream=stream)
         rl.backward(dY, X, W, A, B, alpha, saved, dX=dX, dA=dA, dB=dB, workspace=ws,
                     stream=stream)
+
+    if fp8:  # the frozen W quantised once (outside the timed steps), X and dY per call
+        qw = rl.quantize_w_fp8(W)
+        ws = torch.empty(max(1, rl.fp8_workspace_bytes(M, d_in, d_out, r)), dtype=torch.uint8,
+                         device=dev)
+
+        def step():
+            rl.fp8_forward(X, qw, A, B, alpha, Y=Y, saved=saved, workspace=ws, stream=stream)
+            rl.fp8_backward(dY, X, qw, A, B, alpha, saved, dX=dX, dA=dA, dB=dB, workspace=ws,
+                            stream=stream)
 
     if swiglu:  # the gate/up pair: H = silu(gate) * up, d_out = FFN width
         tu = make_inputs(M, d_in, d_out, r, w.dtype, seed=rank + 1000, device=dev,
@@ -417,22 +435,27 @@ def run_ours(args, w):
     peaks = load_peaks()
     fl, by = (kernel_work_swiglu if swiglu else kernel_work)(dom, M, d_in, d_out, r)
     avg_s = sum(per_kind[dom]) / len(per_kind[dom]) / 1e3
-    if BOUND[dom] == "tensor":
+    peak_note = " (burst)"
+    if BOUND[dom] == "tensor" and fp8:  # e4m3 products: 2 x the bf16 rate (nominal ratio)
+        ach, peak, unit = fl / avg_s / 1e12, 2 * peaks["bf16_tflops"], "TFLOP/s"
+        peak_note = " bf16 burst x 2 (nominal e4m3 / bf16 ratio)"
+    elif BOUND[dom] == "tensor":
         ach, peak, unit = fl / avg_s / 1e12, peaks["bf16_tflops"], "TFLOP/s"
     else:
         ach, peak, unit = by / avg_s / 1e9, peaks["hbm_gbs"], "GB/s"
     roofline = {"kernel": dom, "bound": BOUND[dom], "achieved": ach, "peak": peak,
-                "unit": unit, "frac": ach / peak, "peak_source": peaks["source"] + " (burst)",
+                "unit": unit, "frac": ach / peak, "peak_source": peaks["source"] + peak_note,
                 "traffic": load_traffic(w.name, dom)}
 
-    e2e = None if (args.no_e2e or swiglu) else run_e2e(args, w, t, tdt, dev, stream, world)
+    e2e = None if (args.no_e2e or swiglu or fp8) else run_e2e(args, w, t, tdt, dev, stream, world)
 
     if rank == 0:
         line = {
             "metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": world,
             "steps": args.steps, "warmup": args.warmup,
             "ms_per_step": 1e3 * sec / args.steps, "higher_is_better": True,
-            "scaling": "weak", "vs_baseline": None, "dtype": w.dtype, "data": "synthetic",
+            "scaling": "weak", "vs_baseline": None,
+            "dtype": "e4m3 W product, bf16 elsewhere" if fp8 else w.dtype, "data": "synthetic",
             "config": {"workload": w.name, "layer": w.layer, "M": M, "d_in": d_in,
                        "d_out": d_out, "r": r,
                        "alpha": alpha, "l2": "flushed before every step (256 MiB write)",

@@ -192,7 +192,8 @@ typedef enum {
     LORA_K_GRAD_A = 5,    /* dA = (s dY B)^T X   (skinny split-K)            */
     LORA_K_GRAD_B = 6,    /* dB = dY^T (s X A^T) (skinny split-K)            */
     LORA_K_DOWN_BWD_GRAD_B = 7, /* s dY B and dB in one launch (both read dY) */
-    LORA_K_SWIGLU_GRAD = 8      /* SwiGLU pair: elementwise d_gate, d_up      */
+    LORA_K_SWIGLU_GRAD = 8,     /* SwiGLU pair: elementwise d_gate, d_up      */
+    LORA_K_QUANT = 9            /* fp8 variant: e4m3 quantisation of X or dY  */
 } lora_kernel_kind_t;
 
 /*

@@ -45,6 +45,11 @@ struct MainGemmArgs {
   // Second B segment of the main K range (not gated): K blocks >= kb_switch
   // read B from tmB3 at K coordinate (kb - kb_switch) * 64.  -1: none.
   int kb_switch = -1;
+  // fp8 main segment: A and B are e4m3 K-major maps (box 128 bytes x rows),
+  // kb_main counts 128-wide K blocks, the extension stays bf16; the epilogue
+  // multiplies row m of the result by row_scale[m] (times w_scale[0] if given).
+  bool fp8 = false;
+  const float *row_scale = nullptr, *w_scale = nullptr;
 };
 constexpr int kMainBM = 128, kMainBK = 64;
 int main_gemm_pick_bn(int M, int N, int num_sms);
@@ -89,6 +94,9 @@ struct SkinnyArgs {
   // Test hook of the bounded waits: the first CTA's producer leaves its
   // first stage unfilled, so that CTA's MMA wait runs out (problem 0 only).
   int withhold_first_stage = 0;
+  // Optional per-row divisor of out0 (powers of two, so exact): out0 row m
+  // is divided by row_div[m]; out1 is not.
+  const float *row_div = nullptr;
 };
 // Runs one or two independent problems in one launch.
 cudaError_t launch_skinny(const SkinnyArgs *probs, int nprob, int num_sms, cudaStream_t s);
@@ -125,5 +133,18 @@ cudaError_t launch_swiglu_grad_bf16(const void *dH, const void *gate, const void
 // dst [2 r_pad][d_in] = [Ag (r rows) ; 0 ; Au (r rows) ; 0].
 cudaError_t launch_stack_rows_bf16(const void *Ag, const void *Au, int r, int r_pad, int64_t d_in,
                                    void *dst, cudaStream_t s);
+// e4m3 with power-of-two scales: one scale per row of x [rows][cols]
+// (cols % 8 == 0, cols <= 65536) -> q [rows][cols] bytes and scale [rows]
+// floats, the row's scale times mul[0] when mul is given.
+cudaError_t launch_quant_rows_e4m3(const void *x, int64_t rows, int64_t cols, void *q,
+                                   float *scale, const float *mul, cudaStream_t s);
+// One scale for all of w [rows][cols]: q [rows][cols], qT [cols][rows],
+// scale[0]; amax_bits is one word of device scratch.
+cudaError_t launch_quant_tensor_e4m3(const void *w, int rows, int cols, unsigned *amax_bits,
+                                     void *q, void *qT, float *scale, int num_sms,
+                                     cudaStream_t s);
+// out [cols][r_pad] = in^T / scale[0] for in [r][cols] (no scale: 1), zero-padded.
+cudaError_t launch_transpose_scale_bf16(const void *in, int r, int64_t cols, int r_pad,
+                                        const float *scale, void *out, cudaStream_t s);
 
 }  // namespace lora

@@ -13,6 +13,7 @@
 
 #include "internal.h"
 #include "lora_linear.h"
+#include "lora_fp8.h"
 #include "lora_swiglu.h"
 #include "ptx.cuh"
 
@@ -847,6 +848,266 @@ lora_status_t sw_bwd_bf16(const void *dH, const void *X, const void *Wg, const v
              [&] { return launch_skinny(a, 2, di.sms, st); });
 }
 
+// ---------------------------------------------------------------- fp8 frozen W
+// 2-D map over a row-major [outer][inner] tensor of bytes (e4m3 codes), box
+// 128 bytes x box_outer rows, 128-byte swizzle.
+lora_status_t tmap_u8(CUtensorMap *tm, const void *ptr, uint64_t inner, uint64_t outer,
+                      uint64_t pitch_bytes, uint32_t box_outer, const char *what) {
+  auto fn = encode_fn();
+  if (!fn) return fail(LORA_ERR_CUDA, "cuTensorMapEncodeTiled is not available from the driver");
+  cuuint64_t dims[2] = {inner, outer};
+  cuuint64_t strides[1] = {pitch_bytes};
+  cuuint32_t box[2] = {128, box_outer};
+  cuuint32_t es[2] = {1, 1};
+  CUresult r = fn(tm, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<void *>(ptr), dims, strides,
+                  box, es, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                  CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  if (r != CUDA_SUCCESS)
+    return fail(LORA_ERR_CUDA, "tensor map for %s (%llu x %llu bytes) failed: CUresult %d", what,
+                (unsigned long long)outer, (unsigned long long)inner, static_cast<int>(r));
+  return LORA_OK;
+}
+
+// Workspace layout of the fp8 forward and backward.
+struct FpPlan {
+  int r_pad = 0;
+  int64_t Mp = 0;
+  size_t xq_off = 0, xs_off = 0, bs_off = 0, fsplit_off = 0, fcnt_off = 0, fwd_ws = 0,
+         fwd_ws_min = 0;
+  size_t dq_off = 0, ds_off = 0, sg_off = 0, sgt_off = 0, at_off = 0, bt_off = 0,
+         bsplit_off = 0, bcnt_off = 0, bwd_ws = 0, bwd_ws_min = 0;
+  MainSplit fsplit, bsplit;
+};
+
+FpPlan make_fp_plan(int64_t M, int64_t d_in, int64_t d_out, int r, int pairs_f, int pairs_b) {
+  FpPlan P;
+  P.r_pad = static_cast<int>(rup(r, 16));
+  P.Mp = rup(M, 8);
+  // forward: [X codes] [X scales] [B / w_scale, padded] [split partials] [counters]
+  size_t off = 0;
+  P.xq_off = off;
+  off += rup(size_t(M) * d_in, 256);
+  P.xs_off = off;
+  off += rup(size_t(M) * 4, 256);
+  P.bs_off = off;
+  off += rup(size_t(d_out) * P.r_pad * 2, 256);
+  P.fwd_ws_min = M > 0 ? off : 0;
+  if (pairs_f > 0 && M > 0) P.fsplit = main_gemm_split(int(M), int(d_out), pairs_f);
+  P.fsplit_off = off;
+  off += rup(P.fsplit.partial_bytes, 256);
+  P.fcnt_off = off;
+  off += rup(P.fsplit.counter_bytes, 256);
+  P.fwd_ws = M > 0 ? (P.fsplit.k > 1 ? off : P.fwd_ws_min) : 0;
+  // backward: [dY codes] [dY scales] [sG / dy_scale] [sG^T] [(A / w_scale)^T]
+  // [B^T (r % 8 != 0)] [split partials] [counters]
+  off = 0;
+  P.dq_off = off;
+  off += rup(size_t(M) * d_out, 256);
+  P.ds_off = off;
+  off += rup(size_t(M) * 4, 256);
+  P.sg_off = off;
+  off += rup(size_t(M) * P.r_pad * 2, 256);
+  P.sgt_off = off;
+  off += rup(size_t(P.r_pad) * P.Mp * 2, 256);
+  P.at_off = off;
+  off += rup(size_t(d_in) * P.r_pad * 2, 256);
+  P.bt_off = off;
+  if (r % 8) off += rup(size_t(P.r_pad) * d_out * 2, 256);
+  P.bwd_ws_min = M > 0 ? off : 0;
+  if (pairs_b > 0 && M > 0) P.bsplit = main_gemm_split(int(M), int(d_in), pairs_b);
+  P.bsplit_off = off;
+  off += rup(P.bsplit.partial_bytes, 256);
+  P.bcnt_off = off;
+  off += rup(P.bsplit.counter_bytes, 256);
+  P.bwd_ws = M > 0 ? (P.bsplit.k > 1 ? off : P.bwd_ws_min) : 0;
+  return P;
+}
+
+lora_status_t fp8_fwd(const void *X, const void *Wq, const float *w_scale, const void *A,
+                      const void *B, float alpha, int r, int64_t M, int64_t d_in, int64_t d_out,
+                      void *Y, void *saved, void *ws, size_t ws_bytes, cudaStream_t st) {
+  DevInfo di;
+  LORA_TRY(device_info(di));
+  FpPlan P = make_fp_plan(M, d_in, d_out, r, main_gemm_pairs(false, di.sms), 0);
+  const bool split = P.fsplit.k > 1 && ws != nullptr && ws_bytes >= P.fwd_ws;
+  if (!split) P = make_fp_plan(M, d_in, d_out, r, 0, 0);
+  unsigned *counters = split ? reinterpret_cast<unsigned *>(at(ws, P.fcnt_off)) : nullptr;
+  const Plan L = make_plan(M, d_in, d_out, r, LORA_BF16);  // the saved buffer's layout
+  const float s = alpha / static_cast<float>(r);
+  void *xq = at(ws, P.xq_off);
+  float *xs = reinterpret_cast<float *>(at(ws, P.xs_off));  // x_scale * w_scale per row
+  LORA_TRY(run(LORA_K_QUANT, st, "quantise X",
+               [&] { return launch_quant_rows_e4m3(X, M, d_in, xq, xs, w_scale, st); }));
+  const void *Bsrc = B;
+  int64_t b_inner = r;
+  if (r % 8 != 0) {  // B's row pitch is not a multiple of 16 bytes: pad it
+    void *bs = at(ws, P.bs_off);
+    LORA_TRY(run(LORA_K_PREP, st, "pad B", [&] {
+      return launch_pad_cols_bf16(B, static_cast<int>(d_out), r, P.r_pad, bs, st);
+    }));
+    Bsrc = bs;
+    b_inner = P.r_pad;
+  }
+  // sH / (x_scale w_scale) (row-major, the GEMM's extension: every tile's
+  // accumulator is multiplied by x_scale w_scale in the epilogue) and sH^T
+  // (unscaled, for the backward)
+  SkinnyArgs f1;
+  LORA_TRY(tmap(&f1.tmA, X, d_in, M, d_in * 2, 64, 128, "X"));
+  LORA_TRY(tmap(&f1.tmB, A, d_in, r, d_in * 2, 64, P.r_pad, "A"));
+  f1.a_mn = false;
+  f1.rows = static_cast<int>(M);
+  f1.RP = P.r_pad;
+  f1.K = static_cast<int>(d_in);
+  f1.scale = s;
+  f1.out0 = saved;
+  f1.ld0 = P.r_pad;
+  f1.n0 = P.r_pad;
+  f1.row_div = xs;
+  f1.out1 = at(saved, L.sHt_off);
+  f1.ld1 = P.Mp;
+  f1.n1 = P.r_pad;
+  f1.dev_status = di.status;
+  f1.zero_ptr = counters;
+  f1.zero_words = split ? 2 * P.fsplit.rem : 0;
+  LORA_TRY(run(LORA_K_DOWN_FWD, st, "s X A^T pass", [&] { return launch_skinny(&f1, 1, di.sms, st); }));
+  MainGemmArgs g;
+  g.fp8 = true;
+  g.bn = 256;
+  LORA_TRY(tmap_u8(&g.tmA, xq, d_in, M, d_in, 128, "X (e4m3)"));
+  LORA_TRY(tmap_u8(&g.tmB, Wq, d_in, d_out, d_in, 128, "W (e4m3)"));
+  LORA_TRY(tmap(&g.tmA2, saved, P.r_pad, M, P.r_pad * 2, 64, 128, "sH / row scale"));
+  LORA_TRY(tmap(&g.tmB2, Bsrc, b_inner, d_out, b_inner * 2, 64, 128, "B"));
+  g.M = static_cast<int>(M);
+  g.N = static_cast<int>(d_out);
+  g.kb_main = static_cast<int>((d_in + 127) / 128);
+  g.k_ext = P.r_pad;
+  g.out = Y;
+  g.ldo = d_out;
+  g.row_scale = xs;
+  g.dev_status = di.status;
+  if (split) {
+    g.split_k = P.fsplit.k;
+    g.split_rem = P.fsplit.rem;
+    g.partials = reinterpret_cast<float *>(at(ws, P.fsplit_off));
+    g.counters = counters;
+  }
+  return run(LORA_K_MAIN_FWD, st, "fp8 forward GEMM", [&] { return launch_main_gemm(g, di.sms, st); });
+}
+
+lora_status_t fp8_bwd(const void *dY, const void *X, const void *WqT, const float *w_scale,
+                      const void *A, const void *B, const void *saved, float alpha, int r,
+                      int64_t M, int64_t d_in, int64_t d_out, void *dX, void *dA, void *dB,
+                      void *ws, size_t ws_bytes, cudaStream_t st) {
+  DevInfo di;
+  LORA_TRY(device_info(di));
+  FpPlan P = make_fp_plan(M, d_in, d_out, r, 0, main_gemm_pairs(false, di.sms));
+  const bool split = dX != nullptr && P.bsplit.k > 1 && ws != nullptr && ws_bytes >= P.bwd_ws;
+  if (!split) P = make_fp_plan(M, d_in, d_out, r, 0, 0);
+  unsigned *counters = split ? reinterpret_cast<unsigned *>(at(ws, P.bcnt_off)) : nullptr;
+  const Plan L = make_plan(M, d_in, d_out, r, LORA_BF16);
+  const float s = alpha / static_cast<float>(r);
+  const void *sHt = static_cast<const uint8_t *>(saved) + L.sHt_off;
+  void *dq = at(ws, P.dq_off);
+  float *ds = reinterpret_cast<float *>(at(ws, P.ds_off));  // dy_scale * w_scale per row
+  void *sG = at(ws, P.sg_off);
+  void *sGt = at(ws, P.sgt_off);
+  LORA_TRY(run(LORA_K_QUANT, st, "quantise dY",
+               [&] { return launch_quant_rows_e4m3(dY, M, d_out, dq, ds, w_scale, st); }));
+
+  // sG / (dy_scale w_scale) (row-major, the dX GEMM's extension) and sG^T, and
+  // dB = dY^T sH: one launch, both read dY
+  SkinnyArgs g[2];
+  SkinnyArgs &b1 = g[0];
+  LORA_TRY(tmap(&b1.tmA, dY, d_out, M, d_out * 2, 64, 128, "dY"));
+  if (r % 8 == 0) {
+    LORA_TRY(tmap(&b1.tmB, B, r, d_out, int64_t(r) * 2, 64, 64, "B (MN-major)"));
+    b1.b_mn = true;
+  } else {
+    void *Bt = at(ws, P.bt_off);
+    LORA_TRY(run(LORA_K_PREP, st, "transpose B", [&] {
+      return launch_transpose_pad_bf16(B, static_cast<int>(d_out), r, P.r_pad, Bt, st);
+    }));
+    LORA_TRY(tmap(&b1.tmB, Bt, d_out, P.r_pad, d_out * 2, 64, P.r_pad, "B^T"));
+    b1.b_mn = false;
+  }
+  b1.a_mn = false;
+  b1.rows = static_cast<int>(M);
+  b1.RP = P.r_pad;
+  b1.K = static_cast<int>(d_out);
+  b1.scale = s;
+  b1.out0 = sG;
+  b1.ld0 = P.r_pad;
+  b1.n0 = P.r_pad;
+  b1.row_div = ds;
+  b1.out1 = sGt;
+  b1.ld1 = P.Mp;
+  b1.n1 = P.r_pad;
+  b1.dev_status = di.status;
+  b1.zero_ptr = counters;
+  b1.zero_words = split ? 2 * P.bsplit.rem : 0;
+  SkinnyArgs &b4 = g[1];
+  LORA_TRY(tmap(&b4.tmA, dY, d_out, M, d_out * 2, 64, 64, "dY^T"));
+  LORA_TRY(tmap(&b4.tmB, sHt, M, P.r_pad, P.Mp * 2, 64, P.r_pad, "sH^T"));
+  b4.a_mn = true;
+  b4.rows = static_cast<int>(d_out);
+  b4.RP = P.r_pad;
+  b4.K = static_cast<int>(M);
+  b4.scale = 1.f;
+  b4.out0 = dB;
+  b4.ld0 = r;
+  b4.n0 = r;
+  b4.dev_status = di.status;
+  LORA_TRY(run(LORA_K_DOWN_BWD_GRAD_B, st, "s dY B and dB pass",
+               [&] { return launch_skinny(g, 2, di.sms, st); }));
+
+  // dX = Q(dY) Q(W) + sG A: the accumulator takes Q codes and sG / (dy_scale
+  // w_scale), and the epilogue multiplies by dy_scale w_scale
+  if (dX != nullptr) {
+    void *at_ = at(ws, P.at_off);
+    LORA_TRY(run(LORA_K_PREP, st, "A^T", [&] {
+      return launch_transpose_scale_bf16(A, r, d_in, P.r_pad, nullptr, at_, st);
+    }));
+    MainGemmArgs b2;
+    b2.fp8 = true;
+    b2.bn = 256;
+    LORA_TRY(tmap_u8(&b2.tmA, dq, d_out, M, d_out, 128, "dY (e4m3)"));
+    LORA_TRY(tmap_u8(&b2.tmB, WqT, d_out, d_in, d_out, 128, "W^T (e4m3)"));
+    LORA_TRY(tmap(&b2.tmA2, sG, P.r_pad, M, P.r_pad * 2, 64, 128, "sG / row scale"));
+    LORA_TRY(tmap(&b2.tmB2, at_, P.r_pad, d_in, P.r_pad * 2, 64, 128, "A^T"));
+    b2.M = static_cast<int>(M);
+    b2.N = static_cast<int>(d_in);
+    b2.kb_main = static_cast<int>((d_out + 127) / 128);
+    b2.k_ext = P.r_pad;
+    b2.out = dX;
+    b2.ldo = d_in;
+    b2.row_scale = ds;
+    b2.dev_status = di.status;
+    if (split) {
+      b2.split_k = P.bsplit.k;
+      b2.split_rem = P.bsplit.rem;
+      b2.partials = reinterpret_cast<float *>(at(ws, P.bsplit_off));
+      b2.counters = counters;
+    }
+    LORA_TRY(run(LORA_K_MAIN_BWD, st, "fp8 dX GEMM",
+                 [&] { return launch_main_gemm(b2, di.sms, st); }));
+  }
+
+  // dA^T = X^T sG   (the unscaled transpose)
+  SkinnyArgs b3;
+  LORA_TRY(tmap(&b3.tmA, X, d_in, M, d_in * 2, 64, 64, "X^T"));
+  LORA_TRY(tmap(&b3.tmB, sGt, M, P.r_pad, P.Mp * 2, 64, P.r_pad, "sG^T"));
+  b3.a_mn = true;
+  b3.rows = static_cast<int>(d_in);
+  b3.RP = P.r_pad;
+  b3.K = static_cast<int>(M);
+  b3.scale = 1.f;
+  b3.out1 = dA;
+  b3.ld1 = d_in;
+  b3.n1 = r;
+  b3.dev_status = di.status;
+  return run(LORA_K_GRAD_A, st, "dA pass", [&] { return launch_skinny(&b3, 1, di.sms, st); });
+}
+
 }  // namespace
 }  // namespace lora
 
@@ -1052,6 +1313,118 @@ lora_status_t lora_set_timing_events(void *const *events, int *kinds, int n_pair
 }
 
 int lora_timing_used(void) { return t_hook.used; }
+
+static int current_pairs(bool b_mn);
+
+// ---------------------------------------------------------------- fp8 frozen W
+static lora_status_t check_fp8_shape(int r, int64_t M, int64_t d_in, int64_t d_out,
+                                     float alpha) {
+  LORA_TRY(check_shape(r, M, d_in, d_out, LORA_BF16, alpha));
+  if (d_in % 16 != 0 || d_out % 16 != 0 || d_in > 65536 || d_out > 65536)
+    return fail(LORA_ERR_UNSUPPORTED,
+                "the fp8 variant needs d_in and d_out to be multiples of 16, at most 65536 "
+                "(got %lld, %lld)", (long long)d_in, (long long)d_out);
+  return LORA_OK;
+}
+
+size_t lora_fp8_quantize_w_workspace_bytes(void) { return 256; }
+
+lora_status_t lora_fp8_quantize_w(const void *W, int64_t d_out, int64_t d_in, void *Wq,
+                                  void *WqT, float *w_scale, void *workspace,
+                                  size_t workspace_bytes, void *stream) {
+  t_err.clear();
+  if (d_out < 1 || d_in < 1 || d_out % 16 != 0 || d_in % 16 != 0)
+    return fail(LORA_ERR_UNSUPPORTED, "d_out, d_in must be positive multiples of 16");
+  if (d_out > INT32_MAX / 2 || d_in > INT32_MAX / 2)
+    return fail(LORA_ERR_UNSUPPORTED, "a dimension exceeds 2^30");
+  LORA_TRY(check_ptr(W, "W"));
+  LORA_TRY(check_ptr(Wq, "Wq"));
+  LORA_TRY(check_ptr(WqT, "WqT"));
+  if (w_scale == nullptr) return fail(LORA_ERR_INVALID_ARG, "w_scale is NULL");
+  LORA_TRY(check_ws(workspace, workspace_bytes, lora_fp8_quantize_w_workspace_bytes()));
+  DevInfo di;
+  LORA_TRY(device_info(di));
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  return run(LORA_K_QUANT, st, "quantise W", [&] {
+    return launch_quant_tensor_e4m3(W, static_cast<int>(d_out), static_cast<int>(d_in),
+                                    static_cast<unsigned *>(workspace), Wq, WqT, w_scale, di.sms,
+                                    st);
+  });
+}
+
+lora_status_t lora_fp8_quantize_rows(const void *x, int64_t rows, int64_t cols, void *q,
+                                     float *scale, void *stream) {
+  t_err.clear();
+  if (rows < 0 || cols < 1 || cols % 16 != 0 || rows > INT32_MAX || cols > 65536)
+    return fail(LORA_ERR_UNSUPPORTED,
+                "rows >= 0 and cols a positive multiple of 16, at most 65536, needed");
+  if (rows == 0) return LORA_OK;
+  LORA_TRY(check_ptr(x, "x"));
+  LORA_TRY(check_ptr(q, "q"));
+  if (scale == nullptr) return fail(LORA_ERR_INVALID_ARG, "scale is NULL");
+  DevInfo di;
+  LORA_TRY(device_info(di));
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  return run(LORA_K_QUANT, st, "quantise rows",
+             [&] { return launch_quant_rows_e4m3(x, rows, cols, q, scale, nullptr, st); });
+}
+
+size_t lora_fp8_workspace_bytes(int64_t M, int64_t d_in, int64_t d_out, int r) {
+  if (M < 0 || d_in < 1 || d_out < 1 || r < 1 || r > 256) return 0;
+  const FpPlan P = make_fp_plan(M, d_in, d_out, r, current_pairs(false), current_pairs(false));
+  return P.fwd_ws > P.bwd_ws ? P.fwd_ws : P.bwd_ws;
+}
+
+lora_status_t lora_fp8_fwd(const void *X, const void *Wq, const float *w_scale, const void *A,
+                           const void *B, float alpha, int r, int64_t M, int64_t d_in,
+                           int64_t d_out, void *Y, void *saved, void *workspace,
+                           size_t workspace_bytes, void *stream) {
+  t_err.clear();
+  LORA_TRY(check_fp8_shape(r, M, d_in, d_out, alpha));
+  const bool empty = M == 0;
+  LORA_TRY(check_ptr(X, "X", empty));
+  LORA_TRY(check_ptr(Wq, "Wq"));
+  if (w_scale == nullptr) return fail(LORA_ERR_INVALID_ARG, "w_scale is NULL");
+  LORA_TRY(check_ptr(A, "A"));
+  LORA_TRY(check_ptr(B, "B"));
+  LORA_TRY(check_ptr(Y, "Y", empty));
+  LORA_TRY(check_ptr(saved, "saved", empty));
+  const FpPlan P = make_fp_plan(M, d_in, d_out, r, 0, 0);
+  LORA_TRY(check_ws(workspace, workspace_bytes, P.fwd_ws_min));
+  if (empty) return LORA_OK;
+  return fp8_fwd(X, Wq, w_scale, A, B, alpha, r, M, d_in, d_out, Y, saved, workspace,
+                 workspace_bytes, static_cast<cudaStream_t>(stream));
+}
+
+lora_status_t lora_fp8_bwd(const void *dY, const void *X, const void *WqT, const float *w_scale,
+                           const void *A, const void *B, const void *saved, float alpha, int r,
+                           int64_t M, int64_t d_in, int64_t d_out, void *dX, void *dA, void *dB,
+                           void *workspace, size_t workspace_bytes, void *stream) {
+  t_err.clear();
+  LORA_TRY(check_fp8_shape(r, M, d_in, d_out, alpha));
+  const bool empty = M == 0;
+  LORA_TRY(check_ptr(dY, "dY", empty));
+  LORA_TRY(check_ptr(X, "X", empty));
+  LORA_TRY(check_ptr(WqT, "WqT"));
+  if (w_scale == nullptr) return fail(LORA_ERR_INVALID_ARG, "w_scale is NULL");
+  LORA_TRY(check_ptr(A, "A"));
+  LORA_TRY(check_ptr(B, "B"));
+  LORA_TRY(check_ptr(saved, "saved", empty));
+  LORA_TRY(check_ptr(dX, "dX", true));
+  LORA_TRY(check_ptr(dA, "dA"));
+  LORA_TRY(check_ptr(dB, "dB"));
+  const FpPlan P = make_fp_plan(M, d_in, d_out, r, 0, 0);
+  LORA_TRY(check_ws(workspace, workspace_bytes, empty ? 0 : P.bwd_ws_min));
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  if (empty) {  // sums over zero tokens
+    cudaError_t e = cudaMemsetAsync(dA, 0, size_t(r) * d_in * 2, st);
+    if (e == cudaSuccess) e = cudaMemsetAsync(dB, 0, size_t(d_out) * r * 2, st);
+    if (e != cudaSuccess) return fail(LORA_ERR_CUDA, "zero dA/dB: %s", cudaGetErrorString(e));
+    return LORA_OK;
+  }
+  return fp8_bwd(dY, X, WqT, w_scale, A, B, saved, alpha, r, M, d_in, d_out, dX, dA, dB,
+                 workspace, workspace_bytes, st);
+}
 
 // ---------------------------------------------------------------- SwiGLU pair
 static lora_status_t check_sw_shape(int r, int64_t M, int64_t d_in, int64_t d_ff,

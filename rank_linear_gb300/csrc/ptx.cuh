@@ -224,6 +224,17 @@ __device__ __forceinline__ void tc_mma_bf16_pair(uint32_t d_tmem, uint64_t adesc
       "l"(adesc), "l"(bdesc), "r"(idesc), "r"(accumulate)
       : "memory");
 }
+// Same pair MMA with e4m3 A and B (kind::f8f6f4, K = 32 per instruction);
+// the fp32 accumulator may mix these with kind::f16 MMAs.
+__device__ __forceinline__ void tc_mma_f8_pair(uint32_t d_tmem, uint64_t adesc, uint64_t bdesc,
+                                               uint32_t idesc, uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "setp.ne.b32 p, %4, 0;\n\t"
+      "tcgen05.mma.cta_group::2.kind::f8f6f4 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
+      "l"(adesc), "l"(bdesc), "r"(idesc), "r"(accumulate)
+      : "memory");
+}
 // Arrive once on the mbarrier at offset `bar` of each CTA in cta_mask when
 // the pair MMAs issued so far by this thread have completed.
 __device__ __forceinline__ void tc_commit_pair_mc(uint32_t bar, uint16_t cta_mask) {
@@ -252,6 +263,14 @@ __host__ __device__ constexpr uint32_t idesc_bf16(uint32_t M, uint32_t N, bool a
          | (1u << 10)                    // B format: bf16
          | ((a_mn ? 1u : 0u) << 15)      // A major-ness
          | ((b_mn ? 1u : 0u) << 16)      // B major-ness
+         | ((N >> 3) << 17)              // N / 8
+         | ((M >> 4) << 24);             // M / 16
+}
+
+// Instruction descriptor of kind::f8f6f4 with e4m3 A and B (format code 0),
+// both K-major, and an fp32 accumulator.
+__host__ __device__ constexpr uint32_t idesc_e4m3(uint32_t M, uint32_t N) {
+  return (1u << 4)                       // accumulator format: f32
          | ((N >> 3) << 17)              // N / 8
          | ((M >> 4) << 24);             // M / 16
 }

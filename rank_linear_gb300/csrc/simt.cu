@@ -2,6 +2,7 @@
 // decomposition as the bf16 tensor-core path, and the small copies of the
 // adapter B that the tensor-core path reads.
 #include <cuda_bf16.h>
+#include <cuda_fp8.h>
 
 #include "internal.h"
 #include "ptx.cuh"
@@ -155,6 +156,138 @@ __global__ void k_stack_rows(const __nv_bfloat16 *__restrict__ Ag,
   }
 }
 
+// ---- e4m3 quantisation with power-of-two scales (fp8 frozen-W product) ----
+// The scale of a block with absolute maximum a > 0 is 2^e, e the smallest
+// integer with a <= 448 * 2^e (448 = 0.875 * 2^9, the largest e4m3 value);
+// a = 0 gives 2^0.  Dividing by it is exact, so the one rounding is the
+// conversion to e4m3 (nearest, ties to even, saturating).
+__device__ __forceinline__ int pow2_exponent(float a) {
+  if (!(a > 0.f)) return 0;
+  int k;
+  const float m = frexpf(a, &k);  // a = m 2^k, m in [0.5, 1)
+  return m <= 0.875f ? k - 9 : k - 8;
+}
+
+__device__ __forceinline__ uint8_t to_e4m3(float v) {
+  return static_cast<uint8_t>(__nv_cvt_float_to_fp8(v, __NV_SATFINITE, __NV_E4M3));
+}
+
+// One block per row of x [rows][cols] (cols a multiple of 8), each thread
+// holding up to 64 of the row's elements in registers (one pass over the
+// row): scale[row] = 2^e * (mul ? mul[0] : 1) and the codes
+// q[row][.] = round(x / 2^e).  blockDim.x * 64 >= cols.
+__global__ void __launch_bounds__(1024) k_quant_rows(const __nv_bfloat16 *__restrict__ x,
+                                                     int64_t cols, uint8_t *__restrict__ q,
+                                                     float *__restrict__ scale,
+                                                     const float *__restrict__ mul) {
+  __shared__ float wmax[32];
+  griddep_wait();
+  griddep_launch_dependents();
+  const int64_t row = blockIdx.x;
+  const __nv_bfloat16 *xr = x + row * cols;
+  uint4 v[8];
+  float a = 0.f;
+#pragma unroll
+  for (int j = 0; j < 8; ++j) {
+    const int64_t c = (threadIdx.x + int64_t(j) * blockDim.x) * 8;
+    v[j] = c < cols ? *reinterpret_cast<const uint4 *>(xr + c) : make_uint4(0u, 0u, 0u, 0u);
+    const __nv_bfloat162 *h = reinterpret_cast<const __nv_bfloat162 *>(&v[j]);
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      const float2 f = __bfloat1622float2(h[i]);
+      a = fmaxf(a, fmaxf(fabsf(f.x), fabsf(f.y)));
+    }
+  }
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) a = fmaxf(a, __shfl_xor_sync(0xffffffffu, a, o));
+  if ((threadIdx.x & 31) == 0) wmax[threadIdx.x >> 5] = a;
+  __syncthreads();
+  const int nw = (blockDim.x + 31) >> 5;
+  a = 0.f;
+  for (int i = 0; i < nw; ++i) a = fmaxf(a, wmax[i]);
+  const int e = pow2_exponent(a);
+  const float inv = ldexpf(1.f, -e);
+  if (threadIdx.x == 0) scale[row] = ldexpf(1.f, e) * (mul != nullptr ? mul[0] : 1.f);
+  uint8_t *qr = q + row * cols;
+#pragma unroll
+  for (int j = 0; j < 8; ++j) {
+    const int64_t c = (threadIdx.x + int64_t(j) * blockDim.x) * 8;
+    if (c >= cols) break;
+    const __nv_bfloat162 *h = reinterpret_cast<const __nv_bfloat162 *>(&v[j]);
+    uint32_t lo = 0, hi = 0;
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      const float2 f = __bfloat1622float2(h[i]);
+      const uint32_t pair = to_e4m3(f.x * inv) | (uint32_t(to_e4m3(f.y * inv)) << 8);
+      if (i < 2) lo |= pair << (16 * i);
+      else hi |= pair << (16 * (i - 2));
+    }
+    *reinterpret_cast<uint2 *>(qr + c) = make_uint2(lo, hi);
+  }
+}
+
+// amax_bits |= the bit pattern of max |w| (non-negative floats order like
+// their bit patterns, so an unsigned atomicMax finds the largest).
+__global__ void k_absmax_all(const __nv_bfloat16 *__restrict__ w, int64_t n,
+                             unsigned *__restrict__ amax_bits) {
+  griddep_wait();
+  griddep_launch_dependents();
+  float a = 0.f;
+  for (int64_t i = blockIdx.x * int64_t(blockDim.x) + threadIdx.x; i < n;
+       i += int64_t(gridDim.x) * blockDim.x)
+    a = fmaxf(a, fabsf(__bfloat162float(w[i])));
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) a = fmaxf(a, __shfl_xor_sync(0xffffffffu, a, o));
+  if ((threadIdx.x & 31) == 0) atomicMax(amax_bits, __float_as_uint(a));
+}
+
+// W [rows][cols] -> e4m3 codes q [rows][cols] and their transpose qT
+// [cols][rows], with one scale for the tensor (written to scale[0]); 32 x 32
+// tiles through shared memory.
+__global__ void k_quant_tensor(const __nv_bfloat16 *__restrict__ w, int rows, int cols,
+                               const unsigned *__restrict__ amax_bits, uint8_t *__restrict__ q,
+                               uint8_t *__restrict__ qT, float *__restrict__ scale) {
+  __shared__ uint8_t tile[32][33];
+  griddep_wait();
+  griddep_launch_dependents();
+  const int e = pow2_exponent(__uint_as_float(*amax_bits));
+  const float inv = ldexpf(1.f, -e);
+  if (blockIdx.x == 0 && blockIdx.y == 0 && threadIdx.x == 0 && threadIdx.y == 0)
+    scale[0] = ldexpf(1.f, e);
+  const int r0 = blockIdx.y * 32, c0 = blockIdx.x * 32;
+  for (int i = threadIdx.y; i < 32; i += 8) {
+    const int r = r0 + i, c = c0 + threadIdx.x;
+    uint8_t v = 0;
+    if (r < rows && c < cols) {
+      v = to_e4m3(__bfloat162float(w[int64_t(r) * cols + c]) * inv);
+      q[int64_t(r) * cols + c] = v;
+    }
+    tile[i][threadIdx.x] = v;
+  }
+  __syncthreads();
+  for (int i = threadIdx.y; i < 32; i += 8) {
+    const int c = c0 + i, r = r0 + threadIdx.x;
+    if (c < cols && r < rows) qT[int64_t(c) * rows + r] = tile[threadIdx.x][i];
+  }
+}
+
+// out [cols][r_pad] = (j < r ? in[j][col] : 0) / scale[0]   (in: [r][cols];
+// no scale: 1)
+__global__ void k_transpose_scale(const __nv_bfloat16 *__restrict__ in, int r, int64_t cols,
+                                  int r_pad, const float *__restrict__ scale,
+                                  __nv_bfloat16 *__restrict__ out) {
+  griddep_wait();
+  griddep_launch_dependents();
+  const float inv = scale != nullptr ? 1.f / scale[0] : 1.f;
+  const int64_t total = cols * r_pad;
+  for (int64_t i = blockIdx.x * int64_t(blockDim.x) + threadIdx.x; i < total;
+       i += int64_t(gridDim.x) * blockDim.x) {
+    const int64_t k = i / r_pad;
+    const int j = static_cast<int>(i % r_pad);
+    out[i] = __float2bfloat16_rn(j < r ? __bfloat162float(in[j * cols + k]) * inv : 0.f);
+  }
+}
+
 // Launch with programmatic stream serialisation allowed (every kernel of the
 // library waits on griddep_wait before touching global memory).
 template <typename... KArgs, typename... Args>
@@ -186,6 +319,42 @@ cudaError_t launch_swiglu_grad_bf16(const void *dH, const void *gate, const void
                     static_cast<const __nv_bfloat16 *>(gate),
                     static_cast<const __nv_bfloat16 *>(up), M, d_ff, half,
                     static_cast<__nv_bfloat16 *>(D));
+}
+
+cudaError_t launch_quant_rows_e4m3(const void *x, int64_t rows, int64_t cols, void *q,
+                                   float *scale, const float *mul, cudaStream_t s) {
+  if (rows <= 0) return cudaSuccess;
+  if (cols > 1024 * 64) return cudaErrorInvalidValue;
+  const int threads = static_cast<int>(((cols + 63) / 64 + 31) / 32 * 32);
+  return launch_pdl(k_quant_rows, dim3(static_cast<unsigned>(rows)), dim3(threads), s,
+                    static_cast<const __nv_bfloat16 *>(x), cols, static_cast<uint8_t *>(q), scale,
+                    mul);
+}
+
+cudaError_t launch_quant_tensor_e4m3(const void *w, int rows, int cols, unsigned *amax_bits,
+                                     void *q, void *qT, float *scale, int num_sms,
+                                     cudaStream_t s) {
+  cudaError_t e = cudaMemsetAsync(amax_bits, 0, sizeof(unsigned), s);
+  if (e != cudaSuccess) return e;
+  const int64_t n = int64_t(rows) * cols;
+  const int64_t want = (n + 255) / 256;
+  const int blocks = static_cast<int>(want < 4LL * num_sms ? want : 4LL * num_sms);
+  e = launch_pdl(k_absmax_all, dim3(blocks > 0 ? blocks : 1), dim3(256), s,
+                 static_cast<const __nv_bfloat16 *>(w), n, amax_bits);
+  if (e != cudaSuccess) return e;
+  dim3 grid((cols + 31) / 32, (rows + 31) / 32), block(32, 8);
+  return launch_pdl(k_quant_tensor, grid, block, s, static_cast<const __nv_bfloat16 *>(w), rows,
+                    cols, static_cast<const unsigned *>(amax_bits), static_cast<uint8_t *>(q),
+                    static_cast<uint8_t *>(qT), scale);
+}
+
+cudaError_t launch_transpose_scale_bf16(const void *in, int r, int64_t cols, int r_pad,
+                                        const float *scale, void *out, cudaStream_t s) {
+  const int64_t total = cols * r_pad;
+  const int blocks = static_cast<int>(total / 256 + 1 < 4096 ? total / 256 + 1 : 4096);
+  return launch_pdl(k_transpose_scale, dim3(blocks), dim3(256), s,
+                    static_cast<const __nv_bfloat16 *>(in), r, cols, r_pad, scale,
+                    static_cast<__nv_bfloat16 *>(out));
 }
 
 cudaError_t launch_stack_rows_bf16(const void *Ag, const void *Au, int r, int r_pad, int64_t d_in,

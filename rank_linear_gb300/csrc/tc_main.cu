@@ -175,7 +175,7 @@ __device__ __forceinline__ void store_gated(const float (&g)[32], const float (&
   store_chunk(pk, stage, lane, out, ldo, row0, col0, M, N);
 }
 
-template <bool B_MN, int BN, bool SPLIT, bool GATED, bool DUAL_B>
+template <bool B_MN, int BN, bool SPLIT, bool GATED, bool DUAL_B, bool FP8>
 __global__ void __launch_bounds__(NUM_THREADS, 1)
     k_main_gemm(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                 const __grid_constant__ CUtensorMap tmA2, const __grid_constant__ CUtensorMap tmB2,
@@ -183,8 +183,10 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                 int M, int N, int kb_main, int k_ext, int kb_switch, int ext_shift,
                 __nv_bfloat16 *__restrict__ out, __nv_bfloat16 *__restrict__ aux0,
                 __nv_bfloat16 *__restrict__ aux1, int64_t ldo, int split_k, int split_rem,
-                float *__restrict__ partials, unsigned *counters, unsigned *dev_status) {
+                float *__restrict__ partials, unsigned *counters, unsigned *dev_status,
+                const float *__restrict__ row_scale, const float *__restrict__ w_scale) {
   static_assert(!(GATED && B_MN), "the gated pair reads K-major B");
+  static_assert(!(FP8 && (B_MN || GATED || DUAL_B)), "the fp8 product reads K-major operands");
   constexpr int TN = GATED ? BN / 2 : BN;  // output columns per pair tile
   using G = Geo<BN>;
   constexpr int STAGES = G::STAGES;
@@ -286,7 +288,8 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
             dep_done = true;
           }
           const CUtensorMap *ta = ext ? &tmA2 : &tmA;
-          const int k0 = (ext ? kb - kb_main : kb) * BK;  // K of A
+          // K of A: the fp8 main segment's 128-byte rows hold 2 x BK elements
+          const int k0 = ext ? (kb - kb_main) * BK : kb * (FP8 ? 2 * BK : BK);
           // B: the odd CTA of the gated pair reads the up projection (its
           // extension shifted so it meets the second half of [sH_g | sH_u]);
           // otherwise the main segment switches to tmB3 at kb_switch
@@ -349,6 +352,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     // ------------------------------------------------------ MMA issuer (even CTA)
     if (leader && lane == 0) {
       constexpr uint32_t idesc = idesc_bf16(CLUSTER * BM, BN, false, B_MN);
+      constexpr uint32_t idesc8 = idesc_e4m3(CLUSTER * BM, BN);
       // per 16-wide K step: 32 B along a K-major row, or two 1 KB MN-major
       // swizzle atoms (descriptor units of 16 B)
       constexpr uint64_t A_STEP = 32 >> 4, B_STEP = B_MN ? (2048 >> 4) : (32 >> 4);
@@ -385,9 +389,14 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
           }
           tc_fence_after();
           if (kb < kb_main) {
+            // fp8: four K = 32 steps of 32 bytes each, like bf16's K = 16
 #pragma unroll
-            for (int kk = 0; kk < BK / 16; ++kk)
-              tc_mma_bf16_pair(d, ad + kk * A_STEP, bd + kk * B_STEP, idesc, kk ? 1u : accum);
+            for (int kk = 0; kk < BK / 16; ++kk) {
+              if constexpr (FP8)
+                tc_mma_f8_pair(d, ad + kk * A_STEP, bd + kk * B_STEP, idesc8, kk ? 1u : accum);
+              else
+                tc_mma_bf16_pair(d, ad + kk * A_STEP, bd + kk * B_STEP, idesc, kk ? 1u : accum);
+            }
           } else {
             const int nk = min(BK / 16, (k_ext - (kb - kb_main) * BK) / 16);
             for (int kk = 0; kk < nk; ++kk)
@@ -443,6 +452,11 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
       const uint32_t taddr = tmem_base + (static_cast<uint32_t>(qd * 32) << 16) + acc * BN;
       uint8_t *stage = epi_stage + qd * EPI_WARP_BYTES;
       const int row0 = (2 * mp + q) * BM + qd * 32;
+      float sc = 1.f;  // fp8 product: this thread's row scale times W's scale
+      if constexpr (FP8) {
+        const int row = row0 + lane;
+        sc = (row < M ? __ldg(row_scale + row) : 0.f) * (w_scale != nullptr ? __ldg(w_scale) : 1.f);
+      }
       if (!SPLIT || !split) {
         if constexpr (GATED) {  // columns [0, TN) gate, [TN, 2 TN) up
 #pragma unroll 1
@@ -457,6 +471,10 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
           for (int c = 0; c < BN / 32; ++c) {
             float v[32];
             tmem_ld_32cols(taddr + c * 32, v);
+            if constexpr (FP8) {
+#pragma unroll
+              for (int i = 0; i < 32; ++i) v[i] *= sc;
+            }
             uint32_t pk[16];
 #pragma unroll
             for (int i = 0; i < 16; ++i) pk[i] = pack_bf16x2(v[2 * i], v[2 * i + 1]);
@@ -540,7 +558,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
             uint32_t pk[16];
 #pragma unroll
             for (int i = 0; i < 16; ++i)
-              pk[i] = pack_bf16x2(v[2 * i] + o[2 * i], v[2 * i + 1] + o[2 * i + 1]);
+              pk[i] = pack_bf16x2((v[2 * i] + o[2 * i]) * sc, (v[2 * i + 1] + o[2 * i + 1]) * sc);
             store_chunk(pk, stage, lane, out, ldo, row0, nb * BN + c * 32, M, N);
           }
         }
@@ -566,9 +584,10 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
   }
 }
 
-template <bool B_MN, int BN, bool SPLIT, bool GATED = false, bool DUAL_B = false>
+template <bool B_MN, int BN, bool SPLIT, bool GATED = false, bool DUAL_B = false,
+          bool FP8 = false>
 constexpr auto kernel_of() {
-  return &k_main_gemm<B_MN, BN, SPLIT, GATED, DUAL_B>;
+  return &k_main_gemm<B_MN, BN, SPLIT, GATED, DUAL_B, FP8>;
 }
 
 int g_max_clusters[64][2] = {};
@@ -604,13 +623,13 @@ int max_clusters(int num_sms) {
   return n;
 }
 
-template <bool B_MN, int BN, bool SPLIT, bool GATED, bool DUAL_B>
+template <bool B_MN, int BN, bool SPLIT, bool GATED, bool DUAL_B, bool FP8 = false>
 cudaError_t launch_variant(const MainGemmArgs &a, int num_sms, cudaStream_t s) {
   constexpr int TN = GATED ? BN / 2 : BN;
   const int m_tiles = (a.M + BM - 1) / BM, n_tiles = (a.N + TN - 1) / TN;
   const int tiles = ((m_tiles + 1) / 2) * n_tiles;  // pair tiles
   if (tiles == 0) return cudaSuccess;
-  auto kern = kernel_of<B_MN, BN, SPLIT, GATED, DUAL_B>();
+  auto kern = kernel_of<B_MN, BN, SPLIT, GATED, DUAL_B, FP8>();
   constexpr size_t smem = smem_bytes<BN>();
   cudaError_t e =
       cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));
@@ -640,7 +659,7 @@ cudaError_t launch_variant(const MainGemmArgs &a, int num_sms, cudaStream_t s) {
                             static_cast<__nv_bfloat16 *>(a.out),
                             static_cast<__nv_bfloat16 *>(a.aux0),
                             static_cast<__nv_bfloat16 *>(a.aux1), a.ldo, a.split_k, a.split_rem,
-                            a.partials, a.counters, a.dev_status);
+                            a.partials, a.counters, a.dev_status, a.row_scale, a.w_scale);
 }
 
 }  // namespace
@@ -675,6 +694,12 @@ int main_gemm_pick_bn(int, int, int) { return 256; }
 
 cudaError_t launch_main_gemm(const MainGemmArgs &a, int num_sms, cudaStream_t s) {
   const bool split = a.split_k > 1 && a.split_rem > 0;
+  if (a.fp8) {  // e4m3 main segment, K-major operands only
+    if (a.b_mn || a.gated || a.kb_switch >= 0 || !a.row_scale)
+      return cudaErrorInvalidValue;
+    return split ? launch_variant<false, 256, true, false, false, true>(a, num_sms, s)
+                 : launch_variant<false, 256, false, false, false, true>(a, num_sms, s);
+  }
   if (a.gated) {
     if (a.b_mn || a.kb_switch >= 0) return cudaErrorInvalidValue;
     return split ? launch_variant<false, 256, true, true, false>(a, num_sms, s)

@@ -58,6 +58,7 @@ struct Prob {
   __nv_bfloat16 *out1 = nullptr;
   int64_t ld1 = 0;
   int n1 = 0;
+  const float *row_div = nullptr;  // out0 row m divided by row_div[m]
 };
 
 struct Params {
@@ -326,6 +327,13 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     *reinterpret_cast<float4 *>(red + keep * pitch + c4 * 4) = acc;
     const int row = m0 + r_lo + rr;
     if (pr.out0 != nullptr && row < pr.rows) {
+      if (pr.row_div != nullptr) {  // a power of two: the reciprocal is exact
+        const float inv = 1.f / pr.row_div[row];
+        acc.x *= inv;
+        acc.y *= inv;
+        acc.z *= inv;
+        acc.w *= inv;
+      }
       const int c = c4 * 4;
       __nv_bfloat16 *o = pr.out0 + static_cast<int64_t>(row) * pr.ld0 + c;
       if (vec0 && c + 4 <= pr.n0) {
@@ -384,6 +392,7 @@ Prob to_prob(const SkinnyArgs &a, int S) {
   p.out1 = static_cast<__nv_bfloat16 *>(a.out1);
   p.ld1 = a.ld1;
   p.n1 = a.n1;
+  p.row_div = a.row_div;
   return p;
 }
 

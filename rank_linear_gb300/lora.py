@@ -239,3 +239,92 @@ def lora_swiglu(X, Wg, Ag, Bg, Wu, Au, Bu, alpha: float):
     """silu(X Wg^T + s X Ag^T Bg^T) * (X Wu^T + s X Au^T Bu^T) with gradients for
     X and the four adapter matrices (Wg, Wu frozen)."""
     return LoRASwiGLUFunction.apply(X, Wg, Ag, Bg, Wu, Au, Bu, alpha)
+
+
+# ---------------------------------------------------------------- fp8 frozen W
+# The LoRA layer with its frozen-weight product on e4m3 values (ch05
+# "Acceleration principles: Triton kernels and fused LoRA", §5.9 fp8 over the
+# LoRA layer of §5.3): W quantised once with one power-of-two scale, X and dY
+# per row on every call; the low-rank extension and dA, dB stay bf16.
+
+class FP8Weight(tuple):
+    """(Wq [d_out, d_in], WqT [d_in, d_out]) e4m3 bytes and w_scale (1 float)."""
+    __slots__ = ()
+
+    def __new__(cls, Wq, WqT, w_scale):
+        return super().__new__(cls, (Wq, WqT, w_scale))
+
+    Wq = property(lambda self: self[0])
+    WqT = property(lambda self: self[1])
+    w_scale = property(lambda self: self[2])
+
+
+def quantize_w_fp8(W, stream=None) -> FP8Weight:
+    """Quantise a frozen bf16 W once for the fp8 layer."""
+    _check_dev(W)
+    d_out, d_in = W.shape
+    L = _lib.lib()
+    Wq = torch.empty(d_out, d_in, dtype=torch.uint8, device=W.device)
+    WqT = torch.empty(d_in, d_out, dtype=torch.uint8, device=W.device)
+    scale = torch.empty(1, dtype=torch.float32, device=W.device)
+    ws = _buffer(L.lora_fp8_quantize_w_workspace_bytes(), W.device)
+    _lib.check(L.lora_fp8_quantize_w(_ptr(W), d_out, d_in, _ptr(Wq), _ptr(WqT), _ptr(scale),
+                                     _ptr(ws), ws.numel(), _stream_ptr(stream)),
+               "lora_fp8_quantize_w")
+    return FP8Weight(Wq, WqT, scale)
+
+
+def quantize_rows_fp8(x, stream=None):
+    """(codes [rows, cols] uint8, scale [rows] float32) of a bf16 matrix."""
+    _check_dev(x)
+    rows, cols = x.shape
+    q = torch.empty(rows, cols, dtype=torch.uint8, device=x.device)
+    scale = torch.empty(max(rows, 1), dtype=torch.float32, device=x.device)
+    _lib.check(_lib.lib().lora_fp8_quantize_rows(_ptr(x), rows, cols, _ptr(q), _ptr(scale),
+                                                  _stream_ptr(stream)), "lora_fp8_quantize_rows")
+    return q, scale[:rows]
+
+
+def fp8_workspace_bytes(M: int, d_in: int, d_out: int, r: int) -> int:
+    return int(_lib.lib().lora_fp8_workspace_bytes(M, d_in, d_out, r))
+
+
+def fp8_forward(X, qw: FP8Weight, A, B, alpha: float, *, Y=None, saved=None, workspace=None,
+                stream=None):
+    """Y = Q(X) Q(W)^T + (alpha/r) X A^T B^T.  Returns (Y, saved)."""
+    _check_dev(X, A, B)
+    M, d_in = X.shape
+    d_out, r = B.shape
+    L = _lib.lib()
+    if Y is None:
+        Y = torch.empty(M, d_out, dtype=X.dtype, device=X.device)
+    if saved is None:
+        saved = _buffer(L.lora_linear_saved_bytes(M, r, _lib.LORA_BF16), X.device)
+    if workspace is None:
+        workspace = _buffer(L.lora_fp8_workspace_bytes(M, d_in, d_out, r), X.device)
+    st = L.lora_fp8_fwd(_ptr(X), _ptr(qw.Wq), _ptr(qw.w_scale), _ptr(A), _ptr(B), float(alpha),
+                        r, M, d_in, d_out, _ptr(Y), _ptr(saved), _ptr(workspace),
+                        workspace.numel(), _stream_ptr(stream))
+    _lib.check(st, "lora_fp8_fwd")
+    return Y, saved
+
+
+def fp8_backward(dY, X, qw: FP8Weight, A, B, alpha: float, saved, *, need_dX=True, dX=None,
+                 dA=None, dB=None, workspace=None, stream=None):
+    """Returns (dX or None, dA, dB) for the upstream gradient dY."""
+    _check_dev(dY, X, A, B)
+    M, d_in = X.shape
+    d_out, r = B.shape
+    L = _lib.lib()
+    if need_dX and dX is None:
+        dX = torch.empty(M, d_in, dtype=X.dtype, device=X.device)
+    dA = torch.empty(r, d_in, dtype=X.dtype, device=X.device) if dA is None else dA
+    dB = torch.empty(d_out, r, dtype=X.dtype, device=X.device) if dB is None else dB
+    if workspace is None:
+        workspace = _buffer(L.lora_fp8_workspace_bytes(M, d_in, d_out, r), X.device)
+    st = L.lora_fp8_bwd(_ptr(dY), _ptr(X), _ptr(qw.WqT), _ptr(qw.w_scale), _ptr(A), _ptr(B),
+                        _ptr(saved), float(alpha), r, M, d_in, d_out,
+                        _ptr(dX) if need_dX else None, _ptr(dA), _ptr(dB), _ptr(workspace),
+                        workspace.numel(), _stream_ptr(stream))
+    _lib.check(st, "lora_fp8_bwd")
+    return (dX if need_dX else None), dA, dB

@@ -36,7 +36,8 @@ class Workload:
     alpha: float
     dtype: str    # "bf16" or "fp32"
     # "linear": one LoRA layer; "swiglu": the gate/up pair, d_out = FFN width
-    # (the up projection's W, A, B are drawn with seed + 1000)
+    # (the up projection's W, A, B are drawn with seed + 1000); "fp8": one
+    # LoRA layer whose frozen-W product runs on e4m3 values
     layer: str = "linear"
 
     def as_dict(self) -> dict:
@@ -52,6 +53,8 @@ WORKLOADS = {
         Workload("llama3_8b_down_proj", 8192, 14336, 4096, 64, 128.0, "bf16"),
         Workload("qwen_wide_ffn", 16384, 5120, 27648, 128, 256.0, "bf16"),
         Workload("llama3_8b_swiglu_gate_up", 8192, 4096, 14336, 16, 32.0, "bf16", "swiglu"),
+        Workload("llama3_8b_q_proj_fp8", 4096, 4096, 4096, 16, 16.0, "bf16", "fp8"),
+        Workload("llama3_8b_gate_up_fp8", 8192, 4096, 14336, 16, 32.0, "bf16", "fp8"),
     ]
 }
 

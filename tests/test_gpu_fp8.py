@@ -1,0 +1,133 @@
+"""The LoRA layer with an fp8 (e4m3) frozen-W product, on the GPU vs the
+oracle (needs a GB300).
+
+Quantisation is byte work: the codes and scales of W and of X's rows must
+equal the oracle's exactly (both sides take every rounding decision in exact
+arithmetic, the scales being powers of two).  The layer's outputs are
+compared with max|T_gpu - T_ref| / max|T_ref| <= 1e-2, the oracle applying
+the same quantisation; small ragged shapes element by element, the 4096^2
+q_proj shape on sampled rows of Y and dX and on all of dA and dB.
+"""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from oracle import fp8 as ofp8
+import rank_linear_gb300 as rl
+from rank_linear_gb300.synth import make_inputs
+
+pytestmark = pytest.mark.gpu
+
+TOL = 1e-2
+DEV = "cuda:0"
+
+
+def rel_err(got, ref) -> float:
+    if isinstance(got, torch.Tensor):
+        got = got.detach().double().cpu().numpy()
+    den = np.abs(ref).max()
+    return float(np.abs(got - ref).max() / (den if den > 0 else 1.0))
+
+
+def inputs(M, d_in, d_out, r, seed):
+    t = make_inputs(M, d_in, d_out, r, "bf16", seed=seed)
+    t["B"] = (t["B"].float() * 10).bfloat16()  # a low-rank term that matters
+    return t
+
+
+def run_gpu(t, alpha, need_dX=True):
+    g = {k: v.to(DEV) for k, v in t.items()}
+    qw = rl.quantize_w_fp8(g["W"])
+    Y, saved = rl.fp8_forward(g["X"], qw, g["A"], g["B"], alpha)
+    dX, dA, dB = rl.fp8_backward(g["dY"], g["X"], qw, g["A"], g["B"], alpha, saved,
+                                 need_dX=need_dX)
+    torch.cuda.synchronize()
+    rl.device_status()
+    return Y, dX, dA, dB
+
+
+def test_w_quantisation_is_byte_exact():
+    t = make_inputs(64, 4096, 1040, 16, "bf16", seed=3)
+    W = (t["W"].float() * torch.linspace(0.01, 3.0, 4096)).bfloat16()  # a wide range
+    qw = rl.quantize_w_fp8(W.to(DEV))
+    torch.cuda.synchronize()
+    codes, scale = ofp8.quantize_tensor(W)
+    assert np.array_equal(qw.Wq.cpu().numpy(), codes)
+    assert np.array_equal(qw.WqT.cpu().numpy(), codes.T)
+    assert float(qw.w_scale.item()) == scale
+
+
+def test_row_quantisation_is_byte_exact():
+    x = make_inputs(777, 1024, 16, 16, "bf16", seed=4)["X"]
+    x = (x.float() * torch.exp(torch.linspace(-20, 20, 777))[:, None]).bfloat16()
+    x[5] = 0.0  # an all-zero row gets scale 1
+    q, scale = rl.quantize_rows_fp8(x.to(DEV))
+    torch.cuda.synchronize()
+    codes, ref_scale = ofp8.quantize_rows(x)
+    assert np.array_equal(scale.cpu().numpy().astype(np.float64), ref_scale)
+    assert np.array_equal(q.cpu().numpy(), codes)
+
+
+# M, d_in, d_out, r, alpha (d_in, d_out multiples of 16)
+SMALL = [
+    (300, 384, 272, 16, 32.0),     # ragged M and N, K not a multiple of 128
+    (129, 144, 272, 12, 24.0),     # r not a multiple of 8
+    (1, 64, 64, 1, 2.0),           # one token, rank one
+    (256, 512, 384, 256, 512.0),   # maximum rank
+    (1000, 1024, 768, 64, 128.0),
+    (2048, 1536, 2560, 128, 256.0),
+    (1024, 4096, 5120, 16, 32.0),  # both GEMMs' last waves split two ways
+]
+
+
+@pytest.mark.parametrize("shape", SMALL, ids=lambda s: "x".join(map(str, s[:4])))
+def test_small_against_oracle(shape):
+    M, d_in, d_out, r, alpha = shape
+    t = inputs(M, d_in, d_out, r, seed=sum(shape[:4]))
+    got = run_gpu(t, alpha)
+    _, Yr = ofp8.forward(t["X"], t["W"], t["A"], t["B"], alpha)
+    ref = (Yr,) + tuple(ofp8.backward(t["dY"], t["X"], t["W"], t["A"], t["B"], alpha))
+    errs = {n: rel_err(g, e) for n, g, e in zip(("Y", "dX", "dA", "dB"), got, ref)}
+    for n, e in errs.items():
+        assert e <= TOL, f"{n}: {e:.3e} ({errs})"
+
+
+def test_q_proj_shape_sampled():
+    M = d_in = d_out = 4096
+    r, alpha = 16, 16.0
+    t = inputs(M, d_in, d_out, r, seed=0)
+    Y, dX, dA, dB = run_gpu(t, alpha)
+    X, W, A, B, dY = (oracle._f64(t[k]) for k in ("X", "W", "A", "B", "dY"))
+    s = alpha / r
+    Wq, ws = ofp8.quantize_tensor(W)
+    Wd = ofp8.e4m3_decode(Wq) * ws
+    rows = np.array([0, 1, 255, 256, 2047, 2048, 4000, 4095])
+    xq, xs = ofp8.quantize_rows(X[rows])
+    dq, dsc = ofp8.quantize_rows(dY[rows])
+    H = X @ A.T
+    G = dY @ B
+    Y_rows = ofp8.dequant_rows(xq, xs) @ Wd.T + s * H[rows] @ B.T
+    dX_rows = ofp8.dequant_rows(dq, dsc) @ Wd + s * G[rows] @ A
+    assert rel_err(Y[rows], Y_rows) <= TOL
+    assert rel_err(dX[rows], dX_rows) <= TOL
+    assert rel_err(dA, s * G.T @ X) <= TOL
+    assert rel_err(dB, s * dY.T @ H) <= TOL
+
+
+def test_deterministic():
+    t = inputs(1000, 1024, 768, 64, seed=5)
+    a = run_gpu(t, 128.0)
+    b = run_gpu(t, 128.0)
+    for x, y in zip(a, b):
+        assert torch.equal(x, y)
+
+
+def test_close_to_the_bf16_layer():
+    """fp8 quantisation of X, W, dY is the only difference from the bf16 layer."""
+    t = inputs(512, 1024, 1024, 16, seed=6)
+    g = {k: v.to(DEV) for k, v in t.items()}
+    Y8 = run_gpu(t, 32.0)[0]
+    Y16, _ = rl.forward(g["X"], g["W"], g["A"], g["B"], 32.0)
+    torch.cuda.synchronize()
+    assert rel_err(Y8, Y16.double().cpu().numpy()) < 0.1
