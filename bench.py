@@ -219,6 +219,12 @@ def oracle_run(t, alpha, layer="linear"):
         fp8.forward(t["X"], t["W"], t["A"], t["B"], alpha)
         fp8.backward(t["dY"], t["X"], t["W"], t["A"], t["B"], alpha)
         return
+    if layer == "q4":
+        from oracle import q4
+        codes, scales = q4.quantize_w(t["W"])
+        q4.forward(t["X"], codes, scales, t["A"], t["B"], alpha)
+        q4.backward(t["dY"], t["X"], codes, scales, t["A"], t["B"], alpha)
+        return
     if "Wu" in t:
         from oracle import swiglu
         args = [t[k] for k in ("X", "W", "A", "B", "Wu", "Au", "Bu")]
@@ -317,6 +323,7 @@ def run_ours(args, w):
 
     swiglu = w.layer == "swiglu"
     fp8 = w.layer == "fp8"
+    q4 = w.layer == "q4"
     # CPU baseline first (rank 0, N = 1 only), before the GPU is busy
     cpu = cpu_baseline(w) if (rank == 0 and world == 1 and not args.no_cpu_baseline) else None
 
@@ -348,6 +355,14 @@ def run_ours(args, w):
             rl.fp8_forward(X, qw, A, B, alpha, Y=Y, saved=saved, workspace=ws, stream=stream)
             rl.fp8_backward(dY, X, qw, A, B, alpha, saved, dX=dX, dA=dA, dB=dB, workspace=ws,
                             stream=stream)
+
+    if q4:  # the frozen W quantised to 4 bits once (outside the timed steps)
+        qw4 = rl.quantize_w_q4(W)
+
+        def step():
+            rl.q4_forward(X, qw4, A, B, alpha, Y=Y, saved=saved, workspace=ws, stream=stream)
+            rl.q4_backward(dY, X, qw4, A, B, alpha, saved, dX=dX, dA=dA, dB=dB, workspace=ws,
+                           stream=stream)
 
     if swiglu:  # the gate/up pair: H = silu(gate) * up, d_out = FFN width
         tu = make_inputs(M, d_in, d_out, r, w.dtype, seed=rank + 1000, device=dev,
@@ -447,7 +462,8 @@ def run_ours(args, w):
                 "unit": unit, "frac": ach / peak, "peak_source": peaks["source"] + peak_note,
                 "traffic": load_traffic(w.name, dom)}
 
-    e2e = None if (args.no_e2e or swiglu or fp8) else run_e2e(args, w, t, tdt, dev, stream, world)
+    e2e = None if (args.no_e2e or swiglu or fp8 or q4) else run_e2e(args, w, t, tdt, dev, stream,
+                                                                     world)
 
     if rank == 0:
         line = {
@@ -455,7 +471,9 @@ def run_ours(args, w):
             "steps": args.steps, "warmup": args.warmup,
             "ms_per_step": 1e3 * sec / args.steps, "higher_is_better": True,
             "scaling": "weak", "vs_baseline": None,
-            "dtype": "e4m3 W product, bf16 elsewhere" if fp8 else w.dtype, "data": "synthetic",
+            "dtype": ("e4m3 W product, bf16 elsewhere" if fp8 else
+                      "4-bit W codes expanded to bf16, bf16 elsewhere" if q4 else w.dtype),
+            "data": "synthetic",
             "config": {"workload": w.name, "layer": w.layer, "M": M, "d_in": d_in,
                        "d_out": d_out, "r": r,
                        "alpha": alpha, "l2": "flushed before every step (256 MiB write)",

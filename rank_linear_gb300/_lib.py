@@ -45,6 +45,12 @@ SIGNATURES = {
                       _sz, _vp], _int),
     "lora_fp8_bwd": ([_vp, _vp, _vp, _vp, _vp, _vp, _vp, _f32, _int, _i64, _i64, _i64, _vp,
                       _vp, _vp, _vp, _sz, _vp], _int),
+    "lora_q4_quantize_w": ([_vp, _i64, _i64, _vp, _vp, _vp], _int),
+    "lora_q4_dequantize_w": ([_vp, _vp, _i64, _i64, _vp, _vp], _int),
+    "lora_q4_fwd": ([_vp, _vp, _vp, _vp, _vp, _f32, _int, _i64, _i64, _i64, _vp, _vp, _vp, _sz,
+                     _vp], _int),
+    "lora_q4_bwd": ([_vp, _vp, _vp, _vp, _vp, _vp, _vp, _f32, _int, _i64, _i64, _i64, _vp, _vp,
+                     _vp, _vp, _sz, _vp], _int),
     "lora_swiglu_saved_bytes": ([_i64, _i64, _int], _sz),
     "lora_swiglu_workspace_bytes": ([_i64, _i64, _i64, _int], _sz),
     "lora_swiglu_fwd": ([_vp, _vp, _vp, _vp, _vp, _vp, _vp, _f32, _int, _i64, _i64, _i64, _int,

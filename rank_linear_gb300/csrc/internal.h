@@ -50,6 +50,12 @@ struct MainGemmArgs {
   // multiplies row m of the result by row_scale[m] (times w_scale[0] if given).
   bool fp8 = false;
   const float *row_scale = nullptr, *w_scale = nullptr;
+  // 4-bit W main segment (bn 256): tmB holds the packed codes [d_out][d_in/2]
+  // bytes (box 32 bytes x 128 rows; with b_mn box 64 bytes x 64 rows) and
+  // tmB3 the bf16 group scales [d_in/64][d_out] (box 128 x 1; with b_mn
+  // 64 x 2).  Each CTA dequantises its half of the B tile to bf16 in shared
+  // memory before the MMAs read it.
+  bool q4 = false;
 };
 constexpr int kMainBM = 128, kMainBK = 64;
 int main_gemm_pick_bn(int M, int N, int num_sms);
@@ -138,6 +144,12 @@ cudaError_t launch_stack_rows_bf16(const void *Ag, const void *Au, int r, int r_
 // floats, the row's scale times mul[0] when mul is given.
 cudaError_t launch_quant_rows_e4m3(const void *x, int64_t rows, int64_t cols, void *q,
                                    float *scale, const float *mul, cudaStream_t s);
+// Symmetric 4-bit W [d_out][d_in] (d_in % 64 == 0): packed codes
+// [d_out][d_in / 2] bytes and bf16 group scales [d_in / 64][d_out]; and back.
+cudaError_t launch_quant_q4(const void *w, int d_out, int d_in, void *codes, void *scales,
+                            cudaStream_t s);
+cudaError_t launch_dequant_q4(const void *codes, const void *scales, int d_out, int d_in, void *w,
+                              int num_sms, cudaStream_t s);
 // One scale for all of w [rows][cols]: q [rows][cols], qT [cols][rows],
 // scale[0]; amax_bits is one word of device scratch.
 cudaError_t launch_quant_tensor_e4m3(const void *w, int rows, int cols, unsigned *amax_bits,

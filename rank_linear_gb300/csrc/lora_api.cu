@@ -14,6 +14,7 @@
 #include "internal.h"
 #include "lora_linear.h"
 #include "lora_fp8.h"
+#include "lora_q4.h"
 #include "lora_swiglu.h"
 #include "ptx.cuh"
 
@@ -122,6 +123,33 @@ lora_status_t tmap(CUtensorMap *tm, const void *ptr, uint64_t inner, uint64_t ou
                 (unsigned long long)pitch_bytes, static_cast<int>(r));
   return LORA_OK;
 }
+
+// Map without swizzle over a row-major [outer][inner] tensor of `dt`
+// elements (the 4-bit W's packed codes and group scales, staged raw).
+lora_status_t tmap_plain(CUtensorMap *tm, CUtensorMapDataType dt, const void *ptr, uint64_t inner,
+                         uint64_t outer, uint64_t pitch_bytes, uint32_t box_inner,
+                         uint32_t box_outer, const char *what) {
+  auto fn = encode_fn();
+  if (!fn) return fail(LORA_ERR_CUDA, "cuTensorMapEncodeTiled is not available from the driver");
+  cuuint64_t dims[2] = {inner, outer};
+  cuuint64_t strides[1] = {pitch_bytes};
+  cuuint32_t box[2] = {box_inner, box_outer};
+  cuuint32_t es[2] = {1, 1};
+  CUresult r = fn(tm, dt, 2, const_cast<void *>(ptr), dims, strides, box, es,
+                  CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
+                  CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  if (r != CUDA_SUCCESS)
+    return fail(LORA_ERR_CUDA, "tensor map for %s (%llu x %llu, pitch %llu) failed: CUresult %d",
+                what, (unsigned long long)outer, (unsigned long long)inner,
+                (unsigned long long)pitch_bytes, static_cast<int>(r));
+  return LORA_OK;
+}
+
+// A frozen W held as 4-bit codes: packed [d_out][d_in / 2] bytes (element
+// 2j in the low nibble of byte j) and bf16 group scales [d_in / 64][d_out].
+struct Q4W {
+  const void *codes = nullptr, *scales = nullptr;
+};
 
 // ---------------------------------------------------------------- launches
 template <class F>
@@ -292,7 +320,7 @@ lora_status_t down_fwd_bf16(const DevInfo &di, const Plan &P, const void *X, con
 
 lora_status_t fwd_bf16(const void *X, const void *W, const void *A, const void *B, float alpha,
                        int r, int64_t M, int64_t d_in, int64_t d_out, void *Y, void *saved,
-                       void *ws, size_t ws_bytes, cudaStream_t st) {
+                       void *ws, size_t ws_bytes, cudaStream_t st, const Q4W *q4 = nullptr) {
   DevInfo di;
   LORA_TRY(device_info(di));
   Plan P = make_plan(M, d_in, d_out, r, LORA_BF16, main_gemm_pairs(false, di.sms));
@@ -321,7 +349,15 @@ lora_status_t fwd_bf16(const void *X, const void *W, const void *A, const void *
   }
   f2.bn = main_gemm_pick_bn(static_cast<int>(M), static_cast<int>(d_out), di.sms);
   LORA_TRY(tmap(&f2.tmA, X, d_in, M, d_in * 2, 64, 128, "X"));
-  LORA_TRY(tmap(&f2.tmB, W, d_in, d_out, d_in * 2, 64, f2.bn / 2, "W"));
+  if (q4 != nullptr) {  // 128 rows x 64 codes, and their 128 scales, per K block
+    LORA_TRY(tmap_plain(&f2.tmB, CU_TENSOR_MAP_DATA_TYPE_UINT8, q4->codes, d_in / 2, d_out,
+                        d_in / 2, 32, 128, "W codes"));
+    LORA_TRY(tmap_plain(&f2.tmB3, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, q4->scales, d_out, d_in / 64,
+                        d_out * 2, 128, 1, "W scales"));
+    f2.q4 = true;
+  } else {
+    LORA_TRY(tmap(&f2.tmB, W, d_in, d_out, d_in * 2, 64, f2.bn / 2, "W"));
+  }
   LORA_TRY(tmap(&f2.tmA2, saved, P.r_pad, M, P.r_pad * 2, 64, 128, "sH"));
   LORA_TRY(tmap(&f2.tmB2, Bsrc, b_inner, d_out, b_inner * 2, 64, f2.bn / 2, "B"));
   f2.M = static_cast<int>(M);
@@ -338,7 +374,7 @@ lora_status_t fwd_bf16(const void *X, const void *W, const void *A, const void *
 lora_status_t bwd_bf16(const void *dY, const void *X, const void *W, const void *A, const void *B,
                        const void *saved, float alpha, int r, int64_t M, int64_t d_in,
                        int64_t d_out, void *dX, void *dA, void *dB, void *ws, size_t ws_bytes,
-                       cudaStream_t st) {
+                       cudaStream_t st, const Q4W *q4 = nullptr) {
   DevInfo di;
   LORA_TRY(device_info(di));
   Plan P = make_plan(M, d_in, d_out, r, LORA_BF16, main_gemm_pairs(true, di.sms));
@@ -408,7 +444,15 @@ lora_status_t bwd_bf16(const void *dY, const void *X, const void *W, const void 
     MainGemmArgs b2;
     b2.bn = main_gemm_pick_bn(static_cast<int>(M), static_cast<int>(d_in), di.sms);
     LORA_TRY(tmap(&b2.tmA, dY, d_out, M, d_out * 2, 64, 128, "dY"));
-    LORA_TRY(tmap(&b2.tmB, W, d_in, d_out, d_in * 2, 64, 64, "W (MN-major)"));
+    if (q4 != nullptr) {  // 64 K-rows x 128 codes, and the scales of 2 column groups
+      LORA_TRY(tmap_plain(&b2.tmB, CU_TENSOR_MAP_DATA_TYPE_UINT8, q4->codes, d_in / 2, d_out,
+                          d_in / 2, 64, 64, "W codes (MN-major)"));
+      LORA_TRY(tmap_plain(&b2.tmB3, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, q4->scales, d_out,
+                          d_in / 64, d_out * 2, 64, 2, "W scales (MN-major)"));
+      b2.q4 = true;
+    } else {
+      LORA_TRY(tmap(&b2.tmB, W, d_in, d_out, d_in * 2, 64, 64, "W (MN-major)"));
+    }
     LORA_TRY(tmap(&b2.tmA2, sG, P.r_pad, M, P.r_pad * 2, 64, 128, "sG"));
     LORA_TRY(tmap(&b2.tmB2, A, d_in, r, d_in * 2, 64, 64, "A (MN-major)"));
     b2.M = static_cast<int>(M);
@@ -1522,6 +1566,109 @@ lora_status_t lora_swiglu_bwd(const void *dH, const void *X, const void *Wg, con
   }
   return sw_bwd_bf16(dH, X, Wg, Ag, Bg, Wu, Au, Bu, saved, alpha, r, M, d_in, d_ff, dX, dAg, dBg,
                      dAu, dBu, workspace, workspace_bytes, st);
+}
+
+// ---------------------------------------------------------------- 4-bit frozen W
+static lora_status_t check_q4_dims(int64_t d_in, int64_t d_out) {
+  if (d_in < 64 || d_out < 8 || d_in % 64 != 0 || d_out % 8 != 0)
+    return fail(LORA_ERR_UNSUPPORTED,
+                "the 4-bit variant needs d_in a positive multiple of 64 and d_out of 8 "
+                "(got %lld, %lld)", (long long)d_in, (long long)d_out);
+  if (d_in > INT32_MAX / 2 || d_out > INT32_MAX / 2)
+    return fail(LORA_ERR_UNSUPPORTED, "a dimension exceeds 2^30");
+  return LORA_OK;
+}
+
+lora_status_t lora_q4_quantize_w(const void *W, int64_t d_out, int64_t d_in, void *codes,
+                                 void *scales, void *stream) {
+  t_err.clear();
+  LORA_TRY(check_q4_dims(d_in, d_out));
+  LORA_TRY(check_ptr(W, "W"));
+  LORA_TRY(check_ptr(codes, "codes"));
+  LORA_TRY(check_ptr(scales, "scales"));
+  DevInfo di;
+  LORA_TRY(device_info(di));
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  return run(LORA_K_QUANT, st, "quantise W to 4 bits", [&] {
+    return launch_quant_q4(W, static_cast<int>(d_out), static_cast<int>(d_in), codes, scales, st);
+  });
+}
+
+lora_status_t lora_q4_dequantize_w(const void *codes, const void *scales, int64_t d_out,
+                                   int64_t d_in, void *Wd, void *stream) {
+  t_err.clear();
+  LORA_TRY(check_q4_dims(d_in, d_out));
+  LORA_TRY(check_ptr(codes, "codes"));
+  LORA_TRY(check_ptr(scales, "scales"));
+  LORA_TRY(check_ptr(Wd, "Wd"));
+  DevInfo di;
+  LORA_TRY(device_info(di));
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  return run(LORA_K_QUANT, st, "dequantise 4-bit W", [&] {
+    return launch_dequant_q4(codes, scales, static_cast<int>(d_out), static_cast<int>(d_in), Wd,
+                             di.sms, st);
+  });
+}
+
+lora_status_t lora_q4_fwd(const void *X, const void *codes, const void *scales, const void *A,
+                          const void *B, float alpha, int r, int64_t M, int64_t d_in,
+                          int64_t d_out, void *Y, void *saved, void *workspace,
+                          size_t workspace_bytes, void *stream) {
+  t_err.clear();
+  LORA_TRY(check_shape(r, M, d_in, d_out, LORA_BF16, alpha));
+  LORA_TRY(check_q4_dims(d_in, d_out));
+  const bool empty = M == 0;
+  LORA_TRY(check_ptr(X, "X", empty));
+  LORA_TRY(check_ptr(codes, "codes"));
+  LORA_TRY(check_ptr(scales, "scales"));
+  LORA_TRY(check_ptr(A, "A"));
+  LORA_TRY(check_ptr(B, "B"));
+  LORA_TRY(check_ptr(Y, "Y", empty));
+  LORA_TRY(check_ptr(saved, "saved", empty));
+  const Plan P = make_plan(M, d_in, d_out, r, LORA_BF16);
+  LORA_TRY(check_ws(workspace, workspace_bytes, P.fwd_ws_min));
+  if (empty) return LORA_OK;
+  Q4W q4;
+  q4.codes = codes;
+  q4.scales = scales;
+  return fwd_bf16(X, nullptr, A, B, alpha, r, M, d_in, d_out, Y, saved, workspace,
+                  workspace_bytes, static_cast<cudaStream_t>(stream), &q4);
+}
+
+lora_status_t lora_q4_bwd(const void *dY, const void *X, const void *codes, const void *scales,
+                          const void *A, const void *B, const void *saved, float alpha, int r,
+                          int64_t M, int64_t d_in, int64_t d_out, void *dX, void *dA, void *dB,
+                          void *workspace, size_t workspace_bytes, void *stream) {
+  t_err.clear();
+  LORA_TRY(check_shape(r, M, d_in, d_out, LORA_BF16, alpha));
+  LORA_TRY(check_q4_dims(d_in, d_out));
+  const bool empty = M == 0;
+  LORA_TRY(check_ptr(dY, "dY", empty));
+  LORA_TRY(check_ptr(X, "X", empty));
+  LORA_TRY(check_ptr(codes, "codes"));
+  LORA_TRY(check_ptr(scales, "scales"));
+  LORA_TRY(check_ptr(A, "A"));
+  LORA_TRY(check_ptr(B, "B"));
+  LORA_TRY(check_ptr(saved, "saved", true));
+  LORA_TRY(check_ptr(dX, "dX", true));
+  LORA_TRY(check_ptr(dA, "dA"));
+  LORA_TRY(check_ptr(dB, "dB"));
+  const Plan P = make_plan(M, d_in, d_out, r, LORA_BF16);
+  size_t need = saved != nullptr ? P.bwd_ws_min : P.bwd_ws;
+  if (empty) need = 0;
+  LORA_TRY(check_ws(workspace, workspace_bytes, need));
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  if (empty) {  // sums over zero tokens
+    cudaError_t e = cudaMemsetAsync(dA, 0, size_t(r) * d_in * 2, st);
+    if (e == cudaSuccess) e = cudaMemsetAsync(dB, 0, size_t(d_out) * r * 2, st);
+    if (e != cudaSuccess) return fail(LORA_ERR_CUDA, "zero dA/dB: %s", cudaGetErrorString(e));
+    return LORA_OK;
+  }
+  Q4W q4;
+  q4.codes = codes;
+  q4.scales = scales;
+  return bwd_bf16(dY, X, nullptr, A, B, saved, alpha, r, M, d_in, d_out, dX, dA, dB, workspace,
+                  workspace_bytes, st, &q4);
 }
 
 lora_status_t lora_debug_withhold_arrive(int n) {

@@ -51,16 +51,32 @@ __device__ __forceinline__ void mbar_expect_tx(uint32_t bar, uint32_t bytes) {
 __device__ __forceinline__ void mbar_arrive(uint32_t bar) {
   asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(bar) : "memory");
 }
+// `count` arrivals at once.
+__device__ __forceinline__ void mbar_arrive_n(uint32_t bar, uint32_t count) {
+  asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0], %1;" ::"r"(bar), "r"(count) : "memory");
+}
 // One probe of the phase with the given parity (true = that phase completed).
+// kCluster: acquire at cluster scope, for a phase completed by arrivals that
+// publish another CTA's shared-memory writes.
+template <bool kCluster = false>
 __device__ __forceinline__ bool mbar_test(uint32_t bar, uint32_t parity) {
   uint32_t done;
-  asm volatile(
-      "{\n\t.reg .pred p;\n\t"
-      "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
-      "selp.b32 %0, 1, 0, p;\n\t}"
-      : "=r"(done)
-      : "r"(bar), "r"(parity)
-      : "memory");
+  if constexpr (kCluster)
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "mbarrier.try_wait.parity.acquire.cluster.shared::cta.b64 p, [%1], %2;\n\t"
+        "selp.b32 %0, 1, 0, p;\n\t}"
+        : "=r"(done)
+        : "r"(bar), "r"(parity)
+        : "memory");
+  else
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+        "selp.b32 %0, 1, 0, p;\n\t}"
+        : "=r"(done)
+        : "r"(bar), "r"(parity)
+        : "memory");
   return done != 0;
 }
 
@@ -68,11 +84,12 @@ __device__ __forceinline__ bool mbar_test(uint32_t bar, uint32_t parity) {
 // completing) when another role of the CTA already gave up, or when the
 // time limit passes -- then it raises the CTA's abort flag and ORs
 // kDevErrTimeout into the device status word.
+template <bool kCluster = false>
 __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, volatile int *abort_flag,
                                           unsigned *dev_status) {
-  if (mbar_test(bar, parity)) return true;
+  if (mbar_test<kCluster>(bar, parity)) return true;
   const uint64_t t0 = globaltimer_ns();
-  while (!mbar_test(bar, parity)) {
+  while (!mbar_test<kCluster>(bar, parity)) {
     if (*abort_flag) return false;
     if (globaltimer_ns() - t0 > kWaitLimitNs) {
       *abort_flag = 1;
@@ -252,6 +269,12 @@ __device__ __forceinline__ void tc_commit_pair(uint32_t bar) {
 // Arrive on an mbarrier given by a shared::cluster address (own or peer CTA).
 __device__ __forceinline__ void mbar_arrive_cluster(uint32_t cluster_bar) {
   asm volatile("mbarrier.arrive.release.cluster.shared::cluster.b64 _, [%0];" ::"r"(cluster_bar)
+               : "memory");
+}
+__device__ __forceinline__ void mbar_arrive_cluster_n(uint32_t cluster_bar, uint32_t count) {
+  asm volatile("mbarrier.arrive.release.cluster.shared::cluster.b64 _, [%0], %1;" ::"r"(
+                   cluster_bar),
+               "r"(count)
                : "memory");
 }
 

@@ -288,6 +288,79 @@ __global__ void k_transpose_scale(const __nv_bfloat16 *__restrict__ in, int r, i
   }
 }
 
+// ---- symmetric 4-bit W with bf16 scales per group of 64 along d_in ----
+// Thread (row o, group g) of W [d_out][d_in]: scale = bf16(absmax / 7) (1
+// when the group is all zero), code = clamp(rint(w / scale), -8, 7) + 8,
+// both divisions IEEE fp32; codes[o][g * 32 + j] holds elements 2j (low
+// nibble) and 2j + 1 of the group, scales[g][o] its scale.
+__global__ void __launch_bounds__(128) k_quant_q4(const __nv_bfloat16 *__restrict__ w, int d_out,
+                                                  int d_in, uint8_t *__restrict__ codes,
+                                                  __nv_bfloat16 *__restrict__ scales) {
+  griddep_wait();
+  griddep_launch_dependents();
+  const int o = blockIdx.x * blockDim.x + threadIdx.x, g = blockIdx.y;
+  if (o >= d_out) return;
+  const uint4 *src = reinterpret_cast<const uint4 *>(w + int64_t(o) * d_in + g * 64);
+  float v[64];
+  float a = 0.f;
+#pragma unroll
+  for (int j = 0; j < 8; ++j) {
+    const uint4 u = src[j];
+    const __nv_bfloat162 *h = reinterpret_cast<const __nv_bfloat162 *>(&u);
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      const float2 f = __bfloat1622float2(h[i]);
+      v[8 * j + 2 * i] = f.x;
+      v[8 * j + 2 * i + 1] = f.y;
+      a = fmaxf(a, fmaxf(fabsf(f.x), fabsf(f.y)));
+    }
+  }
+  __nv_bfloat16 sb = __float2bfloat16_rn(__fdiv_rn(a, 7.f));
+  if (__bfloat162float(sb) == 0.f) sb = __float2bfloat16_rn(1.f);
+  const float sc = __bfloat162float(sb);
+  uint32_t word[8];
+#pragma unroll
+  for (int j = 0; j < 8; ++j) {
+    uint32_t x = 0;
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+      const float q = fminf(fmaxf(rintf(__fdiv_rn(v[8 * j + i], sc)), -8.f), 7.f);
+      x |= static_cast<uint32_t>(static_cast<int>(q) + 8) << (4 * i);
+    }
+    word[j] = x;
+  }
+  uint4 *dst = reinterpret_cast<uint4 *>(codes + int64_t(o) * (d_in / 2) + g * 32);
+  dst[0] = make_uint4(word[0], word[1], word[2], word[3]);
+  dst[1] = make_uint4(word[4], word[5], word[6], word[7]);
+  scales[int64_t(g) * d_out + o] = sb;
+}
+
+// W[o][k] = bf16((code - 8) * scale): the product is exact in fp32, so the
+// one rounding is to bf16, nearest even.  One thread per 8 elements.
+__global__ void k_dequant_q4(const uint8_t *__restrict__ codes,
+                             const __nv_bfloat16 *__restrict__ scales, int d_out, int d_in,
+                             __nv_bfloat16 *__restrict__ w) {
+  griddep_wait();
+  griddep_launch_dependents();
+  const int64_t total = int64_t(d_out) * (d_in / 8);
+  for (int64_t i = blockIdx.x * int64_t(blockDim.x) + threadIdx.x; i < total;
+       i += int64_t(gridDim.x) * blockDim.x) {
+    const int o = static_cast<int>(i / (d_in / 8));
+    const int k0 = static_cast<int>(i % (d_in / 8)) * 8;
+    const uint32_t x = *reinterpret_cast<const uint32_t *>(codes + int64_t(o) * (d_in / 2) + k0 / 2);
+    const float sc = __bfloat162float(scales[int64_t(k0 / 64) * d_out + o]);
+    uint32_t out[4];
+#pragma unroll
+    for (int p = 0; p < 4; ++p) {
+      const float lo = static_cast<float>(static_cast<int>((x >> (8 * p)) & 0xF) - 8) * sc;
+      const float hi = static_cast<float>(static_cast<int>((x >> (8 * p + 4)) & 0xF) - 8) * sc;
+      const __nv_bfloat162 b = __floats2bfloat162_rn(lo, hi);
+      out[p] = *reinterpret_cast<const uint32_t *>(&b);
+    }
+    *reinterpret_cast<uint4 *>(w + int64_t(o) * d_in + k0) = make_uint4(out[0], out[1], out[2], out[3]);
+  }
+}
+
 // Launch with programmatic stream serialisation allowed (every kernel of the
 // library waits on griddep_wait before touching global memory).
 template <typename... KArgs, typename... Args>
@@ -346,6 +419,25 @@ cudaError_t launch_quant_tensor_e4m3(const void *w, int rows, int cols, unsigned
   return launch_pdl(k_quant_tensor, grid, block, s, static_cast<const __nv_bfloat16 *>(w), rows,
                     cols, static_cast<const unsigned *>(amax_bits), static_cast<uint8_t *>(q),
                     static_cast<uint8_t *>(qT), scale);
+}
+
+cudaError_t launch_quant_q4(const void *w, int d_out, int d_in, void *codes, void *scales,
+                            cudaStream_t s) {
+  if (d_in % 64 != 0) return cudaErrorInvalidValue;
+  dim3 grid((d_out + 127) / 128, d_in / 64);
+  return launch_pdl(k_quant_q4, grid, dim3(128), s, static_cast<const __nv_bfloat16 *>(w), d_out,
+                    d_in, static_cast<uint8_t *>(codes), static_cast<__nv_bfloat16 *>(scales));
+}
+
+cudaError_t launch_dequant_q4(const void *codes, const void *scales, int d_out, int d_in, void *w,
+                              int num_sms, cudaStream_t s) {
+  if (d_in % 64 != 0) return cudaErrorInvalidValue;
+  const int64_t want = (int64_t(d_out) * (d_in / 8) + 255) / 256;
+  const int blocks = static_cast<int>(want < 8LL * num_sms ? want : 8LL * num_sms);
+  return launch_pdl(k_dequant_q4, dim3(blocks > 0 ? blocks : 1), dim3(256), s,
+                    static_cast<const uint8_t *>(codes),
+                    static_cast<const __nv_bfloat16 *>(scales), d_out, d_in,
+                    static_cast<__nv_bfloat16 *>(w));
 }
 
 cudaError_t launch_transpose_scale_bf16(const void *in, int r, int64_t cols, int r_pad,

@@ -44,16 +44,22 @@ constexpr int CLUSTER = 2;                   // the CTA pair
 constexpr uint16_t PAIR_MASK = 0x3;
 constexpr uint32_t A_BYTES = BM * BK * 2;    // 16 KB: this CTA's 128 rows of A
 constexpr int NUM_THREADS = 192;             // producer warp, MMA warp, 4 epilogue warps
+constexpr int Q4_THREADS = 320;              // ... and 4 warps dequantising 4-bit W
+// 4-bit W stage: 128 B-tile rows of 64 codes (32 bytes) or 64 K-rows of 128
+// codes, then 128 bf16 scales
+constexpr uint32_t RAW_CODE_BYTES = 4096, RAW_BYTES = RAW_CODE_BYTES + 256;
 constexpr int GROUP_M = 4;                   // rasterisation: m-block pairs per group
 constexpr int EPI_ARRIVALS = 4 * CLUSTER;    // epilogue warps of both CTAs
 constexpr size_t kStageBudget = 192 * 1024;  // shared memory for the stage ring
 
-// Tile geometry for a pair tile of 256 x BN (BN = 128 or 256).
-template <int BN>
+// Tile geometry for a pair tile of 256 x BN (BN = 128 or 256); Q4 adds the
+// raw 4-bit codes and scales of a stage.
+template <int BN, bool Q4 = false>
 struct Geo {
   static constexpr uint32_t B_BYTES = BN / 2 * BK * 2;  // this CTA's half of B
-  static constexpr uint32_t STAGE_BYTES = A_BYTES + B_BYTES;
-  static constexpr uint32_t PAIR_TX = CLUSTER * STAGE_BYTES;  // bytes per stage for the pair
+  static constexpr uint32_t STAGE_BYTES = A_BYTES + B_BYTES + (Q4 ? RAW_BYTES : 0);
+  // bytes a stage's pair-TMA loads bring to the even CTA's barrier
+  static constexpr uint32_t PAIR_TX = CLUSTER * (A_BYTES + B_BYTES);
   static constexpr int STAGES_RAW = static_cast<int>(kStageBudget / STAGE_BYTES);
   static constexpr int STAGES = STAGES_RAW > 8 ? 8 : STAGES_RAW;
   static constexpr uint32_t TMEM_COLS = 2 * BN;  // two accumulators
@@ -62,6 +68,7 @@ struct Geo {
 template <int STAGES>
 struct __align__(8) MainTail {
   uint64_t full[STAGES];    // even CTA: both CTAs' loads of a stage landed
+  uint64_t rawfull[STAGES]; // each CTA (4-bit W): A and the raw codes landed
   uint64_t empty[STAGES];   // each CTA: the pair MMAs finished reading a stage
   uint64_t tfull[2];        // each CTA: an accumulator is complete
   uint64_t tempty[2];       // even CTA: both CTAs drained an accumulator
@@ -79,10 +86,10 @@ constexpr uint32_t EPI_PITCH = 80;
 constexpr uint32_t EPI_WARP_BYTES = 32 * EPI_PITCH;
 constexpr uint32_t EPI_BYTES = 4 * EPI_WARP_BYTES;
 
-template <int BN>
+template <int BN, bool Q4 = false>
 constexpr size_t smem_bytes() {
-  return 1024 + size_t(Geo<BN>::STAGES) * Geo<BN>::STAGE_BYTES + EPI_BYTES +
-         sizeof(MainTail<Geo<BN>::STAGES>);
+  return 1024 + size_t(Geo<BN, Q4>::STAGES) * Geo<BN, Q4>::STAGE_BYTES + EPI_BYTES +
+         sizeof(MainTail<Geo<BN, Q4>::STAGES>);
 }
 
 // Work item -> tile and K-block range.  Items below split_first are whole
@@ -121,6 +128,28 @@ __device__ __forceinline__ void tile_coords(int tile, int m_pairs, int n_tiles, 
 __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
   __nv_bfloat162 v = __floats2bfloat162_rn(lo, hi);
   return *reinterpret_cast<uint32_t *>(&v);
+}
+
+// Eight 4-bit codes (one 32-bit word, element 2j in the low nibble of byte
+// j, 2j+1 in its high nibble) -> eight bf16 weights (code - 8) * scale.
+// 0x4300 | c is the bf16 value 128 + c, exact for c < 16, so subtracting 136
+// leaves c - 8 exactly; the product with the bf16 scale is then rounded once
+// to bf16, nearest even.
+__device__ __forceinline__ uint4 dequant8(uint32_t w, __nv_bfloat162 scale2) {
+  const uint32_t lo = w & 0x0F0F0F0Fu, hi = (w >> 4) & 0x0F0F0F0Fu;
+  const uint32_t p01 = __byte_perm(lo, hi, 0x5140);  // bytes lo0 hi0 lo1 hi1
+  const uint32_t p23 = __byte_perm(lo, hi, 0x7362);  // bytes lo2 hi2 lo3 hi3
+  const uint32_t x[4] = {__byte_perm(p01, 0x43434343u, 0x4140), __byte_perm(p01, 0x43434343u, 0x4342),
+                         __byte_perm(p23, 0x43434343u, 0x4140), __byte_perm(p23, 0x43434343u, 0x4342)};
+  const __nv_bfloat162 off = __floats2bfloat162_rn(136.f, 136.f);
+  uint32_t o[4];
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    const __nv_bfloat162 c = __hsub2(*reinterpret_cast<const __nv_bfloat162 *>(&x[i]), off);
+    const __nv_bfloat162 v = __hmul2(c, scale2);
+    o[i] = *reinterpret_cast<const uint32_t *>(&v);
+  }
+  return make_uint4(o[0], o[1], o[2], o[3]);
 }
 
 // Writes a warp's 32 x 32 bf16 chunk (lane = row, pk = its 32 columns) to
@@ -175,8 +204,8 @@ __device__ __forceinline__ void store_gated(const float (&g)[32], const float (&
   store_chunk(pk, stage, lane, out, ldo, row0, col0, M, N);
 }
 
-template <bool B_MN, int BN, bool SPLIT, bool GATED, bool DUAL_B, bool FP8>
-__global__ void __launch_bounds__(NUM_THREADS, 1)
+template <bool B_MN, int BN, bool SPLIT, bool GATED, bool DUAL_B, bool FP8, bool Q4>
+__global__ void __launch_bounds__(Q4 ? Q4_THREADS : NUM_THREADS, 1)
     k_main_gemm(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                 const __grid_constant__ CUtensorMap tmA2, const __grid_constant__ CUtensorMap tmB2,
                 const __grid_constant__ CUtensorMap tmB3, const __grid_constant__ CUtensorMap tmB4,
@@ -187,8 +216,9 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                 const float *__restrict__ row_scale, const float *__restrict__ w_scale) {
   static_assert(!(GATED && B_MN), "the gated pair reads K-major B");
   static_assert(!(FP8 && (B_MN || GATED || DUAL_B)), "the fp8 product reads K-major operands");
+  static_assert(!(Q4 && (GATED || DUAL_B || FP8)), "4-bit W: plain layer only");
   constexpr int TN = GATED ? BN / 2 : BN;  // output columns per pair tile
-  using G = Geo<BN>;
+  using G = Geo<BN, Q4>;
   constexpr int STAGES = G::STAGES;
   constexpr uint32_t B_BYTES = G::B_BYTES, STAGE_BYTES = G::STAGE_BYTES, PAIR_TX = G::PAIR_TX;
   constexpr uint32_t TMEM_COLS = G::TMEM_COLS;
@@ -199,6 +229,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
   auto *tail = reinterpret_cast<MainTail<STAGES> *>(epi_stage + EPI_BYTES);
   const uint32_t sA = base;
   const uint32_t sB = base + STAGES * A_BYTES;
+  const uint32_t sRaw = sB + STAGES * B_BYTES;  // 4-bit W: codes and scales per stage
 
   const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
   const int q = static_cast<int>(cluster_ctarank());  // 0: even (MMA-issuing) CTA, 1: odd
@@ -220,7 +251,11 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < STAGES; ++s) {
-      mbar_init(smem_u32(&tail->full[s]), 1);   // the even CTA's expect_tx arrival
+      // the even CTA's expect_tx arrival, or (4-bit W) one arrival from each
+      // dequantising warp of both CTAs, matched on extension stages by the
+      // producers' arrivals
+      mbar_init(smem_u32(&tail->full[s]), Q4 ? 8 : 1);
+      mbar_init(smem_u32(&tail->rawfull[s]), 1);
       mbar_init(smem_u32(&tail->empty[s]), 1);  // the even CTA's multicast commit
     }
     for (int a = 0; a < 2; ++a) {
@@ -260,7 +295,9 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     // ------------------------------------------------------ TMA producer
     if (lane == 0) {
       uint32_t issued[STAGES];
-      for (int s = 0; s < STAGES; ++s) issued[s] = 0;
+      uint32_t rissued[STAGES];  // 4-bit W: main-segment loads on rawfull[s]
+      uint32_t last_ext = 0;     // 4-bit W: stages whose last load was an extension one
+      for (int s = 0; s < STAGES; ++s) issued[s] = rissued[s] = 0;
       int stage = 0;
       uint32_t phase = 0;
       bool ok = true;
@@ -281,8 +318,45 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
           }
           const uint32_t full_local = smem_u32(&tail->full[stage]);
           const uint32_t full = dsmem_map(full_local, 0);  // the even CTA's barrier
-          if (leader) mbar_expect_tx(full_local, PAIR_TX);
           const bool ext = kb >= kb_main;
+          if constexpr (Q4) {
+            if (!ext) {
+              // A and this CTA's 4-bit codes and scales land on its own
+              // rawfull barrier; its dequantising warps turn the codes into
+              // the bf16 B tile and arrive on the even CTA's full barrier
+              const uint32_t rf = smem_u32(&tail->rawfull[stage]);
+              const int k0 = kb * BK;
+              const uint32_t rw = sRaw + stage * RAW_BYTES;
+              mbar_expect_tx(rf, A_BYTES + RAW_BYTES);
+              tma_load_2d(sA + stage * A_BYTES, &tmA, rf, k0, m0);
+              if (B_MN) {  // 64 K-rows x 128 codes (64 bytes); scales of 2 column groups
+                tma_load_2d(rw, &tmB, rf, n0 / 2, k0);
+                tma_load_2d(rw + RAW_CODE_BYTES, &tmB3, rf, k0, n0 / 64);
+              } else {  // 128 rows x 64 codes (32 bytes); their scales
+                tma_load_2d(rw, &tmB, rf, k0 / 2, n0);
+                tma_load_2d(rw + RAW_CODE_BYTES, &tmB3, rf, n0, k0 / 64);
+              }
+              issued[stage] += 1;
+              rissued[stage] += 1;
+              last_ext &= ~(1u << stage);
+              if (++stage == STAGES) {
+                stage = 0;
+                phase ^= 1u;
+              }
+              continue;
+            }
+            // extension stage: pair loads, plus the arrivals that stand in for
+            // the four dequantising warps of each CTA
+            if (leader) {
+              mbar_expect_tx(full_local, PAIR_TX);
+              mbar_arrive_n(full_local, 3);
+            } else {
+              mbar_arrive_cluster_n(full, 4);
+            }
+            last_ext |= 1u << stage;
+          } else {
+            if (leader) mbar_expect_tx(full_local, PAIR_TX);
+          }
           if (ext && !dep_done) {  // sH / sG come from the preceding kernel
             griddep_wait();
             dep_done = true;
@@ -333,10 +407,15 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
           }
       }
       if (!clean) {  // aborting: let the pair's copies in flight land before exiting
+        if constexpr (Q4) {  // this CTA's own main-segment copies
+          for (int s = 0; s < STAGES; ++s)
+            if (rissued[s]) mbar_wait_drain(smem_u32(&tail->rawfull[s]), (rissued[s] - 1u) & 1u);
+        }
         if (leader) {
           // a phase the even CTA armed completes when both CTAs' bytes landed
           for (int s = 0; s < STAGES; ++s)
-            if (issued[s]) mbar_wait_drain(smem_u32(&tail->full[s]), (issued[s] - 1u) & 1u);
+            if (issued[s] && (!Q4 || (last_ext >> s) & 1u))
+              mbar_wait_drain(smem_u32(&tail->full[s]), (issued[s] - 1u) & 1u);
         } else {
           // The odd CTA's copies complete on the even CTA's barriers, which it
           // cannot poll; one it issued for a phase the even CTA never armed
@@ -383,7 +462,9 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         uint64_t bd = b_desc0 + stage * (B_BYTES >> 4);
         uint32_t accum = 0;
         for (int kb = kb_lo; kb < kb_hi; ++kb) {
-          if (!mbar_wait(smem_u32(&tail->full[stage]), phase, abort_flag, dev_status)) {
+          // 4-bit W: the phase also publishes the dequantising warps' stores,
+          // some made by the other CTA of the pair
+          if (!mbar_wait<Q4>(smem_u32(&tail->full[stage]), phase, abort_flag, dev_status)) {
             ok = false;
             break;
           }
@@ -419,6 +500,74 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
       if (!ok) {  // wait for this thread's MMAs in flight before TMEM is freed
         tc_commit_pair(smem_u32(&tail->drain));
         mbar_wait_drain(smem_u32(&tail->drain), 0);
+      }
+    }
+  } else if (Q4 && warp >= 6) {
+    // ------------------------------------------------------ 4-bit W dequantisation (both CTAs)
+    // On each main-segment stage: this CTA's codes and bf16 group scales ->
+    // its bf16 half of the B tile, in the layout the TMA writes for bf16 W
+    // (128-byte swizzle; K-major forward, two MN-major atoms backward); then
+    // one arrival per warp on the even CTA's full barrier.  The stage's
+    // previous B tile is free: its rawfull phase was armed only after the
+    // pair MMAs released the stage.
+    const int dw = warp - 6;
+    const uint8_t *raw_base = smem_raw + (sRaw - raw);
+    uint8_t *b_base = smem_raw + (sB - raw);
+    int stage = 0;
+    uint32_t rbits = 0;  // per stage: parity of its next rawfull phase
+    bool ok = true;
+    for (int item = pair_id; item < num_items && ok; item += num_pairs) {
+      int tile, kb_lo, kb_hi, chunk, rel;
+      item_range(item, split_first, split_k, split_rem, kb_total, tile, kb_lo, kb_hi, chunk, rel);
+      for (int kb = kb_lo; kb < kb_hi; ++kb) {
+        if (kb < kb_main) {
+          const bool got = mbar_wait(smem_u32(&tail->rawfull[stage]), (rbits >> stage) & 1u,
+                                     abort_flag, dev_status);
+          if (!__all_sync(0xffffffffu, got)) {
+            ok = false;
+            break;
+          }
+          rbits ^= 1u << stage;
+          const uint8_t *rw = raw_base + stage * RAW_BYTES;
+          uint8_t *bt = b_base + stage * B_BYTES;
+          // this thread's 64 codes (32 bytes), their scale, and where its
+          // eight 16-byte chunks go (chunk i at slot i ^ (line & 7))
+          const uint8_t *src;
+          uint16_t sbits;
+          uint8_t *dst;
+          int sw;
+          if constexpr (B_MN) {  // K-row k of one 64-column half a
+            const int k = dw * 16 + (lane & 15), a = lane >> 4;
+            src = rw + k * 64 + a * 32;
+            sbits = *reinterpret_cast<const uint16_t *>(rw + RAW_CODE_BYTES + (a * 64 + k) * 2);
+            dst = bt + a * 8192 + (k >> 3) * 1024 + (k & 7) * 128;
+            sw = k & 7;
+          } else {  // B-tile row n (one output column)
+            const int n = dw * 32 + lane;
+            src = rw + n * 32;
+            sbits = *reinterpret_cast<const uint16_t *>(rw + RAW_CODE_BYTES + n * 2);
+            dst = bt + (n >> 3) * 1024 + (n & 7) * 128;
+            sw = n & 7;
+          }
+          const uint4 c0 = *reinterpret_cast<const uint4 *>(src);
+          const uint4 c1 = *reinterpret_cast<const uint4 *>(src + 16);
+          const uint32_t s2 = static_cast<uint32_t>(sbits) * 0x10001u;
+          const __nv_bfloat162 scale2 = *reinterpret_cast<const __nv_bfloat162 *>(&s2);
+          const uint32_t w[8] = {c0.x, c0.y, c0.z, c0.w, c1.x, c1.y, c1.z, c1.w};
+#pragma unroll
+          for (int i = 0; i < 8; ++i)
+            *reinterpret_cast<uint4 *>(dst + ((i ^ sw) << 4)) = dequant8(w[i], scale2);
+          fence_proxy_async_smem();  // visible to the tensor cores
+          __syncwarp();
+          if (lane == 0) {
+            const uint32_t fl = smem_u32(&tail->full[stage]);
+            if (leader)
+              mbar_arrive(fl);
+            else
+              mbar_arrive_cluster(dsmem_map(fl, 0));
+          }
+        }
+        if (++stage == STAGES) stage = 0;
       }
     }
   } else {
@@ -585,26 +734,26 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
 }
 
 template <bool B_MN, int BN, bool SPLIT, bool GATED = false, bool DUAL_B = false,
-          bool FP8 = false>
+          bool FP8 = false, bool Q4 = false>
 constexpr auto kernel_of() {
-  return &k_main_gemm<B_MN, BN, SPLIT, GATED, DUAL_B, FP8>;
+  return &k_main_gemm<B_MN, BN, SPLIT, GATED, DUAL_B, FP8, Q4>;
 }
 
-int g_max_clusters[64][2] = {};
+int g_max_clusters[64][4] = {};
 
 // Largest number of two-CTA clusters of a kernel variant that can be
 // resident at once (queried once per device; the variant's shared-memory
 // attribute must already be set).
-template <bool B_MN, int BN>
+template <bool B_MN, int BN, bool Q4 = false>
 int max_clusters(int num_sms) {
   int dev = 0;
   cudaGetDevice(&dev);
-  int &n = g_max_clusters[dev & 63][B_MN ? 1 : 0];
+  int &n = g_max_clusters[dev & 63][(B_MN ? 1 : 0) + (Q4 ? 2 : 0)];
   if (n == 0) {
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(static_cast<unsigned>(num_sms / CLUSTER * CLUSTER), 1, 1);
-    cfg.blockDim = dim3(NUM_THREADS, 1, 1);
-    cfg.dynamicSmemBytes = smem_bytes<BN>();
+    cfg.blockDim = dim3(Q4 ? Q4_THREADS : NUM_THREADS, 1, 1);
+    cfg.dynamicSmemBytes = smem_bytes<BN, Q4>();
     cudaLaunchAttribute attr[1];
     attr[0].id = cudaLaunchAttributeClusterDimension;
     attr[0].val.clusterDim.x = CLUSTER;
@@ -613,7 +762,8 @@ int max_clusters(int num_sms) {
     cfg.attrs = attr;
     cfg.numAttrs = 1;
     int c = 0;
-    if (cudaOccupancyMaxActiveClusters(&c, kernel_of<B_MN, BN, false>(), &cfg) != cudaSuccess ||
+    if (cudaOccupancyMaxActiveClusters(&c, kernel_of<B_MN, BN, false, false, false, false, Q4>(),
+                                       &cfg) != cudaSuccess ||
         c < 1) {
       cudaGetLastError();  // clear; fall back to one cluster per SM pair
       c = num_sms / CLUSTER;
@@ -623,22 +773,23 @@ int max_clusters(int num_sms) {
   return n;
 }
 
-template <bool B_MN, int BN, bool SPLIT, bool GATED, bool DUAL_B, bool FP8 = false>
+template <bool B_MN, int BN, bool SPLIT, bool GATED, bool DUAL_B, bool FP8 = false,
+          bool Q4 = false>
 cudaError_t launch_variant(const MainGemmArgs &a, int num_sms, cudaStream_t s) {
   constexpr int TN = GATED ? BN / 2 : BN;
   const int m_tiles = (a.M + BM - 1) / BM, n_tiles = (a.N + TN - 1) / TN;
   const int tiles = ((m_tiles + 1) / 2) * n_tiles;  // pair tiles
   if (tiles == 0) return cudaSuccess;
-  auto kern = kernel_of<B_MN, BN, SPLIT, GATED, DUAL_B, FP8>();
-  constexpr size_t smem = smem_bytes<BN>();
+  auto kern = kernel_of<B_MN, BN, SPLIT, GATED, DUAL_B, FP8, Q4>();
+  constexpr size_t smem = smem_bytes<BN, Q4>();
   cudaError_t e =
       cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));
   if (e != cudaSuccess) return e;
-  const int maxc = max_clusters<B_MN, BN>(num_sms);
+  const int maxc = max_clusters<B_MN, BN, Q4>(num_sms);
   const int clusters = tiles < maxc ? tiles : maxc;
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(static_cast<unsigned>(clusters * CLUSTER), 1, 1);
-  cfg.blockDim = dim3(NUM_THREADS, 1, 1);
+  cfg.blockDim = dim3(Q4 ? Q4_THREADS : NUM_THREADS, 1, 1);
   cfg.dynamicSmemBytes = smem;
   cfg.stream = s;
   cudaLaunchAttribute attr[2];
@@ -652,7 +803,7 @@ cudaError_t launch_variant(const MainGemmArgs &a, int num_sms, cudaStream_t s) {
   cfg.numAttrs = 2;
   // without a second B segment the switch point lies past every K block
   const int kb_switch = a.kb_switch >= 0 ? a.kb_switch : (1 << 30);
-  const CUtensorMap &tmB3 = (GATED || a.kb_switch >= 0) ? a.tmB3 : a.tmB;
+  const CUtensorMap &tmB3 = (GATED || Q4 || a.kb_switch >= 0) ? a.tmB3 : a.tmB;
   const CUtensorMap &tmB4 = GATED ? a.tmB4 : a.tmB2;
   return cudaLaunchKernelEx(&cfg, kern, a.tmA, a.tmB, a.tmA2, a.tmB2, tmB3, tmB4, a.M, a.N,
                             a.kb_main, a.k_ext, kb_switch, a.ext_shift,
@@ -694,6 +845,14 @@ int main_gemm_pick_bn(int, int, int) { return 256; }
 
 cudaError_t launch_main_gemm(const MainGemmArgs &a, int num_sms, cudaStream_t s) {
   const bool split = a.split_k > 1 && a.split_rem > 0;
+  if (a.q4) {  // 4-bit W: codes in tmB, bf16 group scales in tmB3
+    if (a.fp8 || a.gated || a.kb_switch >= 0) return cudaErrorInvalidValue;
+    if (a.b_mn)
+      return split ? launch_variant<true, 256, true, false, false, false, true>(a, num_sms, s)
+                   : launch_variant<true, 256, false, false, false, false, true>(a, num_sms, s);
+    return split ? launch_variant<false, 256, true, false, false, false, true>(a, num_sms, s)
+                 : launch_variant<false, 256, false, false, false, false, true>(a, num_sms, s);
+  }
   if (a.fp8) {  // e4m3 main segment, K-major operands only
     if (a.b_mn || a.gated || a.kb_switch >= 0 || !a.row_scale)
       return cudaErrorInvalidValue;

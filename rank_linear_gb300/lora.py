@@ -328,3 +328,84 @@ def fp8_backward(dY, X, qw: FP8Weight, A, B, alpha: float, saved, *, need_dX=Tru
                         workspace.numel(), _stream_ptr(stream))
     _lib.check(st, "lora_fp8_bwd")
     return (dX if need_dX else None), dA, dB
+
+
+# The LoRA layer over a 4-bit frozen W (ch05 "Acceleration principles: Triton
+# kernels and fused LoRA", §5.3's layer with QLoRA's 4-bit base weight, and
+# the Unsloth inference notes' on-chip dequantisation): symmetric INT4 codes
+# with one bf16 scale per 64 weights along d_in, expanded to bf16 in shared
+# memory inside the GEMMs.
+
+class Q4Weight(tuple):
+    """(codes [d_out, d_in / 2] uint8, scales [d_in / 64, d_out] bf16)."""
+    __slots__ = ()
+
+    def __new__(cls, codes, scales):
+        return super().__new__(cls, (codes, scales))
+
+    codes = property(lambda self: self[0])
+    scales = property(lambda self: self[1])
+
+
+def quantize_w_q4(W, stream=None) -> Q4Weight:
+    """Quantise a frozen bf16 W [d_out, d_in] (d_in % 64 == 0) to 4 bits once."""
+    _check_dev(W)
+    d_out, d_in = W.shape
+    codes = torch.empty(d_out, d_in // 2, dtype=torch.uint8, device=W.device)
+    scales = torch.empty(max(d_in // 64, 1), d_out, dtype=torch.bfloat16, device=W.device)
+    _lib.check(_lib.lib().lora_q4_quantize_w(_ptr(W), d_out, d_in, _ptr(codes), _ptr(scales),
+                                             _stream_ptr(stream)), "lora_q4_quantize_w")
+    return Q4Weight(codes, scales)
+
+
+def dequantize_w_q4(qw: Q4Weight, stream=None):
+    """The bf16 W [d_out, d_in] the 4-bit layer computes with."""
+    d_out, half = qw.codes.shape
+    Wd = torch.empty(d_out, 2 * half, dtype=torch.bfloat16, device=qw.codes.device)
+    _lib.check(_lib.lib().lora_q4_dequantize_w(_ptr(qw.codes), _ptr(qw.scales), d_out, 2 * half,
+                                               _ptr(Wd), _stream_ptr(stream)),
+               "lora_q4_dequantize_w")
+    return Wd
+
+
+def q4_forward(X, qw: Q4Weight, A, B, alpha: float, *, Y=None, saved=None, workspace=None,
+               stream=None):
+    """Y = X Wd^T + (alpha/r) X A^T B^T.  Returns (Y, saved)."""
+    _check_dev(X, A, B, qw.codes, qw.scales)
+    M, d_in = X.shape
+    d_out, r = B.shape
+    L = _lib.lib()
+    if Y is None:
+        Y = torch.empty(M, d_out, dtype=X.dtype, device=X.device)
+    if saved is None:
+        saved = _buffer(L.lora_linear_saved_bytes(M, r, _lib.LORA_BF16), X.device)
+    if workspace is None:
+        workspace = _buffer(L.lora_linear_workspace_bytes(M, d_in, d_out, r, _lib.LORA_BF16),
+                            X.device)
+    st = L.lora_q4_fwd(_ptr(X), _ptr(qw.codes), _ptr(qw.scales), _ptr(A), _ptr(B), float(alpha),
+                       r, M, d_in, d_out, _ptr(Y), _ptr(saved), _ptr(workspace),
+                       workspace.numel(), _stream_ptr(stream))
+    _lib.check(st, "lora_q4_fwd")
+    return Y, saved
+
+
+def q4_backward(dY, X, qw: Q4Weight, A, B, alpha: float, saved=None, *, need_dX=True, dX=None,
+                dA=None, dB=None, workspace=None, stream=None):
+    """Returns (dX or None, dA, dB) for the upstream gradient dY."""
+    _check_dev(dY, X, A, B, qw.codes, qw.scales)
+    M, d_in = X.shape
+    d_out, r = B.shape
+    L = _lib.lib()
+    if need_dX and dX is None:
+        dX = torch.empty(M, d_in, dtype=X.dtype, device=X.device)
+    dA = torch.empty(r, d_in, dtype=X.dtype, device=X.device) if dA is None else dA
+    dB = torch.empty(d_out, r, dtype=X.dtype, device=X.device) if dB is None else dB
+    if workspace is None:
+        workspace = _buffer(L.lora_linear_workspace_bytes(M, d_in, d_out, r, _lib.LORA_BF16),
+                            X.device)
+    st = L.lora_q4_bwd(_ptr(dY), _ptr(X), _ptr(qw.codes), _ptr(qw.scales), _ptr(A), _ptr(B),
+                       _ptr(saved), float(alpha), r, M, d_in, d_out,
+                       _ptr(dX) if need_dX else None, _ptr(dA), _ptr(dB), _ptr(workspace),
+                       workspace.numel(), _stream_ptr(stream))
+    _lib.check(st, "lora_q4_bwd")
+    return (dX if need_dX else None), dA, dB

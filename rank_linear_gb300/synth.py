@@ -37,7 +37,8 @@ class Workload:
     dtype: str    # "bf16" or "fp32"
     # "linear": one LoRA layer; "swiglu": the gate/up pair, d_out = FFN width
     # (the up projection's W, A, B are drawn with seed + 1000); "fp8": one
-    # LoRA layer whose frozen-W product runs on e4m3 values
+    # LoRA layer whose frozen-W product runs on e4m3 values; "q4": one LoRA
+    # layer over a 4-bit frozen W (codes + bf16 scales per 64 weights)
     layer: str = "linear"
 
     def as_dict(self) -> dict:
@@ -55,6 +56,8 @@ WORKLOADS = {
         Workload("llama3_8b_swiglu_gate_up", 8192, 4096, 14336, 16, 32.0, "bf16", "swiglu"),
         Workload("llama3_8b_q_proj_fp8", 4096, 4096, 4096, 16, 16.0, "bf16", "fp8"),
         Workload("llama3_8b_gate_up_fp8", 8192, 4096, 14336, 16, 32.0, "bf16", "fp8"),
+        Workload("llama3_8b_q_proj_q4", 4096, 4096, 4096, 16, 16.0, "bf16", "q4"),
+        Workload("llama3_8b_gate_up_q4", 8192, 4096, 14336, 16, 32.0, "bf16", "q4"),
     ]
 }
 

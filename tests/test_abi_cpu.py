@@ -151,6 +151,26 @@ def test_swiglu_sizes_and_rejects():
     assert L.lora_swiglu_bwd(*bwd) == _lib.LORA_ERR_WORKSPACE
 
 
+def test_q4_rejects():
+    fake = ctypes.c_void_p(4096)
+    M = 300
+    fwd = lambda d_in=256, d_out=128, r=16, codes=fake, ws=(fake, 1 << 40): (
+        fake, codes, fake, fake, fake, 32.0, r, M, d_in, d_out, fake, fake) + ws + (None,)
+    assert L.lora_q4_fwd(*fwd(d_in=96)) == _lib.LORA_ERR_UNSUPPORTED
+    assert L.lora_q4_fwd(*fwd(d_out=12)) == _lib.LORA_ERR_UNSUPPORTED
+    assert L.lora_q4_fwd(*fwd(r=0)) == _lib.LORA_ERR_INVALID_ARG
+    assert L.lora_q4_fwd(*fwd(codes=None)) == _lib.LORA_ERR_INVALID_ARG
+    assert L.lora_q4_fwd(*fwd(r=12, ws=(None, 0))) == _lib.LORA_ERR_WORKSPACE  # pad of B
+    bwd = lambda d_in=256, saved=fake, ws=(fake, 1 << 40): (
+        fake, fake, fake, fake, fake, fake, saved, 32.0, 16, M, d_in, 128, fake, fake,
+        fake) + ws + (None,)
+    assert L.lora_q4_bwd(*bwd(d_in=100)) == _lib.LORA_ERR_UNSUPPORTED
+    assert L.lora_q4_bwd(*bwd(ws=(None, 0))) == _lib.LORA_ERR_WORKSPACE
+    assert L.lora_q4_quantize_w(fake, 128, 96, fake, fake, None) == _lib.LORA_ERR_UNSUPPORTED
+    assert L.lora_q4_quantize_w(fake, 128, 128, None, fake, None) == _lib.LORA_ERR_INVALID_ARG
+    assert L.lora_q4_dequantize_w(fake, fake, 128, 32, fake, None) == _lib.LORA_ERR_UNSUPPORTED
+
+
 def test_withhold_hook_arguments():
     assert L.lora_debug_withhold_arrive(-1) == _lib.LORA_ERR_INVALID_ARG
     assert L.lora_debug_withhold_arrive(0) == _lib.LORA_OK
