@@ -44,7 +44,11 @@ constexpr int CLUSTER = 2;                   // the CTA pair
 constexpr uint16_t PAIR_MASK = 0x3;
 constexpr uint32_t A_BYTES = BM * BK * 2;    // 16 KB: this CTA's 128 rows of A
 constexpr int NUM_THREADS = 192;             // producer warp, MMA warp, 4 epilogue warps
-constexpr int Q4_THREADS = 320;              // ... and 4 warps dequantising 4-bit W
+// 4-bit W: warps expanding codes to bf16, one group of them per ring stage
+// (a stage is 128 lines of 64 weights)
+constexpr int DQ_GROUP_WARPS = 2;
+constexpr int DQ_GROUP_THREADS = 32 * DQ_GROUP_WARPS;
+static_assert(128 % DQ_GROUP_THREADS == 0, "dequantising split");
 // 4-bit W stage: 128 B-tile rows of 64 codes (32 bytes) or 64 K-rows of 128
 // codes, then 128 bf16 scales
 constexpr uint32_t RAW_CODE_BYTES = 4096, RAW_BYTES = RAW_CODE_BYTES + 256;
@@ -64,6 +68,13 @@ struct Geo {
   static constexpr int STAGES = STAGES_RAW > 8 ? 8 : STAGES_RAW;
   static constexpr uint32_t TMEM_COLS = 2 * BN;  // two accumulators
 };
+
+// One dequantising group per stage of the 4-bit ring, so that each group
+// waits on every phase of its stage's rawfull barrier in order (a parity
+// wait never runs a phase ahead).
+constexpr int DQ_GROUPS = Geo<256, true>::STAGES;
+constexpr int Q4_THREADS = NUM_THREADS + DQ_GROUPS * DQ_GROUP_THREADS;
+static_assert(DQ_GROUPS <= 15 && Q4_THREADS <= 1024, "named barriers 1..15");
 
 template <int STAGES>
 struct __align__(8) MainTail {
@@ -251,10 +262,10 @@ __global__ void __launch_bounds__(Q4 ? Q4_THREADS : NUM_THREADS, 1)
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < STAGES; ++s) {
-      // the even CTA's expect_tx arrival, or (4-bit W) one arrival from each
-      // dequantising warp of both CTAs, matched on extension stages by the
+      // the even CTA's expect_tx arrival, or (4-bit W) one arrival from the
+      // dequantising group of each CTA, matched on extension stages by the
       // producers' arrivals
-      mbar_init(smem_u32(&tail->full[s]), Q4 ? 8 : 1);
+      mbar_init(smem_u32(&tail->full[s]), Q4 ? 2 : 1);
       mbar_init(smem_u32(&tail->rawfull[s]), 1);
       mbar_init(smem_u32(&tail->empty[s]), 1);  // the even CTA's multicast commit
     }
@@ -271,6 +282,8 @@ __global__ void __launch_bounds__(Q4 ? Q4_THREADS : NUM_THREADS, 1)
     tma_prefetch(&tmB);
     tma_prefetch(&tmA2);
     tma_prefetch(&tmB2);
+    if (GATED || DUAL_B || Q4) tma_prefetch(&tmB3);
+    if (GATED) tma_prefetch(&tmB4);
   }
   // Both CTAs' barriers exist before either signals the other's.
   cluster_sync();
@@ -345,14 +358,12 @@ __global__ void __launch_bounds__(Q4 ? Q4_THREADS : NUM_THREADS, 1)
               }
               continue;
             }
-            // extension stage: pair loads, plus the arrivals that stand in for
-            // the four dequantising warps of each CTA
-            if (leader) {
+            // extension stage: pair loads; the odd CTA's arrival stands in
+            // for its dequantising group's
+            if (leader)
               mbar_expect_tx(full_local, PAIR_TX);
-              mbar_arrive_n(full_local, 3);
-            } else {
-              mbar_arrive_cluster_n(full, 4);
-            }
+            else
+              mbar_arrive_cluster(full);
             last_ext |= 1u << stage;
           } else {
             if (leader) mbar_expect_tx(full_local, PAIR_TX);
@@ -504,68 +515,67 @@ __global__ void __launch_bounds__(Q4 ? Q4_THREADS : NUM_THREADS, 1)
     }
   } else if (Q4 && warp >= 6) {
     // ------------------------------------------------------ 4-bit W dequantisation (both CTAs)
-    // On each main-segment stage: this CTA's codes and bf16 group scales ->
-    // its bf16 half of the B tile, in the layout the TMA writes for bf16 W
-    // (128-byte swizzle; K-major forward, two MN-major atoms backward); then
-    // one arrival per warp on the even CTA's full barrier.  The stage's
-    // previous B tile is free: its rawfull phase was armed only after the
-    // pair MMAs released the stage.
-    const int dw = warp - 6;
+    // Group g of warps owns ring stage g, so that several stages are
+    // expanded at once.  On each main-segment use of its stage, a group
+    // turns the codes and bf16 group scales into this CTA's bf16 half of the B tile,
+    // in the layout the TMA writes for bf16 W (128-byte swizzle; K-major
+    // forward, two MN-major atoms backward), meets on a named barrier, and
+    // one of its threads arrives on the even CTA's full barrier.  The
+    // stage's previous B tile is free: its rawfull phase was armed only
+    // after the pair MMAs released the stage.
+    const int grp = (warp - 6) / DQ_GROUP_WARPS;
+    const int gt = threadIdx.x - (6 + grp * DQ_GROUP_WARPS) * 32;  // 0 .. DQ_GROUP_THREADS - 1
+    const uint32_t bar_id = 1 + grp;  // named barrier of the group (0 is __syncthreads)
     const uint8_t *raw_base = smem_raw + (sRaw - raw);
     uint8_t *b_base = smem_raw + (sB - raw);
+    static_assert(!Q4 || DQ_GROUPS == STAGES, "one dequantising group per stage");
     int stage = 0;
-    uint32_t rbits = 0;  // per stage: parity of its next rawfull phase
+    uint32_t rpar = 0;  // parity of the next rawfull phase of this group's stage
     bool ok = true;
     for (int item = pair_id; item < num_items && ok; item += num_pairs) {
       int tile, kb_lo, kb_hi, chunk, rel;
       item_range(item, split_first, split_k, split_rem, kb_total, tile, kb_lo, kb_hi, chunk, rel);
       for (int kb = kb_lo; kb < kb_hi; ++kb) {
-        if (kb < kb_main) {
-          const bool got = mbar_wait(smem_u32(&tail->rawfull[stage]), (rbits >> stage) & 1u,
-                                     abort_flag, dev_status);
-          if (!__all_sync(0xffffffffu, got)) {
+        if (kb < kb_main && stage == grp) {
+          const bool got = mbar_wait(smem_u32(&tail->rawfull[stage]), rpar, abort_flag,
+                                     dev_status);
+          if (named_bar_red_or(bar_id, DQ_GROUP_THREADS, !got)) {  // the group agrees
             ok = false;
             break;
           }
-          rbits ^= 1u << stage;
           const uint8_t *rw = raw_base + stage * RAW_BYTES;
           uint8_t *bt = b_base + stage * B_BYTES;
-          // this thread's 64 codes (32 bytes), their scale, and where its
-          // eight 16-byte chunks go (chunk i at slot i ^ (line & 7))
-          const uint8_t *src;
-          uint16_t sbits;
-          uint8_t *dst;
-          int sw;
-          if constexpr (B_MN) {  // K-row k of one 64-column half a
-            const int k = dw * 16 + (lane & 15), a = lane >> 4;
-            src = rw + k * 64 + a * 32;
-            sbits = *reinterpret_cast<const uint16_t *>(rw + RAW_CODE_BYTES + (a * 64 + k) * 2);
-            dst = bt + a * 8192 + (k >> 3) * 1024 + (k & 7) * 128;
-            sw = k & 7;
-          } else {  // B-tile row n (one output column)
-            const int n = dw * 32 + lane;
-            src = rw + n * 32;
-            sbits = *reinterpret_cast<const uint16_t *>(rw + RAW_CODE_BYTES + n * 2);
-            dst = bt + (n >> 3) * 1024 + (n & 7) * 128;
-            sw = n & 7;
-          }
-          const uint4 c0 = *reinterpret_cast<const uint4 *>(src);
-          const uint4 c1 = *reinterpret_cast<const uint4 *>(src + 16);
-          const uint32_t s2 = static_cast<uint32_t>(sbits) * 0x10001u;
-          const __nv_bfloat162 scale2 = *reinterpret_cast<const __nv_bfloat162 *>(&s2);
-          const uint32_t w[8] = {c0.x, c0.y, c0.z, c0.w, c1.x, c1.y, c1.z, c1.w};
+          // 128 lines of 128 bytes (a K-major row n, or K-row k of MN-major
+          // atom a, line a * 64 + k): each line's 64 codes (32 bytes) and
+          // scale; chunk c of a line sits at slot c ^ (line & 7)
 #pragma unroll
-          for (int i = 0; i < 8; ++i)
-            *reinterpret_cast<uint4 *>(dst + ((i ^ sw) << 4)) = dequant8(w[i], scale2);
-          fence_proxy_async_smem();  // visible to the tensor cores
-          __syncwarp();
-          if (lane == 0) {
+          for (int li = 0; li < 128 / DQ_GROUP_THREADS; ++li) {
+            const int line = gt + li * DQ_GROUP_THREADS;
+            const uint8_t *src =
+                B_MN ? rw + (line & 63) * 64 + (line >> 6) * 32 : rw + line * 32;
+            const uint4 c0 = *reinterpret_cast<const uint4 *>(src);
+            const uint4 c1 = *reinterpret_cast<const uint4 *>(src + 16);
+            const uint32_t sb =
+                *reinterpret_cast<const uint16_t *>(rw + RAW_CODE_BYTES + line * 2);
+            const uint32_t s2 = sb * 0x10001u;
+            const __nv_bfloat162 scale2 = *reinterpret_cast<const __nv_bfloat162 *>(&s2);
+            uint8_t *dst = bt + (line >> 3) * 1024 + (line & 7) * 128;
+            const int sw = line & 7;
+            const uint32_t w[8] = {c0.x, c0.y, c0.z, c0.w, c1.x, c1.y, c1.z, c1.w};
+#pragma unroll
+            for (int i = 0; i < 8; ++i)
+              *reinterpret_cast<uint4 *>(dst + ((i ^ sw) << 4)) = dequant8(w[i], scale2);
+          }
+          fence_proxy_async_smem();  // this thread's stores, visible to the tensor cores
+          named_bar_sync(bar_id, DQ_GROUP_THREADS);
+          if (gt == 0) {
             const uint32_t fl = smem_u32(&tail->full[stage]);
             if (leader)
               mbar_arrive(fl);
             else
               mbar_arrive_cluster(dsmem_map(fl, 0));
           }
+          rpar ^= 1u;
         }
         if (++stage == STAGES) stage = 0;
       }
