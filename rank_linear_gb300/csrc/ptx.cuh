@@ -51,10 +51,6 @@ __device__ __forceinline__ void mbar_expect_tx(uint32_t bar, uint32_t bytes) {
 __device__ __forceinline__ void mbar_arrive(uint32_t bar) {
   asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(bar) : "memory");
 }
-// `count` arrivals at once.
-__device__ __forceinline__ void mbar_arrive_n(uint32_t bar, uint32_t count) {
-  asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0], %1;" ::"r"(bar), "r"(count) : "memory");
-}
 // One probe of the phase with the given parity (true = that phase completed).
 // kCluster: acquire at cluster scope, for a phase completed by arrivals that
 // publish another CTA's shared-memory writes.
@@ -163,6 +159,20 @@ __device__ __forceinline__ void bulk_load(uint32_t dst, const void *src, uint32_
   asm volatile(
       "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(dst),
       "l"(reinterpret_cast<uint64_t>(src)), "r"(bytes), "r"(bar)
+      : "memory");
+}
+// Bulk copy of `bytes` (a multiple of 16) from this CTA's shared memory to
+// shared memory of a CTA of the cluster (dst and bar: shared::cluster
+// addresses in that CTA), counted on its mbarrier `bar`.  Generic-proxy
+// stores to this CTA's shared memory that are ordered before the copy by
+// fence.proxy.async (and a barrier, for other threads' stores) are visible
+// to the async proxy by then.
+__device__ __forceinline__ void bulk_copy_s2c(uint32_t dst, uint32_t src, uint32_t bytes,
+                                              uint32_t bar) {
+  asm volatile(
+      "cp.async.bulk.shared::cluster.shared::cta.mbarrier::complete_tx::bytes [%0], [%1], %2, "
+      "[%3];" ::"r"(dst),
+      "r"(src), "r"(bytes), "r"(bar)
       : "memory");
 }
 // Orders this thread's earlier generic-proxy accesses of global memory
@@ -289,12 +299,6 @@ __device__ __forceinline__ void tc_commit_pair(uint32_t bar) {
 // Arrive on an mbarrier given by a shared::cluster address (own or peer CTA).
 __device__ __forceinline__ void mbar_arrive_cluster(uint32_t cluster_bar) {
   asm volatile("mbarrier.arrive.release.cluster.shared::cluster.b64 _, [%0];" ::"r"(cluster_bar)
-               : "memory");
-}
-__device__ __forceinline__ void mbar_arrive_cluster_n(uint32_t cluster_bar, uint32_t count) {
-  asm volatile("mbarrier.arrive.release.cluster.shared::cluster.b64 _, [%0], %1;" ::"r"(
-                   cluster_bar),
-               "r"(count)
                : "memory");
 }
 

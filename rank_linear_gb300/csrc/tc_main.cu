@@ -77,7 +77,7 @@ constexpr int Q4_THREADS = NUM_THREADS + DQ_GROUPS * DQ_GROUP_THREADS;
 static_assert(DQ_GROUPS <= 15 && Q4_THREADS <= 1024, "named barriers 1..15");
 
 template <int STAGES>
-struct __align__(8) MainTail {
+struct __align__(16) MainTail {
   uint64_t full[STAGES];    // even CTA: both CTAs' loads of a stage landed
   uint64_t rawfull[STAGES]; // each CTA (4-bit W): A and the raw codes landed
   uint64_t empty[STAGES];   // each CTA: the pair MMAs finished reading a stage
@@ -89,6 +89,8 @@ struct __align__(8) MainTail {
   uint32_t tmem_base;
   int abort_flag;
   int split_last;
+  // 4-bit W: target of the odd CTA's 16-byte "stage expanded" copies
+  alignas(16) uint8_t sig[16];
 };
 
 // Epilogue staging: per epilogue warp, one 32 x 32 bf16 chunk with rows
@@ -262,10 +264,10 @@ __global__ void __launch_bounds__(Q4 ? Q4_THREADS : NUM_THREADS, 1)
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < STAGES; ++s) {
-      // the even CTA's expect_tx arrival, or (4-bit W) one arrival from the
-      // dequantising group of each CTA, matched on extension stages by the
-      // producers' arrivals
-      mbar_init(smem_u32(&tail->full[s]), Q4 ? 2 : 1);
+      // the even CTA's expect_tx arrival: its producer's, or (4-bit W, main
+      // segment) its dequantising group's, which expects the odd CTA's
+      // 16-byte signal copy
+      mbar_init(smem_u32(&tail->full[s]), 1);
       mbar_init(smem_u32(&tail->rawfull[s]), 1);
       mbar_init(smem_u32(&tail->empty[s]), 1);  // the even CTA's multicast commit
     }
@@ -358,12 +360,8 @@ __global__ void __launch_bounds__(Q4 ? Q4_THREADS : NUM_THREADS, 1)
               }
               continue;
             }
-            // extension stage: pair loads; the odd CTA's arrival stands in
-            // for its dequantising group's
-            if (leader)
-              mbar_expect_tx(full_local, PAIR_TX);
-            else
-              mbar_arrive_cluster(full);
+            // extension stage: the pair loads as in the bf16 layer
+            if (leader) mbar_expect_tx(full_local, PAIR_TX);
             last_ext |= 1u << stage;
           } else {
             if (leader) mbar_expect_tx(full_local, PAIR_TX);
@@ -519,10 +517,14 @@ __global__ void __launch_bounds__(Q4 ? Q4_THREADS : NUM_THREADS, 1)
     // expanded at once.  On each main-segment use of its stage, a group
     // turns the codes and bf16 group scales into this CTA's bf16 half of the B tile,
     // in the layout the TMA writes for bf16 W (128-byte swizzle; K-major
-    // forward, two MN-major atoms backward), meets on a named barrier, and
-    // one of its threads arrives on the even CTA's full barrier.  The
-    // stage's previous B tile is free: its rawfull phase was armed only
-    // after the pair MMAs released the stage.
+    // forward, two MN-major atoms backward) and meets on a named barrier;
+    // then one of its threads signals the even CTA's full barrier: there an
+    // arrival expecting 16 bytes, here a 16-byte bulk copy into the even
+    // CTA that completes them (a copy issued after the group's proxy fences
+    // and barrier, so the tensor cores, reading through the async proxy
+    // once the phase completes, see the expanded tile).  The stage's
+    // previous B tile is free: its rawfull phase was armed only after the
+    // pair MMAs released the stage.
     const int grp = (warp - 6) / DQ_GROUP_WARPS;
     const int gt = threadIdx.x - (6 + grp * DQ_GROUP_WARPS) * 32;  // 0 .. DQ_GROUP_THREADS - 1
     const uint32_t bar_id = 1 + grp;  // named barrier of the group (0 is __syncthreads)
@@ -570,10 +572,11 @@ __global__ void __launch_bounds__(Q4 ? Q4_THREADS : NUM_THREADS, 1)
           named_bar_sync(bar_id, DQ_GROUP_THREADS);
           if (gt == 0) {
             const uint32_t fl = smem_u32(&tail->full[stage]);
+            const uint32_t sg = smem_u32(tail->sig);
             if (leader)
-              mbar_arrive(fl);
+              mbar_expect_tx(fl, 16);
             else
-              mbar_arrive_cluster(dsmem_map(fl, 0));
+              bulk_copy_s2c(dsmem_map(sg, 0), sg, 16, dsmem_map(fl, 0));
           }
           rpar ^= 1u;
         }
@@ -735,6 +738,15 @@ __global__ void __launch_bounds__(Q4 ? Q4_THREADS : NUM_THREADS, 1)
   // collective deallocation; neither leaves while the other may still
   // touch its shared memory.
   __syncthreads();
+  if (Q4 && !leader && threadIdx.x == 0 && tail->abort_flag) {
+    // Aborting: a signal copy this CTA sent may still be on its way into
+    // the even CTA, which leaves right after the cluster barrier.  (Without
+    // an abort, the pair MMAs consumed every signal before the end.)  A copy
+    // lands within microseconds: wait 100 us.
+    const uint64_t t0 = globaltimer_ns();
+    while (globaltimer_ns() - t0 < 100000ull) {
+    }
+  }
   tc_fence_before();
   cluster_sync();
   if (warp == 1) {
