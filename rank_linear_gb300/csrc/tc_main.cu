@@ -65,7 +65,9 @@ struct Geo {
   // bytes a stage's pair-TMA loads bring to the even CTA's barrier
   static constexpr uint32_t PAIR_TX = CLUSTER * (A_BYTES + B_BYTES);
   static constexpr int STAGES_RAW = static_cast<int>(kStageBudget / STAGE_BYTES);
-  static constexpr int STAGES = STAGES_RAW > 8 ? 8 : STAGES_RAW;
+  // 4-bit W: six stages (its chain from load to MMA is longer), in the room
+  // the shared-memory limit leaves
+  static constexpr int STAGES = Q4 ? 6 : (STAGES_RAW > 8 ? 8 : STAGES_RAW);
   static constexpr uint32_t TMEM_COLS = 2 * BN;  // two accumulators
 };
 
@@ -93,9 +95,11 @@ struct __align__(16) MainTail {
   alignas(16) uint8_t sig[16];
 };
 
-// Epilogue staging: per epilogue warp, one 32 x 32 bf16 chunk with rows
-// padded to 80 bytes (conflict-free 16-byte writes).
-constexpr uint32_t EPI_PITCH = 80;
+// Epilogue staging: per epilogue warp, one 32 x 32 bf16 chunk, 64 bytes a
+// row; 16-byte segment i of row r sits at slot i ^ ((r >> 1) & 3), so that
+// both the row-wise writes and the segment-wise reads of eight lanes cover
+// all 32 banks.
+constexpr uint32_t EPI_PITCH = 64;
 constexpr uint32_t EPI_WARP_BYTES = 32 * EPI_PITCH;
 constexpr uint32_t EPI_BYTES = 4 * EPI_WARP_BYTES;
 
@@ -104,6 +108,8 @@ constexpr size_t smem_bytes() {
   return 1024 + size_t(Geo<BN, Q4>::STAGES) * Geo<BN, Q4>::STAGE_BYTES + EPI_BYTES +
          sizeof(MainTail<Geo<BN, Q4>::STAGES>);
 }
+static_assert(smem_bytes<256, true>() <= 227 * 1024 && smem_bytes<256>() <= 227 * 1024,
+              "shared memory per CTA");
 
 // Work item -> tile and K-block range.  Items below split_first are whole
 // tiles; the rest are range `chunk` of split tile `rel` (tile split_first+rel).
@@ -172,15 +178,18 @@ __device__ __forceinline__ void store_chunk(const uint32_t (&pk)[16], uint8_t *s
                                            __nv_bfloat16 *out, int64_t ldo, int row0, int col0,
                                            int M, int N) {
   uint4 *my = reinterpret_cast<uint4 *>(stage + lane * EPI_PITCH);
+  const int lsw = (lane >> 1) & 3;
 #pragma unroll
-  for (int i = 0; i < 4; ++i) my[i] = make_uint4(pk[4 * i], pk[4 * i + 1], pk[4 * i + 2], pk[4 * i + 3]);
+  for (int i = 0; i < 4; ++i)
+    my[i ^ lsw] = make_uint4(pk[4 * i], pk[4 * i + 1], pk[4 * i + 2], pk[4 * i + 3]);
   __syncwarp();
   const int seg = lane & 3;  // 16-byte segment (8 columns) of a row
   const int col = col0 + seg * 8;
 #pragma unroll
   for (int j = 0; j < 4; ++j) {
     const int r = 8 * j + (lane >> 2);
-    const uint4 v = *reinterpret_cast<const uint4 *>(stage + r * EPI_PITCH + seg * 16);
+    const uint4 v =
+        *reinterpret_cast<const uint4 *>(stage + r * EPI_PITCH + ((seg ^ ((r >> 1) & 3)) * 16));
     const int row = row0 + r;
     if (row < M && col < N)  // N is a multiple of 8: a segment is all in or all out
       *reinterpret_cast<uint4 *>(out + static_cast<int64_t>(row) * ldo + col) = v;
@@ -311,7 +320,6 @@ __global__ void __launch_bounds__(Q4 ? Q4_THREADS : NUM_THREADS, 1)
     if (lane == 0) {
       uint32_t issued[STAGES];
       uint32_t rissued[STAGES];  // 4-bit W: main-segment loads on rawfull[s]
-      uint32_t last_ext = 0;     // 4-bit W: stages whose last load was an extension one
       for (int s = 0; s < STAGES; ++s) issued[s] = rissued[s] = 0;
       int stage = 0;
       uint32_t phase = 0;
@@ -336,14 +344,14 @@ __global__ void __launch_bounds__(Q4 ? Q4_THREADS : NUM_THREADS, 1)
           const bool ext = kb >= kb_main;
           if constexpr (Q4) {
             if (!ext) {
-              // A and this CTA's 4-bit codes and scales land on its own
-              // rawfull barrier; its dequantising warps turn the codes into
-              // the bf16 B tile and arrive on the even CTA's full barrier
+              // this CTA's 4-bit codes and scales land on its own rawfull
+              // barrier (issued first: the dequantising group waits for
+              // them); the group turns them into the bf16 B tile and
+              // signals the even CTA's full barrier
               const uint32_t rf = smem_u32(&tail->rawfull[stage]);
               const int k0 = kb * BK;
               const uint32_t rw = sRaw + stage * RAW_BYTES;
-              mbar_expect_tx(rf, A_BYTES + RAW_BYTES);
-              tma_load_2d(sA + stage * A_BYTES, &tmA, rf, k0, m0);
+              mbar_expect_tx(rf, RAW_BYTES);
               if (B_MN) {  // 64 K-rows x 128 codes (64 bytes); scales of 2 column groups
                 tma_load_2d(rw, &tmB, rf, n0 / 2, k0);
                 tma_load_2d(rw + RAW_CODE_BYTES, &tmB3, rf, k0, n0 / 64);
@@ -351,9 +359,11 @@ __global__ void __launch_bounds__(Q4 ? Q4_THREADS : NUM_THREADS, 1)
                 tma_load_2d(rw, &tmB, rf, k0 / 2, n0);
                 tma_load_2d(rw + RAW_CODE_BYTES, &tmB3, rf, n0, k0 / 64);
               }
+              // A as in the bf16 layer, onto the even CTA's full barrier
+              // (its bytes are expected by the even CTA's dequantising group)
+              tma_load_2d_pair(sA + stage * A_BYTES, &tmA, full, k0, m0);
               issued[stage] += 1;
               rissued[stage] += 1;
-              last_ext &= ~(1u << stage);
               if (++stage == STAGES) {
                 stage = 0;
                 phase ^= 1u;
@@ -362,7 +372,6 @@ __global__ void __launch_bounds__(Q4 ? Q4_THREADS : NUM_THREADS, 1)
             }
             // extension stage: the pair loads as in the bf16 layer
             if (leader) mbar_expect_tx(full_local, PAIR_TX);
-            last_ext |= 1u << stage;
           } else {
             if (leader) mbar_expect_tx(full_local, PAIR_TX);
           }
@@ -416,15 +425,19 @@ __global__ void __launch_bounds__(Q4 ? Q4_THREADS : NUM_THREADS, 1)
           }
       }
       if (!clean) {  // aborting: let the pair's copies in flight land before exiting
-        if constexpr (Q4) {  // this CTA's own main-segment copies
+        if constexpr (Q4) {
+          // this CTA's own codes; then, for the pair loads and the signal
+          // copies that complete on the even CTA's full barriers (phases
+          // that need a dequantising group's arrival as well), 100 us
           for (int s = 0; s < STAGES; ++s)
             if (rissued[s]) mbar_wait_drain(smem_u32(&tail->rawfull[s]), (rissued[s] - 1u) & 1u);
-        }
-        if (leader) {
+          const uint64_t t0 = globaltimer_ns();
+          while (globaltimer_ns() - t0 < 100000ull) {
+          }
+        } else if (leader) {
           // a phase the even CTA armed completes when both CTAs' bytes landed
           for (int s = 0; s < STAGES; ++s)
-            if (issued[s] && (!Q4 || (last_ext >> s) & 1u))
-              mbar_wait_drain(smem_u32(&tail->full[s]), (issued[s] - 1u) & 1u);
+            if (issued[s]) mbar_wait_drain(smem_u32(&tail->full[s]), (issued[s] - 1u) & 1u);
         } else {
           // The odd CTA's copies complete on the even CTA's barriers, which it
           // cannot poll; one it issued for a phase the even CTA never armed
@@ -573,8 +586,8 @@ __global__ void __launch_bounds__(Q4 ? Q4_THREADS : NUM_THREADS, 1)
           if (gt == 0) {
             const uint32_t fl = smem_u32(&tail->full[stage]);
             const uint32_t sg = smem_u32(tail->sig);
-            if (leader)
-              mbar_expect_tx(fl, 16);
+            if (leader)  // both CTAs' A tiles and the odd CTA's signal
+              mbar_expect_tx(fl, CLUSTER * A_BYTES + 16);
             else
               bulk_copy_s2c(dsmem_map(sg, 0), sg, 16, dsmem_map(fl, 0));
           }
