@@ -568,18 +568,24 @@ __global__ void __launch_bounds__(Q4 ? Q4_THREADS : NUM_THREADS, 1)
             const int line = gt + li * DQ_GROUP_THREADS;
             const uint8_t *src =
                 B_MN ? rw + (line & 63) * 64 + (line >> 6) * 32 : rw + line * 32;
-            const uint4 c0 = *reinterpret_cast<const uint4 *>(src);
-            const uint4 c1 = *reinterpret_cast<const uint4 *>(src + 16);
+            // the 16-byte half read first alternates every 4 lines forward
+            // (every 2 backward), so a quarter-warp's loads spread over the
+            // banks; h0 holds chunks 4 hx .. 4 hx + 3
+            const int hx = B_MN ? (line >> 1) & 1 : (line >> 2) & 1;
+            const uint4 h0 = *reinterpret_cast<const uint4 *>(src + hx * 16);
+            const uint4 h1 = *reinterpret_cast<const uint4 *>(src + (hx ^ 1) * 16);
             const uint32_t sb =
                 *reinterpret_cast<const uint16_t *>(rw + RAW_CODE_BYTES + line * 2);
             const uint32_t s2 = sb * 0x10001u;
             const __nv_bfloat162 scale2 = *reinterpret_cast<const __nv_bfloat162 *>(&s2);
             uint8_t *dst = bt + (line >> 3) * 1024 + (line & 7) * 128;
             const int sw = line & 7;
-            const uint32_t w[8] = {c0.x, c0.y, c0.z, c0.w, c1.x, c1.y, c1.z, c1.w};
+            const uint32_t w[8] = {h0.x, h0.y, h0.z, h0.w, h1.x, h1.y, h1.z, h1.w};
 #pragma unroll
-            for (int i = 0; i < 8; ++i)
-              *reinterpret_cast<uint4 *>(dst + ((i ^ sw) << 4)) = dequant8(w[i], scale2);
+            for (int i = 0; i < 8; ++i) {
+              const int c = i ^ (hx << 2);  // chunk of the line
+              *reinterpret_cast<uint4 *>(dst + ((c ^ sw) << 4)) = dequant8(w[i], scale2);
+            }
           }
           fence_proxy_async_smem();  // this thread's stores, visible to the tensor cores
           named_bar_sync(bar_id, DQ_GROUP_THREADS);
