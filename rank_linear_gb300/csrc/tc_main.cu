@@ -570,10 +570,13 @@ __global__ void __launch_bounds__(Q4 ? Q4_THREADS : NUM_THREADS, 1)
                 B_MN ? rw + (line & 63) * 64 + (line >> 6) * 32 : rw + line * 32;
             // the 16-byte half read first alternates every 4 lines forward
             // (every 2 backward), so a quarter-warp's loads spread over the
-            // banks; h0 holds chunks 4 hx .. 4 hx + 3
+            // banks; the halves are then put back in order, so that the
+            // stores below (chunk c at slot c ^ (line & 7)) stay
+            // conflict-free
             const int hx = B_MN ? (line >> 1) & 1 : (line >> 2) & 1;
-            const uint4 h0 = *reinterpret_cast<const uint4 *>(src + hx * 16);
-            const uint4 h1 = *reinterpret_cast<const uint4 *>(src + (hx ^ 1) * 16);
+            const uint4 ha = *reinterpret_cast<const uint4 *>(src + hx * 16);
+            const uint4 hb = *reinterpret_cast<const uint4 *>(src + (hx ^ 1) * 16);
+            const uint4 h0 = hx ? hb : ha, h1 = hx ? ha : hb;
             const uint32_t sb =
                 *reinterpret_cast<const uint16_t *>(rw + RAW_CODE_BYTES + line * 2);
             const uint32_t s2 = sb * 0x10001u;
@@ -582,10 +585,8 @@ __global__ void __launch_bounds__(Q4 ? Q4_THREADS : NUM_THREADS, 1)
             const int sw = line & 7;
             const uint32_t w[8] = {h0.x, h0.y, h0.z, h0.w, h1.x, h1.y, h1.z, h1.w};
 #pragma unroll
-            for (int i = 0; i < 8; ++i) {
-              const int c = i ^ (hx << 2);  // chunk of the line
-              *reinterpret_cast<uint4 *>(dst + ((c ^ sw) << 4)) = dequant8(w[i], scale2);
-            }
+            for (int i = 0; i < 8; ++i)
+              *reinterpret_cast<uint4 *>(dst + ((i ^ sw) << 4)) = dequant8(w[i], scale2);
           }
           fence_proxy_async_smem();  // this thread's stores, visible to the tensor cores
           named_bar_sync(bar_id, DQ_GROUP_THREADS);
