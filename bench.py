@@ -45,17 +45,20 @@ def step_flops(M, d_in, d_out, r):
     return 4 * M * d_in * d_out + 6 * M * r * (d_in + d_out)
 
 
-def kernel_work(kind, M, d_in, d_out, r):
-    """Algorithmic (flops, bytes) of one launch of each kernel kind (bf16)."""
+def kernel_work(kind, M, d_in, d_out, r, w_bytes=None):
+    """Algorithmic (flops, bytes) of one launch of each kernel kind (bf16).
+    w_bytes: bytes of the frozen W as stored (default bf16; the 4-bit layer
+    passes its codes plus scales)."""
     e = 2
+    wb = e * d_out * d_in if w_bytes is None else w_bytes
     return {
         "prep": (0, e * 2 * d_out * r),
         "down_fwd": (2 * M * d_in * r, e * (M * d_in + r * d_in + M * r)),
         "main_fwd": (2 * M * d_out * (d_in + r),
-                     e * (M * d_in + d_out * d_in + M * r + d_out * r + M * d_out)),
+                     e * (M * d_in + M * r + d_out * r + M * d_out) + wb),
         "down_bwd": (2 * M * d_out * r, e * (M * d_out + r * d_out + M * r)),
         "main_bwd": (2 * M * d_in * (d_out + r),
-                     e * (M * d_out + d_out * d_in + M * r + r * d_in + M * d_in)),
+                     e * (M * d_out + M * r + r * d_in + M * d_in) + wb),
         "grad_a": (2 * M * d_in * r, e * (M * d_in + M * r + r * d_in)),
         "grad_b": (2 * M * d_out * r, e * (M * d_out + M * r + d_out * r)),
         # e4m3 quantisation of X's rows (bf16 in, bytes and scales out)
@@ -448,7 +451,11 @@ def run_ours(args, w):
     dom = max(per_kind, key=lambda k: sum(per_kind[k]))
 
     peaks = load_peaks()
-    fl, by = (kernel_work_swiglu if swiglu else kernel_work)(dom, M, d_in, d_out, r)
+    if swiglu:
+        fl, by = kernel_work_swiglu(dom, M, d_in, d_out, r)
+    else:  # 4-bit W: codes (half a byte each) and a bf16 scale per 64 weights
+        fl, by = kernel_work(dom, M, d_in, d_out, r,
+                             w_bytes=d_out * d_in // 2 + d_out * d_in // 32 if q4 else None)
     avg_s = sum(per_kind[dom]) / len(per_kind[dom]) / 1e3
     peak_note = " (burst)"
     if BOUND[dom] == "tensor" and fp8:  # e4m3 products: 2 x the bf16 rate (nominal ratio)
