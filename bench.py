@@ -299,7 +299,7 @@ def run_reference(args, w):
         "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
         "ms_per_step": 1e3 * sec / args.steps, "higher_is_better": True, "scaling": "weak",
         "vs_baseline": None, "dtype": "f64", "data": "synthetic",
-        "config": {"workload": w.name, "M": w.M, "d_in": w.d_in, "d_out": w.d_out, "r": w.r,
+        "config": {"workload": w.name, "layer": w.layer, "M": w.M, "d_in": w.d_in, "d_out": w.d_out, "r": w.r,
                    "alpha": w.alpha, "sample_tokens": tokens},
         "cpu_baseline": {"value": value, "unit": "TFLOP/s", "cores": oracle.threads(),
                          "kind": "oracle",
