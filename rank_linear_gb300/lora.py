@@ -409,3 +409,66 @@ def q4_backward(dY, X, qw: Q4Weight, A, B, alpha: float, saved=None, *, need_dX=
                        workspace.numel(), _stream_ptr(stream))
     _lib.check(st, "lora_q4_bwd")
     return (dX if need_dX else None), dA, dB
+
+
+# ---------------------------------------------------------------- autograd: quantised W
+
+class LoRAFP8Function(torch.autograd.Function):
+    """Autograd function of the layer with an fp8 frozen-W product."""
+
+    @staticmethod
+    def forward(ctx, X, Wq, WqT, w_scale, A, B, alpha):
+        shape = X.shape
+        X2 = X.reshape(-1, shape[-1]).contiguous()
+        A, B = A.contiguous(), B.contiguous()
+        qw = FP8Weight(Wq, WqT, w_scale)
+        Y, saved = fp8_forward(X2, qw, A, B, alpha)
+        ctx.save_for_backward(X2, Wq, WqT, w_scale, A, B, saved)
+        ctx.alpha = alpha
+        ctx.x_shape = shape
+        return Y.reshape(*shape[:-1], B.shape[0])
+
+    @staticmethod
+    def backward(ctx, dY):
+        X2, Wq, WqT, w_scale, A, B, saved = ctx.saved_tensors
+        dY2 = dY.reshape(-1, dY.shape[-1]).contiguous()
+        dX, dA, dB = fp8_backward(dY2, X2, FP8Weight(Wq, WqT, w_scale), A, B, ctx.alpha, saved,
+                                  need_dX=ctx.needs_input_grad[0])
+        if dX is not None:
+            dX = dX.reshape(ctx.x_shape)
+        return dX, None, None, None, dA, dB, None
+
+
+def lora_linear_fp8(X, qw: FP8Weight, A, B, alpha: float):
+    """Q(X) Q(W)^T + (alpha/r) (X A^T) B^T with gradients for X, A and B."""
+    return LoRAFP8Function.apply(X, qw.Wq, qw.WqT, qw.w_scale, A, B, alpha)
+
+
+class LoRAQ4Function(torch.autograd.Function):
+    """Autograd function of the layer over a 4-bit frozen W."""
+
+    @staticmethod
+    def forward(ctx, X, codes, scales, A, B, alpha):
+        shape = X.shape
+        X2 = X.reshape(-1, shape[-1]).contiguous()
+        A, B = A.contiguous(), B.contiguous()
+        Y, saved = q4_forward(X2, Q4Weight(codes, scales), A, B, alpha)
+        ctx.save_for_backward(X2, codes, scales, A, B, saved)
+        ctx.alpha = alpha
+        ctx.x_shape = shape
+        return Y.reshape(*shape[:-1], B.shape[0])
+
+    @staticmethod
+    def backward(ctx, dY):
+        X2, codes, scales, A, B, saved = ctx.saved_tensors
+        dY2 = dY.reshape(-1, dY.shape[-1]).contiguous()
+        dX, dA, dB = q4_backward(dY2, X2, Q4Weight(codes, scales), A, B, ctx.alpha, saved,
+                                 need_dX=ctx.needs_input_grad[0])
+        if dX is not None:
+            dX = dX.reshape(ctx.x_shape)
+        return dX, None, None, dA, dB, None
+
+
+def lora_linear_q4(X, qw: Q4Weight, A, B, alpha: float):
+    """X Wd^T + (alpha/r) (X A^T) B^T over the 4-bit W, with gradients for X, A and B."""
+    return LoRAQ4Function.apply(X, qw.codes, qw.scales, A, B, alpha)

@@ -131,3 +131,21 @@ def test_close_to_the_bf16_layer():
     Y16, _ = rl.forward(g["X"], g["W"], g["A"], g["B"], 32.0)
     torch.cuda.synchronize()
     assert rel_err(Y8, Y16.double().cpu().numpy()) < 0.1
+
+
+def test_autograd_matches_the_explicit_calls():
+    t = inputs(300, 256, 192, 16, seed=12)
+    g = {k: v.to(DEV) for k, v in t.items()}
+    qw = rl.quantize_w_fp8(g["W"])
+    X = g["X"].reshape(2, 150, 256).clone().requires_grad_(True)
+    A = g["A"].clone().requires_grad_(True)
+    B = g["B"].clone().requires_grad_(True)
+    Y = rl.lora_linear_fp8(X, qw, A, B, 32.0)
+    Y.backward(g["dY"].reshape(2, 150, 192))
+    Y2, saved = rl.fp8_forward(g["X"], qw, g["A"], g["B"], 32.0)
+    dX2, dA2, dB2 = rl.fp8_backward(g["dY"], g["X"], qw, g["A"], g["B"], 32.0, saved)
+    torch.cuda.synchronize()
+    assert Y.shape == (2, 150, 192)
+    assert torch.equal(Y.reshape(300, 192), Y2)
+    assert torch.equal(X.grad.reshape(300, 256), dX2)
+    assert torch.equal(A.grad, dA2) and torch.equal(B.grad, dB2)

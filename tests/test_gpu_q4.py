@@ -161,3 +161,21 @@ def test_rejects_d_in_not_a_multiple_of_64():
     W = torch.zeros(64, 96, dtype=torch.bfloat16, device=DEV)
     with pytest.raises(RuntimeError, match="multiple of 64"):
         rl.quantize_w_q4(W)
+
+
+def test_autograd_matches_the_explicit_calls():
+    t = inputs(300, 256, 192, 16, seed=12)
+    g = {k: v.to(DEV) for k, v in t.items()}
+    qw = rl.quantize_w_q4(g["W"])
+    X = g["X"].reshape(2, 150, 256).clone().requires_grad_(True)
+    A = g["A"].clone().requires_grad_(True)
+    B = g["B"].clone().requires_grad_(True)
+    Y = rl.lora_linear_q4(X, qw, A, B, 32.0)
+    Y.backward(g["dY"].reshape(2, 150, 192))
+    Y2, saved = rl.q4_forward(g["X"], qw, g["A"], g["B"], 32.0)
+    dX2, dA2, dB2 = rl.q4_backward(g["dY"], g["X"], qw, g["A"], g["B"], 32.0, saved)
+    torch.cuda.synchronize()
+    assert Y.shape == (2, 150, 192)
+    assert torch.equal(Y.reshape(300, 192), Y2)
+    assert torch.equal(X.grad.reshape(300, 256), dX2)
+    assert torch.equal(A.grad, dA2) and torch.equal(B.grad, dB2)
