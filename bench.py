@@ -10,6 +10,10 @@ HBM.  The metric is algorithmic TFLOP/s,
 divided by the device time of the step (CUDA events on the launching stream;
 L2 is flushed by a 256 MiB write before every step, outside the events).
 
+Beside the contract keys the line carries, informationally, the step rated
+against NVIDIA's dense BF16 figure and (plain layer, one GPU) the same step
+run as separate PyTorch ops with autograd ("torch_unfused").
+
 Rank 0 prints one JSON line.  Under torchrun each rank runs an independent
 replica on its own GPU (the layer needs no exchange), the timed region is
 bracketed by barriers, and the slowest rank's time is used.
@@ -39,6 +43,9 @@ METRIC = ("fused LoRA fwd+bwd TFLOP/s on 1 GB300 (Llama-3-8B shapes); "
 DEFAULT_WORKLOAD = "llama3_8b_q_proj"
 FLUSH_BYTES = 256 << 20
 FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
+# NVIDIA's dense (no 2:4 sparsity) BF16 tensor figure for one GB300, reported
+# beside the measured peak
+DATASHEET_BF16_TFLOPS = 2250.0
 
 
 def step_flops(M, d_in, d_out, r):
@@ -311,6 +318,42 @@ def run_reference(args, w):
 
 
 # ---------------------------------------------------------------- GPU
+def run_torch_unfused(w, t, dev, stream, steps, flush):
+    """The unfused layer as separate PyTorch ops with autograd (W frozen), in the
+    workload's dtype on the same GPU: the baseline the fused kernels replace.
+    Same step (forward + backward), same L2 flush, same FLOP count."""
+    import torch
+    X = t["X"].detach().clone().requires_grad_(True)
+    W = t["W"].detach()
+    A = t["A"].detach().clone().requires_grad_(True)
+    B = t["B"].detach().clone().requires_grad_(True)
+    dY = t["dY"]
+    s = w.alpha / w.r
+
+    def step():
+        X.grad = A.grad = B.grad = None
+        Y = X @ W.t() + ((X @ A.t()) @ B.t()) * s
+        Y.backward(dY)
+
+    for _ in range(3):
+        flush.zero_()
+        step()
+    torch.cuda.synchronize()
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+          for _ in range(steps)]
+    for e0, e1 in ev:
+        flush.zero_()
+        e0.record(stream)
+        step()
+        e1.record(stream)
+    torch.cuda.synchronize()
+    sec = sum(e0.elapsed_time(e1) for e0, e1 in ev) / 1e3
+    return {"value": step_flops(w.M, w.d_in, w.d_out, w.r) * steps / sec / 1e12,
+            "unit": "TFLOP/s", "ms_per_step": 1e3 * sec / steps, "steps": steps,
+            "what": "X W^T + s (X A^T) B^T as separate torch ops (cuBLAS) with autograd, "
+                    "same dtype, L2 flushed before every step; informational"}
+
+
 def run_ours(args, w):
     import torch
     import rank_linear_gb300 as rl
@@ -480,6 +523,9 @@ def run_ours(args, w):
 
     e2e = None if (args.no_e2e or swiglu or fp8 or q4) else run_e2e(args, w, t, tdt, dev, stream,
                                                                      world)
+    unfused = None
+    if rank == 0 and world == 1 and not (swiglu or fp8 or q4 or args.no_unfused):
+        unfused = run_torch_unfused(w, t, dev, stream, max(3, min(args.steps, 50)), flush)
 
     if rank == 0:
         line = {
@@ -495,10 +541,12 @@ def run_ours(args, w):
                        "alpha": alpha, "l2": "flushed before every step (256 MiB write)",
                        "parallelism": "replicas" if world > 1 else "single GPU"},
             "pct_of_bf16_peak": 100.0 * value / world / peaks["bf16_tflops"],
+            "pct_of_datasheet_bf16_peak": 100.0 * value / world / DATASHEET_BF16_TFLOPS,
+            "datasheet_bf16_tflops": DATASHEET_BF16_TFLOPS,
             "roofline": roofline, "kernels": kern,
             "kernel_timing": "second pass of the same K steps with CUDA events around "
                              "every library launch (on the launching stream)",
-            "cpu_baseline": cpu, "e2e": e2e,
+            "cpu_baseline": cpu, "e2e": e2e, "torch_unfused": unfused,
             "gpu_launches": launched,
             "clocks": clk,
         }
@@ -596,6 +644,8 @@ def main(argv=None):
     ap.add_argument("--workload", default=DEFAULT_WORKLOAD, choices=sorted(WORKLOADS))
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-unfused", action="store_true",
+                    help="skip the informational unfused PyTorch timing")
     args = ap.parse_args(argv)
     args.warmup = max(args.warmup, 3)  # at least three untimed warm-up steps
     w = WORKLOADS[args.workload]
