@@ -108,11 +108,38 @@ def load_peaks():
         return dict(FALLBACK_PEAKS, source="fallback")
 
 
+def _strip_comments(src: str) -> str:
+    """C/C++ source without its // and /* */ comments (string literals kept)."""
+    out, i, n = [], 0, len(src)
+    while i < n:
+        c = src[i]
+        if c == '"':  # string literal, escapes kept
+            j = i + 1
+            while j < n and src[j] != '"':
+                j += 2 if src[j] == "\\" else 1
+            out.append(src[i:j + 1])
+            i = j + 1
+        elif src.startswith("//", i):
+            j = src.find("\n", i)
+            i = n if j < 0 else j
+        elif src.startswith("/*", i):
+            j = src.find("*/", i + 2)
+            i = n if j < 0 else j + 2
+        else:
+            out.append(c)
+            i += 1
+    return "".join(out)
+
+
 def kernel_source_hash():
+    """Hash of the kernel sources with comments removed and whitespace runs
+    collapsed: the committed ncu traffic figures stay valid across comment
+    and layout edits, not across code edits."""
     h = hashlib.sha256()
     csrc = os.path.join(ROOT, "rank_linear_gb300", "csrc")
     for f in sorted(os.listdir(csrc)):
-        h.update(open(os.path.join(csrc, f), "rb").read())
+        code = _strip_comments(open(os.path.join(csrc, f), encoding="utf-8").read())
+        h.update(" ".join(code.split()).encode())
     return h.hexdigest()[:16]
 
 

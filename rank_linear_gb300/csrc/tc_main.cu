@@ -31,6 +31,17 @@
 // counts itself in; the CTA that arrives second adds the other partial to
 // its own, still in TMEM, and writes the bf16 tile.  fp32 addition of two
 // terms is commutative, so the result does not depend on who is second.
+//
+// Instantiations beside the plain one (template flags of k_main_gemm):
+//   GATED  the SwiGLU gate/up pair: the odd CTA streams the up projection,
+//          the epilogue writes silu(gate) * up (and gate, up for training);
+//   DUAL_B the pair's dX GEMM: the B map switches from Wg to Wu mid-K;
+//   FP8    an e4m3 main segment (kind::f8f6f4, 128-wide K blocks) with the
+//          bf16 extension in the same accumulator and per-row scales applied
+//          in the epilogue;
+//   Q4     a 4-bit W: each stage carries packed codes and bf16 group scales,
+//          and six groups of two extra warps (one per ring stage) expand
+//          them into the bf16 B tile in shared memory.
 #include <cuda_bf16.h>
 
 #include "internal.h"

@@ -70,3 +70,18 @@ def test_traffic_only_for_matching_sources(tmp_path, monkeypatch):
     assert bench.load_traffic("wl_b", "main_fwd") is None
     assert bench.load_traffic("wl_a", "main_bwd") is None
 
+
+
+def test_kernel_hash_ignores_comments_not_code(tmp_path, monkeypatch):
+    csrc = tmp_path / "rank_linear_gb300" / "csrc"
+    csrc.mkdir(parents=True)
+    f = csrc / "k.cu"
+    monkeypatch.setattr(bench, "ROOT", str(tmp_path))
+    f.write_text('// header\nint a = 1; /* note */\nconst char *s = "x // y";\n')
+    h0 = bench.kernel_source_hash()
+    f.write_text('// a longer header\n// over two lines\nint a = 1;\n\nconst char *s = "x // y";\n')
+    assert bench.kernel_source_hash() == h0          # comments and layout only
+    f.write_text('int a = 2;\nconst char *s = "x // y";\n')
+    assert bench.kernel_source_hash() != h0          # code
+    f.write_text('int a = 1;\nconst char *s = "x / y";\n')
+    assert bench.kernel_source_hash() != h0          # a string literal is code
