@@ -131,13 +131,19 @@ def _strip_comments(src: str) -> str:
     return "".join(out)
 
 
-def kernel_source_hash():
-    """Hash of the kernel sources with comments removed and whitespace runs
-    collapsed: the committed ncu traffic figures stay valid across comment
-    and layout edits, not across code edits."""
+# the sources each kernel kind is compiled from (kinds not listed: all)
+KERNEL_FILES = {"main_fwd": ("tc_main.cu", "ptx.cuh", "internal.h"),
+                "main_bwd": ("tc_main.cu", "ptx.cuh", "internal.h")}
+
+
+def kernel_source_hash(files=None):
+    """Hash of kernel sources (`files` of csrc/, default all) with comments
+    removed and whitespace runs collapsed: a committed ncu traffic figure
+    stays valid across comment and layout edits, and across edits of other
+    kernels' files, not across its own kernel's code."""
     h = hashlib.sha256()
     csrc = os.path.join(ROOT, "rank_linear_gb300", "csrc")
-    for f in sorted(os.listdir(csrc)):
+    for f in sorted(files if files is not None else os.listdir(csrc)):
         code = _strip_comments(open(os.path.join(csrc, f), encoding="utf-8").read())
         h.update(" ".join(code.split()).encode())
     return h.hexdigest()[:16]
@@ -152,7 +158,7 @@ def load_traffic(workload, kind):
     except Exception:
         return None
     ent = d.get(workload, {}).get(kind)
-    if not ent or ent.get("source_hash") != kernel_source_hash():
+    if not ent or ent.get("source_hash") != kernel_source_hash(KERNEL_FILES.get(kind)):
         return None
     return ent.get("bytes_per_launch")
 

@@ -403,7 +403,8 @@ Prob to_prob(const SkinnyArgs &a, int S) {
 // {1, 2, 4, 8} minimising  waves(S) x (t_kb * ceil(max_kb / S) + t_cta),
 // where waves counts two CTAs per SM, t_kb ~ 0.15 us is the time of one K
 // block of a CTA with every slot streaming and t_cta ~ 4 us is a CTA's fixed
-// cost (start-up latency and the cluster reduction).  Ties go to fewer CTAs.
+// cost (start-up latency and the cluster reduction).  Ties go to fewer CTAs;
+// the grid is then kept to about 1.2 waves.
 int skinny_split_launch(int total_mt, int max_kb, int num_sms) {
   const int slots = 2 * num_sms;
   const double t_kb = 0.15, t_cta = 4.0;
@@ -418,6 +419,10 @@ int skinny_split_launch(int total_mt, int max_kb, int num_sms) {
       best = S;
     }
   }
+  // Grids of more than about 1.2 waves ran slower than the model says
+  // (gate/up's grouped s dY B + dB launch: 82 us at 2.3 waves, 68 us at
+  // 1.16): fewer, longer CTAs then.
+  while (best > 1 && 10 * total_mt * best > 12 * slots) best /= 2;
   return best;
 }
 

@@ -65,7 +65,7 @@ def test_traffic_only_for_matching_sources(tmp_path, monkeypatch):
         "wl_b": {"main_fwd": {"bytes_per_launch": 456, "source_hash": "0" * 16}}}))
     monkeypatch.setattr(bench, "ROOT", str(tmp_path))
     # kernel_source_hash reads the real sources; only traffic.json moves
-    monkeypatch.setattr(bench, "kernel_source_hash", lambda: h)
+    monkeypatch.setattr(bench, "kernel_source_hash", lambda files=None: h)
     assert bench.load_traffic("wl_a", "main_fwd") == 123
     assert bench.load_traffic("wl_b", "main_fwd") is None
     assert bench.load_traffic("wl_a", "main_bwd") is None
