@@ -63,7 +63,11 @@ static_assert(128 % DQ_GROUP_THREADS == 0, "dequantising split");
 // 4-bit W stage: 128 B-tile rows of 64 codes (32 bytes) or 64 K-rows of 128
 // codes, then 128 bf16 scales
 constexpr uint32_t RAW_CODE_BYTES = 4096, RAW_BYTES = RAW_CODE_BYTES + 256;
-constexpr int GROUP_M = 4;                   // rasterisation: m-block pairs per group
+// Rasterisation: m-block pairs per group.  A group's X panels (16 x 256
+// rows) stay in L2 while the W panels stream past, so W is read from DRAM
+// once per group: on the gate/up shape 2 times instead of 8 with groups of
+// 4, and the power-capped GEMMs ran 1.5-2.5 % faster.
+constexpr int GROUP_M = 16;
 constexpr int EPI_ARRIVALS = 4 * CLUSTER;    // epilogue warps of both CTAs
 constexpr size_t kStageBudget = 192 * 1024;  // shared memory for the stage ring
 
