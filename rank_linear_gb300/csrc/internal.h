@@ -103,6 +103,12 @@ struct SkinnyArgs {
   // Optional per-row divisor of out0 (powers of two, so exact): out0 row m
   // is divided by row_div[m]; out1 is not.
   const float *row_div = nullptr;
+  // The preceding kernel is a main GEMM (it signals its dependents only once
+  // every kernel before it has finished) and writes nothing this launch
+  // reads: skip the wait at the start, so the launch streams on the SMs the
+  // GEMM frees; the last cluster waits before it leaves, so the launch still
+  // ends after the GEMM.  Not allowed with zero_ptr.
+  int after_gemm = 0;
 };
 // Runs one or two independent problems in one launch.
 cudaError_t launch_skinny(const SkinnyArgs *probs, int nprob, int num_sms, cudaStream_t s);

@@ -485,6 +485,7 @@ lora_status_t bwd_bf16(const void *dY, const void *X, const void *W, const void 
   b3.ld1 = d_in;
   b3.n1 = r;
   b3.dev_status = di.status;
+  b3.after_gemm = dX != nullptr;  // overlaps the dX GEMM's last wave
   int pending = g_withhold.load();  // test hook of the bounded waits
   while (pending > 0 && !g_withhold.compare_exchange_weak(pending, pending - 1)) {
   }
@@ -887,6 +888,7 @@ lora_status_t sw_bwd_bf16(const void *dH, const void *X, const void *Wg, const v
     a[p].ld1 = d_in;
     a[p].n1 = r;
     a[p].dev_status = di.status;
+    a[p].after_gemm = dX != nullptr;
   }
   return run(LORA_K_GRAD_A, st, "dA passes (gate, up)",
              [&] { return launch_skinny(a, 2, di.sms, st); });
@@ -1149,6 +1151,7 @@ lora_status_t fp8_bwd(const void *dY, const void *X, const void *WqT, const floa
   b3.ld1 = d_in;
   b3.n1 = r;
   b3.dev_status = di.status;
+  b3.after_gemm = dX != nullptr;
   return run(LORA_K_GRAD_A, st, "dA pass", [&] { return launch_skinny(&b3, 1, di.sms, st); });
 }
 

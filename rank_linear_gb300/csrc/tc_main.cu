@@ -319,8 +319,11 @@ __global__ void __launch_bounds__(Q4 ? Q4_THREADS : NUM_THREADS, 1)
   // low-rank operand of the K extension is already final, and nothing this
   // kernel writes is read by it.  Only the producer waits, right before its
   // first load of the extension; the main K segment overlaps the tail of
-  // the preceding kernel.
-  griddep_launch_dependents();
+  // the preceding kernel.  The producer also signals the next kernel, and
+  // only after that wait: once every CTA has signalled (or left), every
+  // kernel before this one has finished, which lets the backward's dA pass
+  // (it reads what the pass before this GEMM wrote) start on the SMs this
+  // grid frees before the grid has ended.
   if (warp == 1) {
     tmem_alloc_pair(smem_u32(&tail->tmem_base), TMEM_COLS);
     tmem_relinquish_pair();
@@ -392,6 +395,7 @@ __global__ void __launch_bounds__(Q4 ? Q4_THREADS : NUM_THREADS, 1)
           }
           if (ext && !dep_done) {  // sH / sG come from the preceding kernel
             griddep_wait();
+            griddep_launch_dependents();
             dep_done = true;
           }
           const CUtensorMap *ta = ext ? &tmA2 : &tmA;
@@ -901,6 +905,9 @@ MainSplit main_gemm_split(int M, int N, int pairs) {
 int main_gemm_pick_bn(int, int, int) { return 256; }
 
 cudaError_t launch_main_gemm(const MainGemmArgs &a, int num_sms, cudaStream_t s) {
+  // Every pair tile ends in the K extension, where the producer waits for the
+  // preceding kernel and signals the next one.
+  if (a.k_ext <= 0) return cudaErrorInvalidValue;
   const bool split = a.split_k > 1 && a.split_rem > 0;
   if (a.q4) {  // 4-bit W: codes in tmB, bf16 group scales in tmB3
     if (a.fp8 || a.gated || a.kb_switch >= 0) return cudaErrorInvalidValue;

@@ -69,6 +69,7 @@ struct Params {
   int zero_words = 0;
   unsigned *dev_status = nullptr;
   int withhold = 0;  // test hook: CTA 0 never fills its first stage
+  int after_gemm = 0;  // no wait at the start; the last cluster waits at the end
 };
 
 struct SkinnyLayout {
@@ -154,8 +155,10 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     tma_prefetch(tmB);
   }
   // Only this CTA's shared memory is touched above; global data and TMEM
-  // are used only after the preceding kernel has finished.
-  griddep_wait();
+  // are used only after the preceding kernel has finished -- or, after a
+  // main GEMM, once that GEMM has signalled: then every kernel before it
+  // has finished, and the GEMM writes nothing read here.
+  if (!P.after_gemm) griddep_wait();
   griddep_launch_dependents();
   if (blockIdx.x == 0 && P.zero_ptr != nullptr)
     for (int i = threadIdx.x; i < P.zero_words; i += NUM_THREADS) P.zero_ptr[i] = 0u;
@@ -372,6 +375,10 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     tc_fence_after();
     tmem_dealloc(tmem_base, L.tmem_cols);
   }
+  // The launch must not end before the GEMM it overlapped: the kernels after
+  // it rely on each kernel having finished after its predecessor.
+  if (P.after_gemm && static_cast<int>(blockIdx.x) >= static_cast<int>(gridDim.x) - S)
+    griddep_wait();
 }
 
 Prob to_prob(const SkinnyArgs &a, int S) {
@@ -456,11 +463,15 @@ cudaError_t launch_skinny(const SkinnyArgs *probs, int nprob, int num_sms, cudaS
   }
   P.dev_status = use[0]->dev_status;
   P.withhold = use[0]->withhold_first_stage;
-  for (int i = 0; i < nprob; ++i)
+  P.after_gemm = use[0]->after_gemm;
+  for (int i = 0; i < nprob; ++i) {
+    if (probs[i].after_gemm != P.after_gemm) return cudaErrorInvalidValue;
     if (probs[i].zero_ptr != nullptr) {
+      if (P.after_gemm) return cudaErrorInvalidValue;  // would race the GEMM's counters
       P.zero_ptr = probs[i].zero_ptr;
       P.zero_words = probs[i].zero_words;
     }
+  }
   cudaError_t e = cudaFuncSetAttribute(k_skinny, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                        static_cast<int>(smem));
   if (e != cudaSuccess) return e;
