@@ -351,10 +351,12 @@ def run_reference(args, w):
 
 
 # ---------------------------------------------------------------- GPU
-def run_torch_unfused(w, t, dev, stream, steps, flush):
+def run_torch_unfused(w, t, dev, stream, steps, flush, gpu_index):
     """The unfused layer as separate PyTorch ops with autograd (W frozen), in the
     workload's dtype on the same GPU: the baseline the fused kernels replace.
-    Same step (forward + backward), same L2 flush, same FLOP count."""
+    Same step (forward + backward), same number of steps, same L2 flush, same
+    FLOP count; its own clock record, since on power-capped shapes the SM
+    clock decides the comparison."""
     import torch
     X = t["X"].detach().clone().requires_grad_(True)
     W = t["W"].detach()
@@ -374,17 +376,25 @@ def run_torch_unfused(w, t, dev, stream, steps, flush):
     torch.cuda.synchronize()
     ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
           for _ in range(steps)]
+    clocks = ClockSampler(gpu_index)
+    clocks.start()
+    time.sleep(0.3)
+    wall0 = time.time()
     for e0, e1 in ev:
         flush.zero_()
         e0.record(stream)
         step()
         e1.record(stream)
     torch.cuda.synchronize()
+    wall1 = time.time()
+    time.sleep(0.2)
+    clocks.stop()
     sec = sum(e0.elapsed_time(e1) for e0, e1 in ev) / 1e3
     return {"value": step_flops(w.M, w.d_in, w.d_out, w.r) * steps / sec / 1e12,
             "unit": "TFLOP/s", "ms_per_step": 1e3 * sec / steps, "steps": steps,
+            "clocks": clocks.summary(wall0, wall1),
             "what": "X W^T + s (X A^T) B^T as separate torch ops (cuBLAS) with autograd, "
-                    "same dtype, L2 flushed before every step; informational"}
+                    "same dtype, same steps, L2 flushed before every step; informational"}
 
 
 def run_ours(args, w):
@@ -558,7 +568,7 @@ def run_ours(args, w):
                                                                      world)
     unfused = None
     if rank == 0 and world == 1 and not (swiglu or fp8 or q4 or args.no_unfused):
-        unfused = run_torch_unfused(w, t, dev, stream, max(3, min(args.steps, 50)), flush)
+        unfused = run_torch_unfused(w, t, dev, stream, args.steps, flush, local)
 
     if rank == 0:
         line = {
