@@ -149,3 +149,28 @@ def test_autograd_matches_the_explicit_calls():
     assert torch.equal(Y.reshape(300, 192), Y2)
     assert torch.equal(X.grad.reshape(300, 256), dX2)
     assert torch.equal(A.grad, dA2) and torch.equal(B.grad, dB2)
+
+
+def test_back_to_back_backward_calls():
+    """Backward calls with different upstream gradients, enqueued back to back
+    on one workspace (the dA pass starts in the dX GEMM's last wave), each
+    give what they give when run alone."""
+    M, d_in, d_out, r, alpha = 2048, 2048, 2048, 16, 32.0
+    g = {k: v.to(DEV) for k, v in inputs(M, d_in, d_out, r, seed=41).items()}
+    qw = rl.quantize_w_fp8(g["W"])
+    ws = torch.empty(rl.fp8_workspace_bytes(M, d_in, d_out, r), dtype=torch.uint8, device=DEV)
+    _, saved = rl.fp8_forward(g["X"], qw, g["A"], g["B"], alpha, workspace=ws)
+    gen = torch.Generator(device=DEV).manual_seed(7)
+    dYs = [torch.randn(M, d_out, device=DEV, generator=gen).bfloat16() for _ in range(4)]
+    alone = []
+    for dY in dYs:
+        alone.append(rl.fp8_backward(dY, g["X"], qw, g["A"], g["B"], alpha, saved, workspace=ws))
+        torch.cuda.synchronize()
+    chained = [rl.fp8_backward(dY, g["X"], qw, g["A"], g["B"], alpha, saved, workspace=ws)
+               for dY in dYs]
+    torch.cuda.synchronize()
+    rl.device_status()
+    for a, b in zip(alone, chained):
+        for x, y in zip(a, b):
+            assert torch.equal(x, y)
+    assert not torch.equal(alone[0][1], alone[1][1])

@@ -242,3 +242,32 @@ def test_tail_split_path():
     rows = np.array([0, 2047, 3071, 3584, 4095])  # include rows of the split tiles
     assert rel_err(s1[0][rows], S.y_rows(rows)) <= TOL["bf16"]
     assert rel_err(s1[1][rows], S.dx_rows(rows)) <= TOL["bf16"]
+
+
+@pytest.mark.parametrize("M,d", [(2048, 2048), (4096, 4096)])
+def test_back_to_back_backward_calls(M, d):
+    """The dA pass starts in the dX GEMM's last wave without waiting for the
+    GEMM: it relies on the GEMM letting it start only once every kernel
+    before the GEMM -- among them the pass that writes sG -- has finished.
+    Backward calls with different upstream gradients, enqueued back to back
+    on one workspace (each overwrites the previous call's sG), must each
+    give what they give when run alone."""
+    r, alpha = 16, 16.0
+    t = make_inputs(M, d, d, r, "bf16", seed=21, device=DEV)
+    X, W, A, B = t["X"], t["W"], t["A"], t["B"]
+    ws = torch.empty(rl.workspace_bytes(M, d, d, r, torch.bfloat16), dtype=torch.uint8,
+                     device=DEV)
+    _, saved = rl.forward(X, W, A, B, alpha, workspace=ws)
+    gen = torch.Generator(device=DEV).manual_seed(5)
+    dYs = [torch.randn(M, d, device=DEV, generator=gen).bfloat16() for _ in range(4)]
+    alone = []
+    for dY in dYs:
+        alone.append(rl.backward(dY, X, W, A, B, alpha, saved, workspace=ws))
+        torch.cuda.synchronize()
+    chained = [rl.backward(dY, X, W, A, B, alpha, saved, workspace=ws) for dY in dYs]
+    torch.cuda.synchronize()
+    rl.device_status()
+    for a, b in zip(alone, chained):
+        for x, y in zip(a, b):
+            assert torch.equal(x, y)
+    assert not torch.equal(alone[0][1], alone[1][1])  # the calls' dA really differ

@@ -178,3 +178,27 @@ def test_empty_batch():
     assert H.shape == (0, 64) and dX.shape == (0, 64)
     for z in (dAg, dBg, dAu, dBu):
         assert torch.count_nonzero(z) == 0
+
+
+def test_back_to_back_backward_calls():
+    """Backward calls with different upstream gradients, enqueued back to back
+    on one workspace (the dA passes start in the dX GEMM's last wave), each
+    give what they give when run alone."""
+    M, d_in, d_ff, r, alpha = 2048, 1024, 2816, 16, 32.0
+    g = {k: v.to(DEV) for k, v in make_pair(M, d_in, d_ff, r, seed=31).items()}
+    args = [g[k] for k in ("Wg", "Ag", "Bg", "Wu", "Au", "Bu")]
+    ws = torch.empty(rl.swiglu_workspace_bytes(M, d_in, d_ff, r), dtype=torch.uint8, device=DEV)
+    _, saved = rl.swiglu_forward(g["X"], *args, alpha, workspace=ws)
+    gen = torch.Generator(device=DEV).manual_seed(6)
+    dHs = [torch.randn(M, d_ff, device=DEV, generator=gen).bfloat16() for _ in range(4)]
+    alone = []
+    for dH in dHs:
+        alone.append(rl.swiglu_backward(dH, g["X"], *args, alpha, saved, workspace=ws))
+        torch.cuda.synchronize()
+    chained = [rl.swiglu_backward(dH, g["X"], *args, alpha, saved, workspace=ws) for dH in dHs]
+    torch.cuda.synchronize()
+    rl.device_status()
+    for a, b in zip(alone, chained):
+        for x, y in zip(a, b):
+            assert torch.equal(x, y)
+    assert not torch.equal(alone[0][1], alone[1][1])
