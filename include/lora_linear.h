@@ -123,7 +123,9 @@ lora_status_t lora_linear_fwd(const void *X, const void *W, const void *A,
  * Kernels: s*dY B is computed once (skinny tensor-core pass) and reused by
  * the K-extended dX GEMM over [dY | s dY B] . [W ; A] and by the dA pass;
  * dA and dB are skinny split-K passes whose partial sums are combined in
- * shared memory across a thread-block cluster in a fixed order.
+ * shared memory across a thread-block cluster in a fixed order.  The dA
+ * pass starts on the SMs the dX GEMM frees in its last wave; work queued
+ * after the call on the same stream still starts only once both are done.
  */
 lora_status_t lora_linear_bwd(const void *dY, const void *X, const void *W,
                               const void *A, const void *B, const void *saved,
