@@ -63,11 +63,16 @@ static_assert(128 % DQ_GROUP_THREADS == 0, "dequantising split");
 // 4-bit W stage: 128 B-tile rows of 64 codes (32 bytes) or 64 K-rows of 128
 // codes, then 128 bf16 scales
 constexpr uint32_t RAW_CODE_BYTES = 4096, RAW_BYTES = RAW_CODE_BYTES + 256;
-// Rasterisation: m-block pairs per group.  A group's X panels (16 x 256
-// rows) stay in L2 while the W panels stream past, so W is read from DRAM
-// once per group: on the gate/up shape 2 times instead of 8 with groups of
-// 4, and the power-capped GEMMs ran 1.5-2.5 % faster.
-constexpr int GROUP_M = 16;
+// Rasterisation: groups of GROUP_M_MIN..GROUP_M_MAX m-block pairs.  A
+// group's A panels (group x 256 rows x K) should stay in L2 while the B
+// panels stream past, so B is read from DRAM once per group: on the gate/up
+// shape 2 times instead of 8 with groups of 4 (the power-capped GEMMs ran
+// 1.5-2.5 % faster).  With K = 14336 a group of 16 holds 117 MB of A, which
+// L2 does not keep; groups sized for about 60 MiB of A (8 there) cut the
+// dX GEMM's DRAM traffic from 1.27 to 1.11 GB and the gate/up, down_proj and
+// Qwen-class steps by 1.0-1.4 %.  Groups of 4 and 6 were slower.
+constexpr int GROUP_M_MIN = 8, GROUP_M_MAX = 16;
+constexpr int64_t kGroupABytes = 60ll << 20;
 constexpr int EPI_ARRIVALS = 4 * CLUSTER;    // epilogue warps of both CTAs
 constexpr size_t kStageBudget = 192 * 1024;  // shared memory for the stage ring
 
@@ -147,13 +152,14 @@ __device__ __forceinline__ void item_range(int item, int split_first, int split_
   }
 }
 
-// Pair-tile order: groups of GROUP_M m-pairs; within a group the m-pair
+// Pair-tile order: groups of group_m m-pairs; within a group the m-pair
 // varies fastest, so the pairs of one wave share a few A and B panels in L2.
-__device__ __forceinline__ void tile_coords(int tile, int m_pairs, int n_tiles, int &mp, int &nb) {
-  const int per_group = GROUP_M * n_tiles;
+__device__ __forceinline__ void tile_coords(int tile, int m_pairs, int n_tiles, int group_m,
+                                            int &mp, int &nb) {
+  const int per_group = group_m * n_tiles;
   const int g = tile / per_group;
-  const int first = g * GROUP_M;
-  const int gm = min(GROUP_M, m_pairs - first);
+  const int first = g * group_m;
+  const int gm = min(group_m, m_pairs - first);
   const int local = tile - g * per_group;
   mp = first + local % gm;
   nb = local / gm;
@@ -246,7 +252,7 @@ __global__ void __launch_bounds__(Q4 ? Q4_THREADS : NUM_THREADS, 1)
     k_main_gemm(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                 const __grid_constant__ CUtensorMap tmA2, const __grid_constant__ CUtensorMap tmB2,
                 const __grid_constant__ CUtensorMap tmB3, const __grid_constant__ CUtensorMap tmB4,
-                int M, int N, int kb_main, int k_ext, int kb_switch, int ext_shift,
+                int M, int N, int kb_main, int k_ext, int kb_switch, int ext_shift, int group_m,
                 __nv_bfloat16 *__restrict__ out, __nv_bfloat16 *__restrict__ aux0,
                 __nv_bfloat16 *__restrict__ aux1, int64_t ldo, int split_k, int split_rem,
                 float *__restrict__ partials, unsigned *counters, unsigned *dev_status,
@@ -347,7 +353,7 @@ __global__ void __launch_bounds__(Q4 ? Q4_THREADS : NUM_THREADS, 1)
         int tile, kb_lo, kb_hi, chunk, rel;
         item_range(item, split_first, split_k, split_rem, kb_total, tile, kb_lo, kb_hi, chunk, rel);
         int mp, nb;
-        tile_coords(tile, m_pairs, n_tiles, mp, nb);
+        tile_coords(tile, m_pairs, n_tiles, group_m, mp, nb);
         const int m0 = (2 * mp + q) * BM;
         // this CTA's half of the B tile: columns q*BN/2.. of the tile, or for
         // the gated pair the same TN rows of its own projection
@@ -645,7 +651,7 @@ __global__ void __launch_bounds__(Q4 ? Q4_THREADS : NUM_THREADS, 1)
       const int acc = t & 1;
       const uint32_t use = static_cast<uint32_t>(t >> 1);
       int mp, nb;
-      tile_coords(tile, m_pairs, n_tiles, mp, nb);
+      tile_coords(tile, m_pairs, n_tiles, group_m, mp, nb);
       const bool got = mbar_wait(smem_u32(&tail->tfull[acc]), use & 1u, abort_flag, dev_status);
       if (!__all_sync(0xffffffffu, got)) break;
       tc_fence_after();
@@ -834,6 +840,14 @@ int max_clusters(int num_sms) {
   return n;
 }
 
+// m-block pairs per raster group for a main K segment of kb_main blocks
+// (each 128 bytes of an A row, bf16 or e4m3).
+int main_gemm_group_m(int kb_main) {
+  const int64_t panel = int64_t(2 * BM) * kb_main * 128;  // A bytes of one m-block pair
+  const int64_t g = panel > 0 ? kGroupABytes / panel : GROUP_M_MAX;
+  return static_cast<int>(g < GROUP_M_MIN ? GROUP_M_MIN : g > GROUP_M_MAX ? GROUP_M_MAX : g);
+}
+
 template <bool B_MN, int BN, bool SPLIT, bool GATED, bool DUAL_B, bool FP8 = false,
           bool Q4 = false>
 cudaError_t launch_variant(const MainGemmArgs &a, int num_sms, cudaStream_t s) {
@@ -867,7 +881,7 @@ cudaError_t launch_variant(const MainGemmArgs &a, int num_sms, cudaStream_t s) {
   const CUtensorMap &tmB3 = (GATED || Q4 || a.kb_switch >= 0) ? a.tmB3 : a.tmB;
   const CUtensorMap &tmB4 = GATED ? a.tmB4 : a.tmB2;
   return cudaLaunchKernelEx(&cfg, kern, a.tmA, a.tmB, a.tmA2, a.tmB2, tmB3, tmB4, a.M, a.N,
-                            a.kb_main, a.k_ext, kb_switch, a.ext_shift,
+                            a.kb_main, a.k_ext, kb_switch, a.ext_shift, main_gemm_group_m(a.kb_main),
                             static_cast<__nv_bfloat16 *>(a.out),
                             static_cast<__nv_bfloat16 *>(a.aux0),
                             static_cast<__nv_bfloat16 *>(a.aux1), a.ldo, a.split_k, a.split_rem,
