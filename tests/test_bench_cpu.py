@@ -85,3 +85,24 @@ def test_kernel_hash_ignores_comments_not_code(tmp_path, monkeypatch):
     assert bench.kernel_source_hash() != h0          # code
     f.write_text('int a = 1;\nconst char *s = "x / y";\n')
     assert bench.kernel_source_hash() != h0          # a string literal is code
+
+
+def test_reference_arm_under_torchrun_prints_once():
+    """Launched as the driver launches N > 1 (torchrun, one process per rank):
+    rank 0 alone times the oracle and prints the line; the other rank exits 0
+    without work."""
+    import socket
+    with socket.socket() as s:
+        s.bind(("127.0.0.1", 0))
+        port = s.getsockname()[1]
+    out = subprocess.run(
+        [sys.executable, "-m", "torch.distributed.run", "--nnodes=1", "--nproc-per-node", "2",
+         "--master-addr", "127.0.0.1", "--master-port", str(port),
+         os.path.join(ROOT, "bench.py"), "--impl", "reference", "--gpus", "2",
+         "--workload", "tiny_fp32", "--steps", "2", "--warmup", "1"],
+        capture_output=True, text=True, timeout=600, cwd=ROOT)
+    assert out.returncode == 0, out.stderr
+    lines = [l for l in out.stdout.splitlines() if l.strip().startswith("{")]
+    assert len(lines) == 1
+    d = json.loads(lines[0])
+    assert d["impl"] == "reference" and d["n_gpus"] == 2 and d["value"] > 0
