@@ -415,12 +415,15 @@ Prob to_prob(const SkinnyArgs &a, int S) {
 int skinny_split_launch(int total_mt, int max_kb, int num_sms) {
   const int slots = 2 * num_sms;
   const double t_kb = 0.15, t_cta = 4.0;
+  auto cost_of = [&](int S) {
+    const double waves = static_cast<double>((total_mt * S + slots - 1) / slots);
+    return waves * (t_kb * ((max_kb + S - 1) / S) + t_cta);
+  };
   int best = 1;
   double best_cost = 1e300;
   for (int S = 1; S <= 8; S *= 2) {
     if (S > 1 && max_kb < 2 * S) break;  // keep at least two K blocks per CTA
-    const double waves = static_cast<double>((total_mt * S + slots - 1) / slots);
-    const double cost = waves * (t_kb * ((max_kb + S - 1) / S) + t_cta);
+    const double cost = cost_of(S);
     if (cost < best_cost - 1e-9) {
       best_cost = cost;
       best = S;
@@ -430,6 +433,14 @@ int skinny_split_launch(int total_mt, int max_kb, int num_sms) {
   // (gate/up's grouped s dY B + dB launch: 82 us at 2.3 waves, 68 us at
   // 1.16): fewer, longer CTAs then.
   while (best > 1 && 10 * total_mt * best > 12 * slots) best /= 2;
+  // A one-wave grid that can run one CTA per SM instead of two, for at most
+  // a quarter more modelled time, takes the smaller grid: the pass is
+  // HBM-bound either way, and the smaller grid leaves room beside the GEMMs
+  // around it (the 4096^2 step's s X A^T and dA passes: 204.9 -> 201.3 us
+  // with 128 CTAs instead of 256).
+  if (best > 1 && total_mt * best <= slots && 5 * total_mt * (best / 2) >= 4 * num_sms &&
+      cost_of(best / 2) <= 1.25 * cost_of(best))
+    best /= 2;
   return best;
 }
 
