@@ -271,3 +271,33 @@ def test_back_to_back_backward_calls(M, d):
         for x, y in zip(a, b):
             assert torch.equal(x, y)
     assert not torch.equal(alone[0][1], alone[1][1])  # the calls' dA really differ
+
+
+def test_back_to_back_alternating_dx():
+    """Backward calls that alternate between computing dX (the dA pass then
+    overlaps the dX GEMM) and skipping it (the dA pass follows the s dY B
+    pass and waits for it), enqueued back to back on one workspace, each give
+    what they give when run alone."""
+    M = d = 2048
+    r, alpha = 16, 16.0
+    t = make_inputs(M, d, d, r, "bf16", seed=23, device=DEV)
+    X, W, A, B = t["X"], t["W"], t["A"], t["B"]
+    ws = torch.empty(rl.workspace_bytes(M, d, d, r, torch.bfloat16), dtype=torch.uint8,
+                     device=DEV)
+    _, saved = rl.forward(X, W, A, B, alpha, workspace=ws)
+    gen = torch.Generator(device=DEV).manual_seed(9)
+    dYs = [torch.randn(M, d, device=DEV, generator=gen).bfloat16() for _ in range(6)]
+    flags = [True, False, True, False, False, True]
+    alone = []
+    for dY, f in zip(dYs, flags):
+        alone.append(rl.backward(dY, X, W, A, B, alpha, saved, need_dX=f, workspace=ws))
+        torch.cuda.synchronize()
+    chained = [rl.backward(dY, X, W, A, B, alpha, saved, need_dX=f, workspace=ws)
+               for dY, f in zip(dYs, flags)]
+    torch.cuda.synchronize()
+    rl.device_status()
+    for a, b, f in zip(alone, chained, flags):
+        assert (a[0] is None) == (not f) and (b[0] is None) == (not f)
+        for x, y in zip(a, b):
+            if x is not None:
+                assert torch.equal(x, y)
