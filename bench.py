@@ -25,7 +25,6 @@ reference implementation).
 from __future__ import annotations
 
 import argparse
-import ctypes
 import hashlib
 import json
 import os

@@ -6,7 +6,6 @@ into a temporary library.  The committed oracle is never modified.  All
 mutated indices stay inside the arrays for the pins' shapes.
 """
 import os
-import subprocess
 
 import pytest
 
