@@ -12,7 +12,9 @@ L2 is flushed by a 256 MiB write before every step, outside the events).
 
 Beside the contract keys the line carries, informationally, the step rated
 against NVIDIA's dense BF16 figure and (plain layer, one GPU) the same step
-run as separate PyTorch ops with autograd ("torch_unfused").
+run as separate PyTorch ops with autograd ("torch_unfused": as many steps, the
+same flush, its own record of the SM clock, which decides the comparison on
+power-capped shapes).
 
 Rank 0 prints one JSON line.  Under torchrun each rank runs an independent
 replica on its own GPU (the layer needs no exchange), the timed region is
