@@ -140,17 +140,6 @@ __device__ __forceinline__ void tma_load_2d(uint32_t dst, const CUtensorMap *tm,
       "l"(reinterpret_cast<uint64_t>(tm)), "r"(bar), "r"(x), "r"(y)
       : "memory");
 }
-// Same, multicast: the box lands at the same shared-memory offset in every
-// CTA of the cluster named in cta_mask, and each of them counts the bytes
-// on its own mbarrier at offset `bar`.  The data is this GPU's own memory.
-__device__ __forceinline__ void tma_load_2d_mc(uint32_t dst, const CUtensorMap *tm, uint32_t bar,
-                                               int32_t x, int32_t y, uint16_t cta_mask) {
-  asm volatile(
-      "cp.async.bulk.tensor.2d.shared::cluster.global.mbarrier::complete_tx::bytes"
-      ".multicast::cluster [%0], [%1, {%3, %4}], [%2], %5;" ::"r"(dst),
-      "l"(reinterpret_cast<uint64_t>(tm)), "r"(bar), "r"(x), "r"(y), "h"(cta_mask)
-      : "memory");
-}
 // Untiled bulk copy of `bytes` from global memory into this CTA's shared
 // memory, counted on `bar`: both addresses 16-byte aligned, bytes a multiple
 // of 16.
