@@ -12,8 +12,19 @@
               hand-picked boundary values
   lossless  : small-integer X, W, dY are quantised without loss, so the fp8
               layer equals the plain LoRA oracle (itself pinned)
+  hand      : a 2-token example worked out by hand
+              (tests/golden/fp8_hand_worked.json) whose X, W and dY round in
+              e4m3 (ties included) and whose small entries fall into the
+              subnormal range under a per-tensor scale but not under a
+              per-row one: it fixes that W is quantised with one tensor scale,
+              X and dY with one scale per row, and that the low-rank terms and
+              the adapter gradients use the unquantised inputs
 Each planted mutant below fails at least one pin.
 """
+import json
+import os
+from fractions import Fraction
+
 import numpy as np
 import pytest
 import torch
@@ -80,8 +91,38 @@ def pin_lossless(seed=1, alpha=8.0):
         assert np.allclose(g, e, rtol=1e-13, atol=1e-11)
 
 
+GOLDEN = os.path.join(os.path.dirname(__file__), "golden", "fp8_hand_worked.json")
+
+
+def _exact(values, shape=None):
+    a = np.array([float(Fraction(v)) for v in values], dtype=np.float64)
+    return a.reshape(shape) if shape is not None else a
+
+
+def pin_hand():
+    g = json.load(open(GOLDEN))
+    sh = g["shapes"]
+    X, W, A, B, dY = (_exact(g[k], sh[k]) for k in ("X", "W", "A", "B", "dY"))
+    e = g["expected"]
+    alpha = g["alpha"]
+    wq, ws = fp8.quantize_tensor(W)
+    assert list(wq.reshape(-1)) == e["W_codes"]
+    assert np.array_equal(np.asarray(ws), np.float64(Fraction(e["W_scale"])))
+    for x, codes, scales in ((X, "X_codes", "X_scales"), (dY, "dY_codes", "dY_scales")):
+        q, sc = fp8.quantize_rows(x)
+        assert list(q.reshape(-1)) == e[codes]
+        assert np.array_equal(sc, _exact(e[scales]))
+    H, Y = fp8.forward(X, W, A, B, alpha)
+    assert np.array_equal(H.reshape(-1), _exact(e["H"]))
+    assert np.array_equal(Y, _exact(e["Y"], (2, 2)))
+    dX, dA, dB = fp8.backward(dY, X, W, A, B, alpha)
+    assert np.array_equal(dX, _exact(e["dX"], (2, 2)))
+    assert np.array_equal(dA, _exact(e["dA"], (1, 2)))
+    assert np.array_equal(dB, _exact(e["dB"], (2, 1)))
+
+
 ALL_PINS = [pin_decode, pin_encode, pin_roundtrip, pin_ties, pin_saturate, pin_scale,
-            pin_lossless]
+            pin_lossless, pin_hand]
 
 
 @pytest.mark.parametrize("pin", ALL_PINS, ids=lambda f: f.__name__)
@@ -132,11 +173,49 @@ def _mut_forward_no_w_quant(X, W, A, B, alpha, lib=None):
     return X @ A.T, fp8.dequant_rows(Xq, xs) @ W.T + s * (X @ A.T) @ B.T
 
 
+def _mut_rows_one_scale(x):
+    """X and dY quantised with one scale for the whole tensor."""
+    x = oracle._f64(x)
+    codes, scale = fp8.quantize_tensor(x)
+    return codes, np.full(x.shape[0], scale)
+
+
+def _mut_w_row_scales(w):
+    """W quantised with one scale per row (a scale that the dX product,
+    summed over d_out, could not factor out)."""
+    codes, scales = fp8.quantize_rows(w)
+    return codes, scales[:, None]
+
+
+def _mut_backward_no_dy_quant(dY, X, W, A, B, alpha, lib=None):
+    dY, X, W, A, B = map(oracle._f64, (dY, X, W, A, B))
+    Wq, ws = fp8.quantize_tensor(W)
+    s = alpha / B.shape[1]
+    G, H = dY @ B, X @ A.T
+    return dY @ (fp8.e4m3_decode(Wq) * ws) + s * G @ A, s * G.T @ X, s * dY.T @ H
+
+
+def _mut_backward_quantised_grads(dY, X, W, A, B, alpha, lib=None):
+    """dA and dB taken from the quantised X and dY."""
+    dX, _, _ = _ORIG_BACKWARD(dY, X, W, A, B, alpha)
+    dY, X, A, B = map(oracle._f64, (dY, X, A, B))
+    Xd = fp8.dequant_rows(*fp8.quantize_rows(X))
+    dYd = fp8.dequant_rows(*fp8.quantize_rows(dY))
+    s = alpha / B.shape[1]
+    G, H = dYd @ B, Xd @ A.T
+    return dX, s * G.T @ Xd, s * dYd.T @ H
+
+
+_ORIG_BACKWARD = fp8.backward
+
 MUTANTS = [("e4m3_encode", _mut_ties_away), ("pow2_scale_exponent", _mut_scale_off_by_one),
-           ("e4m3_decode", _mut_bias8_decode)]
+           ("e4m3_decode", _mut_bias8_decode), ("forward", _mut_forward_no_w_quant),
+           ("quantize_rows", _mut_rows_one_scale), ("quantize_tensor", _mut_w_row_scales),
+           ("backward", _mut_backward_no_dy_quant),
+           ("backward", _mut_backward_quantised_grads)]
 
 
-@pytest.mark.parametrize("name,fn", MUTANTS, ids=[m[0] for m in MUTANTS])
+@pytest.mark.parametrize("name,fn", MUTANTS, ids=[m[1].__name__ for m in MUTANTS])
 def test_mutant_is_caught(monkeypatch, name, fn):
     monkeypatch.setattr(fp8, name, fn)
     failed = []
