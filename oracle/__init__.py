@@ -100,6 +100,13 @@ def _ip(a: np.ndarray):
     return a.ctypes.data_as(_I)
 
 
+def _rowdot(lib, P, Q) -> np.ndarray:
+    """out[a][b] = sum_k P[a][k] Q[b][k] (k ascending), by the H routine."""
+    out = np.empty((P.shape[0], Q.shape[0]))
+    lib.lora_oracle_h(_p(P), _p(Q), P.shape[0], P.shape[1], Q.shape[0], _p(out))
+    return out
+
+
 def threads(lib=None) -> int:
     return (lib or load()).lora_oracle_threads()
 
@@ -174,11 +181,41 @@ class Sampled:
         return self._H
 
     def G(self) -> np.ndarray:
+        """G = dY B.  The H routine on (dY, B^T) forms, for every element, the
+        same products in the same order (o ascending) as the G routine, so
+        the bits are the same; it reads rows of B^T instead of columns of B,
+        which keeps a wide B in cache."""
         if self._G is None:
-            self._G = np.empty((self.M, self.r))
-            self.lib.lora_oracle_g(_p(self.dY), _p(self.B), self.M, self.d_out,
-                                   self.r, _p(self._G))
+            self._G = _rowdot(self.lib, self.dY, np.ascontiguousarray(self.B.T))
         return self._G
+
+    def dA(self) -> np.ndarray:
+        """All of dA = s G^T X, [r, d_in]: s times the row dot products of
+        G^T and X^T (each element the sum over m ascending, then scaled, as
+        the dA routine forms it)."""
+        return self.s * _rowdot(self.lib, np.ascontiguousarray(self.G().T),
+                                np.ascontiguousarray(self.X.T))
+
+    def dB(self) -> np.ndarray:
+        """All of dB = s dY^T H, [d_out, r], likewise from dY^T and H^T."""
+        return self.s * _rowdot(self.lib, np.ascontiguousarray(self.dY.T),
+                                np.ascontiguousarray(self.H().T))
+
+    # The products with the frozen W, taken by numpy's float64 matmul (a
+    # library GEMM as one step, summing in its own order): the plain loops
+    # stream all of W once per output row, which takes minutes on the
+    # largest shapes.  The low-rank terms come from the plain loops.
+    def y_rows_mm(self, rows) -> np.ndarray:
+        """Y[rows] = X[rows] W^T + s H[rows] B^T."""
+        rows = np.ascontiguousarray(rows, dtype=np.int64)
+        H = self._h_rows(rows)[rows]
+        return self.X[rows] @ self.W.T + self.s * (H @ self.B.T)
+
+    def dx_rows_mm(self, rows) -> np.ndarray:
+        """dX[rows] = dY[rows] W + s G[rows] A."""
+        rows = np.ascontiguousarray(rows, dtype=np.int64)
+        G = self._g_rows(rows)[rows]
+        return self.dY[rows] @ self.W + self.s * (G @ self.A)
 
     def _h_rows(self, rows) -> np.ndarray:
         if self._H is not None:

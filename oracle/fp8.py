@@ -134,3 +134,32 @@ def backward(dY, X, W, A, B, alpha: float, lib=None):
     G, H = smp.G(), smp.H()
     dX = dYd @ Wd + s * (G @ A)
     return dX, s * (G.T @ X), s * (dY.T @ H)
+
+
+class SampledRows:
+    """Rows of Y and dX, and all of dA and dB, of a large problem: the same
+    definitions as forward() and backward() (per-row scales of X and dY are
+    those of the sampled rows alone; W's tensor scale needs all of W)."""
+
+    def __init__(self, X, W, A, B, dY, alpha: float, lib=None):
+        self.lib = lib or load()
+        self.smp = Sampled(X, W, A, B, dY, alpha, lib=self.lib)
+        self.s = self.smp.s
+        Wq, w_scale = quantize_tensor(self.smp.W)
+        self.Wd = e4m3_decode(Wq) * w_scale
+
+    def y_rows(self, rows) -> np.ndarray:
+        rows = np.asarray(rows, dtype=np.int64)
+        Xd = dequant_rows(*quantize_rows(self.smp.X[rows]))
+        return Xd @ self.Wd.T + self.s * (self.smp.H()[rows] @ self.smp.B.T)
+
+    def dx_rows(self, rows) -> np.ndarray:
+        rows = np.asarray(rows, dtype=np.int64)
+        dYd = dequant_rows(*quantize_rows(self.smp.dY[rows]))
+        return dYd @ self.Wd + self.s * (self.smp.G()[rows] @ self.smp.A)
+
+    def dA(self) -> np.ndarray:
+        return self.smp.dA()
+
+    def dB(self) -> np.ndarray:
+        return self.smp.dB()

@@ -28,7 +28,7 @@ from __future__ import annotations
 
 import numpy as np
 
-from . import _f64, backward as lora_backward, forward as lora_forward, load
+from . import _f64, backward as lora_backward, forward as lora_forward, load, Sampled
 
 GROUP = 64
 
@@ -84,3 +84,9 @@ def forward(X, codes, scales, A, B, alpha: float, lib=None):
 def backward(dY, X, codes, scales, A, B, alpha: float, lib=None):
     """Returns (dX, dA, dB) of the layer over the dequantised W."""
     return lora_backward(dY, X, dequantize(codes, scales), A, B, alpha, lib=lib or load())
+
+
+def sampled(X, codes, scales, A, B, dY, alpha: float, lib=None) -> Sampled:
+    """The plain oracle's sampled routines (rows of Y and dX, all of dA and
+    dB) for the layer over the dequantised W."""
+    return Sampled(X, dequantize(codes, scales), A, B, dY, alpha, lib=lib or load())

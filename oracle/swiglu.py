@@ -80,6 +80,26 @@ def backward(dH, X, Wg, Ag, Bg, Wu, Au, Bu, alpha: float, lib=None):
     return dXg + dXu, dAg, dBg, dAu, dBu
 
 
+def adapter_grads_mm(dH, X, Wg, Ag, Bg, Wu, Au, Bu, alpha: float, lib=None):
+    """(dAg, dBg, dAu, dBu) as backward() defines them, for shapes where the
+    plain loops would take minutes: gate and up take their frozen-weight
+    products X Wg^T and X Wu^T from numpy's float64 matmul (a library GEMM as
+    one step, summing in its own order); the low-rank terms, the elementwise
+    step and the adapter gradients are the plain routines."""
+    lib = lib or load()
+    X = _f64(X)
+    out = []
+    pre = []
+    for W, A, B in ((Wg, Ag, Bg), (Wu, Au, Bu)):
+        smp = Sampled(X, W, A, B, None, alpha, lib=lib)
+        pre.append(X @ smp.W.T + smp.s * (smp.H() @ smp.B.T))
+    d_gate, d_up = elementwise_backward(dH, pre[0], pre[1])
+    for d, W, A, B in ((d_gate, Wg, Ag, Bg), (d_up, Wu, Au, Bu)):
+        smp = Sampled(X, W, A, B, d, alpha, lib=lib)
+        out += [smp.dA(), smp.dB()]
+    return tuple(out)
+
+
 def loss(dH, X, Wg, Ag, Bg, Wu, Au, Bu, alpha: float, lib=None) -> float:
     """L = <dH, H> from the oracle's forward (sum in fp64)."""
     _, _, H = forward(X, Wg, Ag, Bg, Wu, Au, Bu, alpha, lib=lib)
@@ -108,6 +128,24 @@ class SampledRows:
     def h_rows(self, rows):
         gate, up = self.gate_up_rows(rows)
         return silu(gate) * up
+
+    def h_rows_mm(self, rows):
+        """h_rows with the frozen-W products from numpy's matmul."""
+        rows = np.ascontiguousarray(rows, dtype=np.int64)
+        return silu(self.g.y_rows_mm(rows)) * self.u.y_rows_mm(rows)
+
+    def dx_rows_mm(self, rows):
+        """dx_rows with the frozen-W products from numpy's matmul."""
+        rows = np.ascontiguousarray(rows, dtype=np.int64)
+        gate, up = self.g.y_rows_mm(rows), self.u.y_rows_mm(rows)
+        d_gate, d_up = elementwise_backward(self.dH[rows], gate, up)
+        Xs = np.ascontiguousarray(self.X[rows])
+        local = np.arange(len(rows), dtype=np.int64)
+        out = np.zeros((len(rows), self.X.shape[1]))
+        for d, W, A, B in ((d_gate, self.W[0], self.A[0], self.B[0]),
+                           (d_up, self.W[1], self.A[1], self.B[1])):
+            out += Sampled(Xs, W, A, B, d, self.alpha, lib=self.lib).dx_rows_mm(local)
+        return out
 
     def dx_rows(self, rows):
         rows = np.ascontiguousarray(rows, dtype=np.int64)

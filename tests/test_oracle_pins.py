@@ -193,10 +193,48 @@ def test_sampled_equals_full():
     assert np.array_equal(S.da_entries(ii, kk), dA[ii, kk])
     oo, jj = [0, 39, 20, 20], [7, 0, 4, 5]
     assert np.array_equal(S.db_entries(oo, jj), dB[oo, jj])
+    assert np.array_equal(S.dA(), dA) and np.array_equal(S.dB(), dB)
     # columns computed on demand (no full H/G) give the same bits
     S2 = oracle.Sampled(X, W, A, B, dY, alpha)
     assert np.array_equal(S2.da_entries(ii, kk), dA[ii, kk])
     assert np.array_equal(S2.db_entries(oo, jj), dB[oo, jj])
+
+
+def test_full_skinny_routines_equal_the_full_backward():
+    """Sampled.G/dA/dB read transposed copies through the H routine: every
+    element is the same sum in the same order, so the bits match the
+    backward's own G, dA and dB routines."""
+    p = _problem(11, M=45, d_in=33, d_out=50, r=7)
+    X, W, A, B, dY = p["X"], p["W"], p["A"], p["B"], p["dY"]
+    alpha = 12.0
+    dX, dA, dB = oracle.backward(dY, X, W, A, B, alpha)
+    S = oracle.Sampled(X, W, A, B, dY, alpha)
+    lib = oracle.load()
+    G = np.empty((45, 7))
+    lib.lora_oracle_g(oracle._p(np.ascontiguousarray(dY)), oracle._p(np.ascontiguousarray(B)),
+                      45, 50, 7, oracle._p(G))
+    assert np.array_equal(S.G(), G)
+    assert np.array_equal(S.dA(), dA)
+    assert np.array_equal(S.dB(), dB)
+
+
+def test_matmul_rows_agree_with_the_loops():
+    """The frozen-W products taken by numpy's matmul agree with the plain
+    loops to float64 rounding (they differ only in summation order)."""
+    p = _problem(12, M=70, d_in=300, d_out=260, r=9)
+    X, W, A, B, dY = p["X"], p["W"], p["A"], p["B"], p["dY"]
+    alpha = 18.0
+    _, Y = oracle.forward(X, W, A, B, alpha)
+    dX, _, _ = oracle.backward(dY, X, W, A, B, alpha)
+    for all_rows in (False, True):
+        S = oracle.Sampled(X, W, A, B, dY, alpha)
+        if all_rows:  # full H and G cached first
+            S.H(), S.G()
+        rows = np.arange(70) if all_rows else np.array([0, 3, 69, 40])
+        np.testing.assert_allclose(S.y_rows_mm(rows), Y[rows], rtol=0,
+                                   atol=1e-13 * np.abs(Y).max())
+        np.testing.assert_allclose(S.dx_rows_mm(rows), dX[rows], rtol=0,
+                                   atol=1e-13 * np.abs(dX).max())
 
 
 def test_empty_batch():
