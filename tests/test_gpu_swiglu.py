@@ -4,13 +4,14 @@
 Metric per output tensor T: max|T_gpu - T_ref| / max|T_ref| <= 1e-2 (bf16).
 The gradients carry one rounding more than the plain layer's: d_gate and
 d_up are bf16 intermediates (from bf16-saved gate and up), and each gradient
-is a dot product over them.  Where that product cancels (one token, rank
-one), a gradient may instead meet the forward error bound of such a product,
-max|T_gpu - T_ref| <= 2^-7 max|T_abs|, T_abs being the same formula on
-absolute values (relative error <= 4 u per term, u = 2^-9).
-Small and ragged shapes are compared element by element; the full gate/up
-workload (Llama-3-8B MLP shape) on sampled token rows of H and dX (dA and dB
-depend on every row and are compared at the smaller sizes only).
+is a dot product over them.  On the one shape where that product cancels
+(one token, rank one: dAg is a single 64-term sum that cancels to 1.85e-2 of
+max|ref|), its gradients may instead meet the forward error bound of such a
+product, max|T_gpu - T_ref| <= 2^-7 max|T_abs|, T_abs being the same formula
+on absolute values (relative error <= 4 u per term, u = 2^-9); every other
+shape meets 1e-2 of max|ref|.  Small and ragged shapes are compared element by
+element; the full gate/up workload (Llama-3-8B MLP shape) on one token row of
+H and dX in every 128-row m-tile and on all four adapter gradients.
 """
 import numpy as np
 import pytest
@@ -73,12 +74,18 @@ def oracle_abs(t, alpha):
 
 
 def meets_bar(got, ref, ref_abs=None):
+    """1e-2 of max|ref|; or, where ref_abs is given (the cancelling shape
+    only), the dot-product error bound 2^-7 max|T_abs|."""
     if isinstance(got, torch.Tensor):
         got = got.detach().double().cpu().numpy()
     err = float(np.abs(got - ref).max())
     if err <= TOL * float(np.abs(ref).max()):
         return True
     return ref_abs is not None and err <= 2.0 ** -7 * float(np.abs(ref_abs).max())
+
+
+# the single shape whose gradients are one cancelling dot product
+CANCELLING = (1, 64, 64, 1, 2.0)
 
 
 NAMES = ("H", "dX", "dAg", "dBg", "dAu", "dBu")
@@ -102,24 +109,31 @@ def test_small_against_oracle(shape):
     t = make_pair(M, d_in, d_ff, r, seed=sum(shape[:4]))
     got = run_gpu(t, alpha)
     ref = oracle_all(t, alpha)
-    bound = (None,) + oracle_abs(t, alpha)
+    bound = (None,) + oracle_abs(t, alpha) if tuple(shape) == CANCELLING else (None,) * 6
     errs = {n: rel_err(g, e) for n, g, e in zip(NAMES, got, ref)}
     for n, g, e, b in zip(NAMES, got, ref, bound):
         assert meets_bar(g, e, b), f"{n}: {errs[n]:.3e} ({errs})"
 
 
-def test_full_gate_up_sampled_rows():
-    # Llama-3-8B MLP gate/up shape: M = 8192 tokens, d_in = 4096, d_ff = 14336, r = 16
+def test_full_gate_up():
+    """Llama-3-8B MLP gate/up shape (M = 8192 tokens, d_in = 4096,
+    d_ff = 14336, r = 16): H and dX on one row of every 128-row m-tile, and
+    all of dAg, dBg, dAu, dBu."""
     M, d_in, d_ff, r, alpha = 8192, 4096, 14336, 16, 32.0
     t = make_pair(M, d_in, d_ff, r, seed=0)
     H, dX, dAg, dBg, dAu, dBu = run_gpu(t, alpha)
-    smp = osw.SampledRows(*(t[k] for k in ("X", "Wg", "Ag", "Bg", "Wu", "Au", "Bu")), t["dH"],
-                          alpha)
-    rows = np.array([0, 1, 127, 128, 4095, 4096, 5000, 8191])
-    assert rel_err(H[rows], smp.h_rows(rows)) <= TOL
-    assert rel_err(dX[rows], smp.dx_rows(rows)) <= TOL
-    for g in (dAg, dBg, dAu, dBu):
-        assert torch.isfinite(g.float()).all()
+    args = [t[k] for k in ("X", "Wg", "Ag", "Bg", "Wu", "Au", "Bu")]
+    smp = osw.SampledRows(*args, t["dH"], alpha)
+    rng = np.random.default_rng(1)
+    rows = np.unique(np.concatenate([[0, M - 1],
+                                     np.arange(0, M, 128) + rng.integers(0, 128, M // 128)]))
+    errs = {"H": rel_err(H[rows], smp.h_rows_mm(rows)),
+            "dX": rel_err(dX[rows], smp.dx_rows_mm(rows))}
+    for name, got, ref in zip(("dAg", "dBg", "dAu", "dBu"), (dAg, dBg, dAu, dBu),
+                              osw.adapter_grads_mm(t["dH"], *args, alpha)):
+        errs[name] = rel_err(got, ref)
+    for k, e in errs.items():
+        assert e <= TOL, f"{k}: {e:.3e} ({errs})"
 
 
 def test_inference_forward_keeps_nothing_and_agrees():
