@@ -155,7 +155,14 @@ lora_status_t lora_linear_bwd(const void *dY, const void *X, const void *W,
  *  - No allocation: it calls no cudaMalloc/cudaFree or allocating routine.
  *  - Set-up: the first call on each device looks up the array's device
  *    address (with that device current) and caches it; make that first call
- *    before any stream capture.
+ *    before any stream capture.  The cached address (like the device status
+ *    word's, cached by every entry point) belongs to the device's primary
+ *    context and does not survive cudaDeviceReset: a process that resets a
+ *    device must not call into this library on it afterwards.
+ *  - Errors: the argument checks of lora_linear_bwd, then the size limit
+ *    below, then the device check that every entry point makes (a device
+ *    this library was not built for gives LORA_ERR_UNSUPPORTED, as from
+ *    lora_linear_bwd), all before the array is looked up.
  *  - Sharing: every call uses the same array.  Calls whose work overlaps on
  *    the GPU (other streams, other host threads) race on it and give wrong
  *    results; order them (one stream, or events).  The array keeps the last

@@ -1172,7 +1172,10 @@ void *g_noalloc_ptr[lora::kMaxDevices] = {};
 
 // Device address of the scratch array on the current device.  The array's
 // name is only a host-side stand-in, so the address is looked up once per
-// device (with that device current) and cached.
+// device (with that device current) and cached.  The cached address belongs
+// to the device's primary context (the one the runtime makes current); like
+// the status-word address of device_info, it does not survive
+// cudaDeviceReset.
 lora_status_t noalloc_scratch(void **out) {
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
@@ -1305,9 +1308,16 @@ lora_status_t lora_linear_bwd_noalloc(const void *dY, const void *X, const void 
                 "lora_linear_bwd_noalloc holds %zu (use lora_linear_bwd with a workspace)",
                 need, static_cast<size_t>(LORA_NOALLOC_SCRATCH_BYTES));
   // Nothing in the scratch has to start at zero: every byte the kernels read
-  // is written earlier in the same call.
+  // is written earlier in the same call (the dX GEMM's tail-split counters
+  // are zeroed by the pass that precedes it).
   void *ws = nullptr;
-  LORA_TRY(noalloc_scratch(&ws));
+  if (!empty) {
+    // the device check of the other entry points comes first, so that a
+    // device this library was not built for gets the same status here
+    DevInfo di;
+    LORA_TRY(device_info(di));
+    LORA_TRY(noalloc_scratch(&ws));
+  }
   return lora_linear_bwd(dY, X, W, A, B, saved, alpha, r, M, d_in, d_out, dtype, dX, dA, dB, ws,
                          LORA_NOALLOC_SCRATCH_BYTES, stream);
 }

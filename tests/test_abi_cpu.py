@@ -120,6 +120,49 @@ def test_bwd_rejects(kw, code):
     assert bwd(**kw) == code
 
 
+def bwd_noalloc(**kw):
+    a = dict(dY=FAKE, X=FAKE, W=FAKE, A=FAKE, B=FAKE, saved=FAKE, alpha=16.0, r=16, M=128,
+             d_in=256, d_out=256, dt=_lib.LORA_BF16, dX=FAKE, dA=FAKE, dB=FAKE)
+    a.update(kw)
+    return L.lora_linear_bwd_noalloc(a["dY"], a["X"], a["W"], a["A"], a["B"], a["saved"],
+                                     a["alpha"], a["r"], a["M"], a["d_in"], a["d_out"], a["dt"],
+                                     a["dX"], a["dA"], a["dB"], None)
+
+
+@pytest.mark.parametrize("kw,code", [
+    (dict(dY=None), _lib.LORA_ERR_INVALID_ARG),
+    (dict(dB=FAKE + 2), _lib.LORA_ERR_INVALID_ARG),
+    (dict(r=300), _lib.LORA_ERR_INVALID_ARG),
+    (dict(d_out=12), _lib.LORA_ERR_UNSUPPORTED),
+    # more scratch than the built-in array holds
+    (dict(M=8200, d_in=64, d_out=16384, r=256), _lib.LORA_ERR_UNSUPPORTED),
+])
+def test_bwd_noalloc_rejects(kw, code):
+    n0 = L.lora_launch_count()
+    assert bwd_noalloc(**kw) == code
+    assert L.lora_launch_count() == n0
+
+
+def _no_device() -> bool:
+    import torch
+    return not torch.cuda.is_available()
+
+
+@pytest.mark.skipif(not _no_device(),
+                    reason="valid arguments with fake pointers: only where no device can run them")
+def test_bwd_noalloc_device_status_is_that_of_bwd():
+    """Valid arguments (fake pointers, so only where no device is usable):
+    the allocation-free backward checks the device the way lora_linear_bwd
+    does, before it looks up its array, so both return the same status and
+    launch nothing."""
+    n0 = L.lora_launch_count()
+    a = bwd()
+    b = bwd_noalloc()
+    assert a == b
+    assert a in (_lib.LORA_ERR_CUDA, _lib.LORA_ERR_UNSUPPORTED)
+    assert L.lora_launch_count() == n0
+
+
 def test_timing_hook_set_and_clear():
     assert L.lora_set_timing_events(None, None, 0) == _lib.LORA_OK
     assert L.lora_timing_used() == 0

@@ -7,11 +7,14 @@ cudaMalloc (which may synchronise the device) once it is running.  For them
 the library has lora_linear_bwd_noalloc, which takes its scratch from an
 array built into the library instead of a caller workspace.
 
-The test makes two calls in a row on different problems -- so the second
-call finds the first call's leftovers in the shared scratch -- and compares
-each result with lora_linear_bwd given its own workspace, within the parity
-tolerance of the other tests.  It also checks that a shape needing more than
-the built-in scratch is refused.  The file name makes pytest collect it last.
+The tests make two calls in a row -- so the second call finds the first
+call's leftovers in the shared scratch -- and compare each result with
+lora_linear_bwd given its own workspace, within the parity tolerance of the
+other tests (bit for bit where both take the same path), and with the fp64
+oracle.  One pair of calls is on a shape whose dX GEMM takes the tail-split
+path inside the array, which keeps per-tile arrival counters there.  A shape
+needing more than the built-in scratch is refused.  The file name makes
+pytest collect it last.
 """
 import numpy as np
 import pytest
@@ -52,6 +55,63 @@ def _rel(got, ref):
     ref = ref.double().cpu().numpy()
     den = np.abs(ref).max()
     return float(np.abs(got - ref).max() / (den if den > 0 else 1.0))
+
+
+# M = d_in = d_out = 4096, r = 16: on a GB300 (76 CTA pairs) the dX GEMM's
+# last wave is split two ways, and its split region fits in the array
+SPLIT_PROBLEM = (4096, 4096, 4096, 16, 16.0)
+
+
+def _rows_per_m_tile(M, seed):
+    rng = np.random.default_rng(seed)
+    return np.unique(np.concatenate([[0, M - 1], np.arange(0, M, 128) +
+                                     rng.integers(0, 128, (M + 127) // 128)]).clip(0, M - 1))
+
+
+def test_split_problem_twice_in_a_row():
+    """Two calls in a row on the problem whose dX GEMM takes the tail-split
+    path (its fp32 partials and arrival counters live in the shared array;
+    the second call finds the first call's counters there).  Each call gives
+    the same bits as lora_linear_bwd with a full workspace -- so the split
+    path ran -- which differ from the unsplit (minimal-workspace) bits, and
+    agrees with the oracle on all of dA and dB and one row of dX per 128-row
+    m-tile."""
+    import oracle
+    M, d_in, d_out, r, alpha = SPLIT_PROBLEM
+    bf = torch.bfloat16
+    need_split = rl.workspace_bytes(M, d_in, d_out, r, bf)
+    saved_room = (rl.saved_bytes(M, r, bf) + 255) // 256 * 256
+    no_split = 3 * ((16 * 4096 * 2 + 255) // 256 * 256)  # B^T, sG, sG^T
+    assert no_split < need_split - saved_room <= SCRATCH_BYTES
+    t = make_inputs(M, d_in, d_out, r, "bf16", seed=41, device=DEV)
+    g = dict(t)
+    full = torch.empty(need_split, dtype=torch.uint8, device=DEV)
+    minimal = torch.empty(no_split, dtype=torch.uint8, device=DEV)
+    _, saved = rl.forward(g["X"], g["W"], g["A"], g["B"], alpha, workspace=full)
+    gen = torch.Generator(device=DEV).manual_seed(42)
+    dYs = [g["dY"], torch.randn(M, d_out, device=DEV, generator=gen).bfloat16()]
+    got = []
+    for dY in dYs:  # back to back, nothing in between
+        got.append(_noalloc_bwd(dict(g, dY=dY), alpha, saved, "bf16"))
+    torch.cuda.synchronize()
+    rl.device_status()
+    host = {k: t[k].cpu() for k in ("X", "W", "A", "B")}
+    for dY, (dX, dA, dB) in zip(dYs, got):
+        ref = rl.backward(dY, g["X"], g["W"], g["A"], g["B"], alpha, saved, workspace=full)
+        unsplit = rl.backward(dY, g["X"], g["W"], g["A"], g["B"], alpha, saved,
+                              workspace=minimal)
+        torch.cuda.synchronize()
+        for a, b in zip((dX, dA, dB), ref):
+            assert torch.equal(a, b)
+            assert _rel(a, b) <= TOL["bf16"]
+        assert not torch.equal(ref[0], unsplit[0])  # the split path gives other bits
+        S = oracle.Sampled(host["X"], host["W"], host["A"], host["B"], dY.cpu(), alpha)
+        rows = _rows_per_m_tile(M, seed=43)
+        for name, a, e in (("dX", dX[rows], S.dx_rows_mm(rows)), ("dA", dA, S.dA()),
+                           ("dB", dB, S.dB())):
+            err = _rel(a, torch.from_numpy(e))
+            assert err <= TOL["bf16"], f"{name}: {err:.3e}"
+    assert not torch.equal(got[0][1], got[1][1])  # the two calls' dA really differ
 
 
 # two different problems, run back to back through the shared scratch
