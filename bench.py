@@ -10,9 +10,13 @@ HBM.  The metric is algorithmic TFLOP/s,
 divided by the device time of the step (CUDA events on the launching stream;
 L2 is flushed by a 256 MiB write before every step, outside the events).
 
-Beside the contract keys the line carries, informationally, the step rated
-against NVIDIA's dense BF16 figure and (plain layer, one GPU) the same step
-run as separate PyTorch ops with autograd ("torch_unfused": as many steps, the
+Beside the contract keys the line carries the median step beside the mean;
+on the default workload (the Llama-3-8B q_proj shape) the other two Llama-3-8B
+shapes of the metric (gate/up, down_proj), each from its own timed region with
+its own clocks and roofline; an end-to-end figure that also copies Y and dX
+out ("e2e_all_outputs"); and, informationally, the step rated against
+NVIDIA's datasheet BF16 figures and (plain layer, one GPU) the same step run
+as separate PyTorch ops with autograd ("torch_unfused": as many steps, the
 same flush, its own record of the SM clock, which decides the comparison on
 power-capped shapes).
 
@@ -44,9 +48,18 @@ METRIC = ("fused LoRA fwd+bwd TFLOP/s on 1 GB300 (Llama-3-8B shapes); "
 DEFAULT_WORKLOAD = "llama3_8b_q_proj"
 FLUSH_BYTES = 256 << 20
 FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
-# NVIDIA's dense (no 2:4 sparsity) BF16 tensor figure for one GB300, reported
-# beside the measured peak
-DATASHEET_BF16_TFLOPS = 2250.0
+# NVIDIA's datasheet BF16 tensor figures, turned into dense (no 2:4 sparsity)
+# figures per GPU, reported beside the measured peak.  The GB300 NVL72
+# datasheet gives 360 PFLOPS FP16/BF16 with sparsity for its 72 GPUs
+# (180 dense / 72 = 2.5 PF each); the HGX B300 datasheet 36 PFLOPS with
+# sparsity for 8 GPUs (18 dense / 8 = 2.25 PF each).  This part is the
+# NVL72's GB300, so its figure is the one the percentage uses.
+DATASHEET_BF16_TFLOPS = {"gb300_nvl72_per_gpu": 2500.0, "hgx_b300_per_gpu": 2250.0}
+DATASHEET_SOURCE = ("NVIDIA GB300 NVL72 datasheet: 360 PFLOPS FP16/BF16 tensor with sparsity "
+                    "for 72 GPUs -> 2.5 PF dense per GPU; NVIDIA HGX B300 datasheet: 36 PFLOPS "
+                    "with sparsity for 8 GPUs -> 2.25 PF dense per GPU")
+# the Llama-3-8B shapes the metric is quoted on, besides the default q_proj one
+OTHER_LLAMA_SHAPES = ("llama3_8b_gate_up", "llama3_8b_down_proj")
 
 
 def step_flops(M, d_in, d_out, r):
@@ -398,27 +411,19 @@ def run_torch_unfused(w, t, dev, stream, steps, flush, gpu_index):
                     "same dtype, same steps, L2 flushed before every step; informational"}
 
 
-def run_ours(args, w):
+def measure(args, w, dev, stream, rank, world, local, steps):
+    """Warm-up, K timed steps (clocks sampled meanwhile) and a second pass of
+    K steps with events around every library launch, for one workload.
+    Returns the step's figures, the per-kernel breakdown and the dominant
+    kernel's roofline; "inputs" holds the drawn tensors."""
     import torch
     import rank_linear_gb300 as rl
     from rank_linear_gb300 import _lib
     from rank_linear_gb300.synth import make_inputs
-
-    rank, world, local = dist_env()
-    if world > 1:
-        import torch.distributed as dist
-        torch.cuda.set_device(local)
-        dist.init_process_group("nccl", device_id=torch.device("cuda", local))
-    dev = torch.device("cuda", local)
-    torch.cuda.set_device(dev)
     L = _lib.lib()
-
     swiglu = w.layer == "swiglu"
     fp8 = w.layer == "fp8"
     q4 = w.layer == "q4"
-    # CPU baseline first (rank 0, N = 1 only), before the GPU is busy
-    cpu = cpu_baseline(w) if (rank == 0 and world == 1 and not args.no_cpu_baseline) else None
-
     M, d_in, d_out, r, alpha = w.M, w.d_in, w.d_out, w.r, w.alpha
     tdt = torch.bfloat16 if w.dtype == "bf16" else torch.float32
     t = make_inputs(M, d_in, d_out, r, w.dtype, seed=rank, device=dev)
@@ -431,7 +436,6 @@ def run_ours(args, w):
     ws = torch.empty(max(1, rl.workspace_bytes(M, d_in, d_out, r, tdt)), dtype=torch.uint8,
                      device=dev)
     flush = torch.empty(FLUSH_BYTES, dtype=torch.uint8, device=dev)
-    stream = torch.cuda.current_stream()
 
     def step():
         rl.forward(X, W, A, B, alpha, Y=Y, saved=saved, workspace=ws, stream=stream)
@@ -483,8 +487,8 @@ def run_ours(args, w):
     step()
     torch.cuda.synchronize()
     launches_per_step = rl.launch_count() - n0
-    s_ev = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
-    e_ev = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+    s_ev = [torch.cuda.Event(enable_timing=True) for _ in range(steps)]
+    e_ev = [torch.cuda.Event(enable_timing=True) for _ in range(steps)]
 
     clocks = ClockSampler(local) if rank == 0 else None
     if clocks:
@@ -497,7 +501,7 @@ def run_ours(args, w):
     torch.cuda.synchronize()
     c0 = rl.launch_count()
     wall0 = time.time()
-    for i in range(args.steps):
+    for i in range(steps):
         flush.zero_()
         s_ev[i].record(stream)
         step()
@@ -510,11 +514,11 @@ def run_ours(args, w):
 
     # Second pass of K steps with an event pair around every launch of the
     # library (per-kernel durations for the breakdown and the roofline).
-    n_pairs = launches_per_step * args.steps
+    n_pairs = launches_per_step * steps
     kev, karr, kinds = rl.timing_events(n_pairs, stream)
     torch.cuda.synchronize()
     _lib.check(L.lora_set_timing_events(karr, kinds, n_pairs), "timing hook")
-    for i in range(args.steps):
+    for i in range(steps):
         flush.zero_()
         step()
     torch.cuda.synchronize()
@@ -525,10 +529,10 @@ def run_ours(args, w):
         time.sleep(0.2)
         clocks.stop()
 
-    step_ms = [s.elapsed_time(e) for s, e in zip(s_ev, e_ev)]
+    step_ms = [a.elapsed_time(b) for a, b in zip(s_ev, e_ev)]
     sec = max_over_ranks(sum(step_ms) / 1e3, world, dev)
+    med_s = max_over_ranks(statistics.median(step_ms) / 1e3, world, dev)
     flops = step_flops(M, d_in, d_out, r) * (2 if swiglu else 1)
-    value = world * flops * args.steps / sec / 1e12
 
     per_kind = {}
     for j in range(used):
@@ -564,35 +568,96 @@ def run_ours(args, w):
     roofline = {"kernel": dom, "bound": BOUND[dom], "achieved": ach, "peak": peak,
                 "unit": unit, "frac": ach / peak, "peak_source": peaks["source"] + peak_note,
                 "traffic": load_traffic(w.name, dom)}
+    return {"value": world * flops * steps / sec / 1e12,
+            "value_median": world * flops / med_s / 1e12,
+            "ms_per_step": 1e3 * sec / steps, "ms_per_step_median": 1e3 * med_s,
+            "launched": launched, "kernels": kern, "roofline": roofline, "clocks": clk,
+            "peaks": peaks, "inputs": t, "dtype": tdt, "flush": flush}
 
-    e2e = None if (args.no_e2e or swiglu or fp8 or q4) else run_e2e(args, w, t, tdt, dev, stream,
-                                                                     world)
+
+def run_ours(args, w):
+    import torch
+    rank, world, local = dist_env()
+    if world > 1:
+        import torch.distributed as dist
+        torch.cuda.set_device(local)
+        dist.init_process_group("nccl", device_id=torch.device("cuda", local))
+    dev = torch.device("cuda", local)
+    torch.cuda.set_device(dev)
+    from rank_linear_gb300 import _lib
+    _lib.lib()
+
+    swiglu = w.layer == "swiglu"
+    fp8 = w.layer == "fp8"
+    q4 = w.layer == "q4"
+    # CPU baseline first (rank 0, N = 1 only), before the GPU is busy
+    cpu = cpu_baseline(w) if (rank == 0 and world == 1 and not args.no_cpu_baseline) else None
+    stream = torch.cuda.current_stream()
+
+    res = measure(args, w, dev, stream, rank, world, local, args.steps)
+    t, tdt = res["inputs"], res["dtype"]
+
+    e2e = e2e_all = None
+    if not (args.no_e2e or swiglu or fp8 or q4):
+        e2e = run_e2e(args, w, t, tdt, dev, stream, world)
+        e2e_all = run_e2e(args, w, t, tdt, dev, stream, world, all_outputs=True)
     unfused = None
     if rank == 0 and world == 1 and not (swiglu or fp8 or q4 or args.no_unfused):
-        unfused = run_torch_unfused(w, t, dev, stream, args.steps, flush, local)
+        unfused = run_torch_unfused(w, t, dev, stream, args.steps, res["flush"], local)
+
+    # The other Llama-3-8B shapes of the metric, each in its own timed region
+    others = None
+    if w.name == DEFAULT_WORKLOAD and not args.no_other_shapes:
+        from rank_linear_gb300.synth import WORKLOADS
+        del t, res["inputs"], res["flush"]
+        torch.cuda.empty_cache()
+        others = {}
+        for name in OTHER_LLAMA_SHAPES:
+            wo = WORKLOADS[name]
+            ro = measure(args, wo, dev, stream, rank, world, local, args.steps)
+            others[name] = {
+                "value": ro["value"], "unit": "TFLOP/s", "ms_per_step": ro["ms_per_step"],
+                "value_median": ro["value_median"],
+                "ms_per_step_median": ro["ms_per_step_median"],
+                "pct_of_bf16_peak": 100.0 * ro["value"] / world / ro["peaks"]["bf16_tflops"],
+                "config": {"M": wo.M, "d_in": wo.d_in, "d_out": wo.d_out, "r": wo.r,
+                           "alpha": wo.alpha},
+                "roofline": ro["roofline"], "kernels": ro["kernels"], "clocks": ro["clocks"],
+                "gpu_launches": ro["launched"], "steps": args.steps}
+            del ro
+            torch.cuda.empty_cache()
 
     if rank == 0:
+        value = res["value"]
+        peaks = res["peaks"]
+        ds = DATASHEET_BF16_TFLOPS["gb300_nvl72_per_gpu"]
         line = {
             "metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": world,
             "steps": args.steps, "warmup": args.warmup,
-            "ms_per_step": 1e3 * sec / args.steps, "higher_is_better": True,
+            "ms_per_step": res["ms_per_step"], "higher_is_better": True,
             "scaling": "weak", "vs_baseline": None,
             "dtype": ("e4m3 W product, bf16 elsewhere" if fp8 else
                       "4-bit W codes expanded to bf16, bf16 elsewhere" if q4 else w.dtype),
             "data": "synthetic",
-            "config": {"workload": w.name, "layer": w.layer, "M": M, "d_in": d_in,
-                       "d_out": d_out, "r": r,
-                       "alpha": alpha, "l2": "flushed before every step (256 MiB write)",
+            "config": {"workload": w.name, "layer": w.layer, "M": w.M, "d_in": w.d_in,
+                       "d_out": w.d_out, "r": w.r,
+                       "alpha": w.alpha, "l2": "flushed before every step (256 MiB write)",
                        "parallelism": "replicas" if world > 1 else "single GPU"},
+            "ms_per_step_median": res["ms_per_step_median"],
+            "value_median": res["value_median"],
             "pct_of_bf16_peak": 100.0 * value / world / peaks["bf16_tflops"],
-            "pct_of_datasheet_bf16_peak": 100.0 * value / world / DATASHEET_BF16_TFLOPS,
-            "datasheet_bf16_tflops": DATASHEET_BF16_TFLOPS,
-            "roofline": roofline, "kernels": kern,
+            "pct_of_datasheet_bf16_peak": 100.0 * value / world / ds,
+            "pct_of_datasheet_bf16_peak_hgx_b300": (
+                100.0 * value / world / DATASHEET_BF16_TFLOPS["hgx_b300_per_gpu"]),
+            "datasheet_bf16_tflops": ds, "datasheet_source": DATASHEET_SOURCE,
+            "roofline": res["roofline"], "kernels": res["kernels"],
             "kernel_timing": "second pass of the same K steps with CUDA events around "
                              "every library launch (on the launching stream)",
-            "cpu_baseline": cpu, "e2e": e2e, "torch_unfused": unfused,
-            "gpu_launches": launched,
-            "clocks": clk,
+            "other_llama3_8b_shapes": others,
+            "cpu_baseline": cpu, "e2e": e2e, "e2e_all_outputs": e2e_all,
+            "torch_unfused": unfused,
+            "gpu_launches": res["launched"],
+            "clocks": res["clocks"],
         }
         print(json.dumps(line), flush=True)
     if world > 1:
@@ -600,13 +665,14 @@ def run_ours(args, w):
         dist.destroy_process_group()
 
 
-def run_e2e(args, w, t, tdt, dev, stream, world):
+def run_e2e(args, w, t, tdt, dev, stream, world, all_outputs=False):
     """Same metric through the public API with pinned host buffers.  Every
     step copies its inputs -- the batch's activations X and the upstream
     gradient dY -- in, and its result -- the gradients dA and dB the
     optimizer takes -- out, inside the timed region.  The frozen W and the
     adapters A, B are model state: uploaded once, before, and kept on the
-    GPU; Y and dX stay on the GPU for the neighbouring layers.  Steps are
+    GPU; Y and dX stay on the GPU for the neighbouring layers, unless
+    all_outputs, when they are copied out every step as well.  Steps are
     pipelined the way a training loop would be: two device buffer sets,
     uploads on one stream, the layer on the launching stream, downloads on a
     third, so that step i+1's upload and step i-1's download overlap step
@@ -618,12 +684,16 @@ def run_e2e(args, w, t, tdt, dev, stream, world):
     h_in = {k: t[k].cpu().pin_memory() for k in per_step}
     state = {k: t[k] for k in ("W", "A", "B")}  # model state, resident on the GPU
     outs = {"dA": (r, d_in), "dB": (d_out, r)}
+    if all_outputs:
+        outs.update(Y=(M, d_out), dX=(M, d_in))
     nbuf = 2
     d_in_t = [{k: torch.empty_like(t[k]) for k in per_step} for _ in range(nbuf)]
-    d_act = [{"Y": torch.empty(M, d_out, dtype=tdt, device=dev),
-              "dX": torch.empty(M, d_in, dtype=tdt, device=dev)} for _ in range(nbuf)]
     d_out_t = [{k: torch.empty(s, dtype=tdt, device=dev) for k, s in outs.items()}
                for _ in range(nbuf)]
+    # Y and dX: among the outputs copied out, or device-only activations
+    d_act = [{k: (d_out_t[b][k] if k in outs else
+                  torch.empty(shape, dtype=tdt, device=dev))
+              for k, shape in (("Y", (M, d_out)), ("dX", (M, d_in)))} for b in range(nbuf)]
     h_out = [{k: torch.empty(s, dtype=tdt).pin_memory() for k, s in outs.items()}
              for _ in range(nbuf)]
     saved = torch.empty(max(1, rl.saved_bytes(M, r, tdt)), dtype=torch.uint8, device=dev)
@@ -681,11 +751,14 @@ def run_e2e(args, w, t, tdt, dev, stream, world):
     bo = sum(v.numel() * v.element_size() for v in h_out[0].values())
     return {"value": world * step_flops(M, d_in, d_out, r) * n / sec / 1e12, "unit": "TFLOP/s",
             "h2d_bytes_per_step": bi, "d2h_bytes_per_step": bo, "steps": n,
-            "inputs": "every step: X and dY copied in, dA and dB copied out (pinned host); "
-                      "W, A, B resident (uploaded once, before); Y and dX stay on the GPU; "
-                      "uploads, kernels and downloads on three streams with two device "
-                      "buffer sets (step i+1's upload and step i-1's download overlap step "
-                      "i's kernels)"}
+            "inputs": ("every step: X and dY copied in, Y, dX, dA and dB copied out "
+                       "(pinned host); " if all_outputs else
+                       "every step: X and dY copied in, dA and dB copied out (pinned host); ")
+                      + "W, A, B resident (uploaded once, before); "
+                      + ("" if all_outputs else "Y and dX stay on the GPU; ")
+                      + "uploads, kernels and downloads on three streams with two device "
+                        "buffer sets (step i+1's upload and step i-1's download overlap step "
+                        "i's kernels)"}
 
 
 def main(argv=None):
@@ -700,6 +773,8 @@ def main(argv=None):
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-unfused", action="store_true",
                     help="skip the informational unfused PyTorch timing")
+    ap.add_argument("--no-other-shapes", action="store_true",
+                    help="default workload only: skip timing the gate/up and down_proj shapes")
     args = ap.parse_args(argv)
     args.warmup = max(args.warmup, 3)  # at least three untimed warm-up steps
     w = WORKLOADS[args.workload]
