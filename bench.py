@@ -87,6 +87,9 @@ def kernel_work(kind, M, d_in, d_out, r, w_bytes=None):
         # s dY B and dY^T sH in one launch; dY counted once
         "down_bwd_grad_b": (4 * M * d_out * r,
                             e * (M * d_out + r * d_out + 2 * M * r + d_out * r)),
+        # dA and dB in one launch after the dX GEMM (X and dY each read once)
+        "grad_a_b": (2 * M * r * (d_in + d_out),
+                     e * (M * d_in + M * d_out + 2 * M * r + r * d_in + d_out * r)),
     }[kind]
 
 
@@ -107,7 +110,8 @@ def kernel_work_swiglu(kind, M, d_in, d_ff, r):
 
 
 BOUND = {"prep": "hbm", "swiglu_grad": "hbm", "quant": "hbm", "down_fwd": "hbm", "down_bwd": "hbm", "grad_a": "hbm",
-         "grad_b": "hbm", "down_bwd_grad_b": "hbm", "main_fwd": "tensor", "main_bwd": "tensor"}
+         "grad_b": "hbm", "down_bwd_grad_b": "hbm", "grad_a_b": "hbm", "main_fwd": "tensor",
+         "main_bwd": "tensor"}
 
 
 def load_peaks():

@@ -202,7 +202,8 @@ typedef enum {
     LORA_K_GRAD_B = 6,    /* dB = dY^T (s X A^T) (skinny split-K)            */
     LORA_K_DOWN_BWD_GRAD_B = 7, /* s dY B and dB in one launch (both read dY) */
     LORA_K_SWIGLU_GRAD = 8,     /* SwiGLU pair: elementwise d_gate, d_up      */
-    LORA_K_QUANT = 9            /* fp8 variant: e4m3 quantisation of X or dY  */
+    LORA_K_QUANT = 9,           /* fp8 variant: e4m3 quantisation of X or dY  */
+    LORA_K_GRAD_A_B = 10        /* dA and dB in one launch, after the dX GEMM */
 } lora_kernel_kind_t;
 
 /*
@@ -220,9 +221,9 @@ int lora_timing_used(void);
 /*
  * Test hook for the bounded device-side waits (the pages have no
  * counterpart; it exists so that the timeout path can be exercised without
- * faulting or hanging a GPU).  The next n bf16 backward dA passes (the last
- * launch of lora_linear_bwd) launched by this process (any thread) leave
- * the first pipeline stage of their first CTA unfilled.  That CTA's MMA
+ * faulting or hanging a GPU).  The next n bf16 backward dA-and-dB passes
+ * (the last launch of lora_linear_bwd) launched by this process (any
+ * thread) leave the first pipeline stage of their first dA CTA unfilled.  That CTA's MMA
  * wait then runs out after the wait limit (about 2 s), the kernel leaves
  * through its abort path (no fault, no hang), the caller's next
  * lora_device_status() returns LORA_ERR_TIMEOUT, and dA of that call is
@@ -230,6 +231,19 @@ int lora_timing_used(void);
  * LORA_ERR_INVALID_ARG for n < 0.
  */
 lora_status_t lora_debug_withhold_arrive(int n);
+
+/*
+ * Test hook of the main GEMMs' tile width (the pages have no counterpart).
+ * The plain bf16 layer's two GEMMs run 256 x 512 or 256 x 256 pair tiles
+ * (the latter with the split of a short last wave), chosen per shape by a
+ * cost model of the waves.  width = 256 or 512 forces that width for every
+ * later call in this process (512 only where it is built: not for the
+ * 4-bit, fp8 or SwiGLU GEMMs); 0 restores the cost model.  Results differ
+ * between widths only by the rounding order of the split tiles.  Workspace
+ * sizes do not depend on it.  Returns LORA_ERR_INVALID_ARG for any other
+ * width.
+ */
+lora_status_t lora_debug_gemm_width(int width);
 
 #ifdef __cplusplus
 }

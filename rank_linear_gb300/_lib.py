@@ -16,7 +16,7 @@ LORA_OK, LORA_ERR_INVALID_ARG, LORA_ERR_UNSUPPORTED, LORA_ERR_WORKSPACE, \
     LORA_ERR_CUDA, LORA_ERR_TIMEOUT = range(6)
 LORA_BF16, LORA_FP32 = 0, 1
 KERNEL_KINDS = ["prep", "down_fwd", "main_fwd", "down_bwd", "main_bwd", "grad_a", "grad_b",
-                "down_bwd_grad_b", "swiglu_grad", "quant"]
+                "down_bwd_grad_b", "swiglu_grad", "quant", "grad_a_b"]
 
 _vp, _i64, _sz = ctypes.c_void_p, ctypes.c_int64, ctypes.c_size_t
 _int, _f32 = ctypes.c_int, ctypes.c_float
@@ -36,6 +36,7 @@ SIGNATURES = {
     "lora_launch_count": ([], ctypes.c_uint64),
     "lora_set_timing_events": ([ctypes.POINTER(_vp), ctypes.POINTER(_int), _int], _int),
     "lora_debug_withhold_arrive": ([_int], _int),
+    "lora_debug_gemm_width": ([_int], _int),
     "lora_timing_used": ([], _int),
     "lora_fp8_quantize_w_workspace_bytes": ([], _sz),
     "lora_fp8_quantize_w": ([_vp, _i64, _i64, _vp, _vp, _vp, _vp, _sz, _vp], _int),

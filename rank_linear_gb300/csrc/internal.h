@@ -56,6 +56,9 @@ struct MainGemmArgs {
   // 64 x 2).  Each CTA dequantises its half of the B tile to bf16 in shared
   // memory before the MMAs read it.
   bool q4 = false;
+  // 256 x 512 pair tiles (two N = 256 MMAs per K step sharing A; plain bf16
+  // layer only, no tail split); from main_gemm_plan
+  bool wide = false;
 };
 constexpr int kMainBM = 128, kMainBK = 64;
 int main_gemm_pick_bn(int M, int N, int num_sms);
@@ -64,11 +67,19 @@ int main_gemm_pairs(bool b_mn, int num_sms);
 struct MainSplit {
   int k = 1, rem = 0;
   size_t partial_bytes = 0, counter_bytes = 0;
+  bool wide = false;  // 256 x 512 tiles (never split)
 };
 // Tail split for an M x N output on `pairs` CTA pairs: the last wave's rem
 // tiles are split two ways (K ranges) when 2 * rem <= pairs.  For the gated
 // pair pass N = 2 x roundup(output columns, 128) (tiles of 128 columns).
 MainSplit main_gemm_split(int M, int N, int pairs);
+// The plain layer's choice between 256 x 512 tiles and 256 x 256 tiles with
+// the tail split, by a cost model of the waves (allow_wide false: the
+// latter only, as main_gemm_split).
+MainSplit main_gemm_plan(int M, int N, int pairs, bool allow_wide);
+// Test hook: 0 = choose by the cost model, 256 or 512 = that width only
+// (512 where allowed).
+void main_gemm_force_width(int w);
 cudaError_t launch_main_gemm(const MainGemmArgs &a, int num_sms, cudaStream_t s);
 
 // ---- skinny tensor-core pass with cluster split-K -------------------------
@@ -109,7 +120,14 @@ struct SkinnyArgs {
   // GEMM frees; the last cluster waits before it leaves, so the launch still
   // ends after the GEMM.  Not allowed with zero_ptr.
   int after_gemm = 0;
+  // This pass feeds a main GEMM launched right after it, which needs its
+  // result only at the end of each tile: when one CTA per 128 rows makes at
+  // most kSkinnyFeedMaxCtas CTAs, run that way (no K split, no cluster), so
+  // that the GEMM's CTA pairs start on the other SMs at once instead of
+  // waiting for this pass to leave them.
+  int feeds_gemm = 0;
 };
+constexpr int kSkinnyFeedMaxCtas = 64;
 // Runs one or two independent problems in one launch.
 cudaError_t launch_skinny(const SkinnyArgs *probs, int nprob, int num_sms, cudaStream_t s);
 int skinny_split(int rows, int K, int num_sms);

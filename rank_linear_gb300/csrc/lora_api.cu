@@ -198,7 +198,10 @@ struct Plan {
 };
 
 // pairs: CTA pairs of the main GEMM on the target device (0: no tail split).
-Plan make_plan(int64_t M, int64_t d_in, int64_t d_out, int r, lora_dtype_t dt, int pairs = 0) {
+// allow_wide: the GEMMs may take 256 x 512 tiles (the plain bf16 layer; the
+// 4-bit layer's dequantising GEMM has 256-wide tiles only).
+Plan make_plan(int64_t M, int64_t d_in, int64_t d_out, int r, lora_dtype_t dt, int pairs = 0,
+               bool allow_wide = false) {
   Plan P;
   if (dt == LORA_BF16) {
     P.r_pad = static_cast<int>(rup(r, 16));
@@ -209,7 +212,7 @@ Plan make_plan(int64_t M, int64_t d_in, int64_t d_out, int r, lora_dtype_t dt, i
     // forward: [B padded (r % 8 != 0)] [split partials] [split counters]
     size_t off = (r % 8) ? rup(size_t(d_out) * P.r_pad * 2, 256) : 0;
     P.fwd_ws_min = off;
-    if (pairs > 0 && M > 0) P.fsplit = main_gemm_split(int(M), int(d_out), pairs);
+    if (pairs > 0 && M > 0) P.fsplit = main_gemm_plan(int(M), int(d_out), pairs, allow_wide);
     P.fsplit_off = off;
     off += rup(P.fsplit.partial_bytes, 256);
     P.fcnt_off = off;
@@ -224,7 +227,7 @@ Plan make_plan(int64_t M, int64_t d_in, int64_t d_out, int r, lora_dtype_t dt, i
     P.sgt_off = off;
     off += rup(size_t(P.r_pad) * P.Mp * 2, 256);
     const size_t base_end = off;
-    if (pairs > 0 && M > 0) P.bsplit = main_gemm_split(int(M), int(d_in), pairs);
+    if (pairs > 0 && M > 0) P.bsplit = main_gemm_plan(int(M), int(d_in), pairs, allow_wide);
     P.bsplit_off = off;
     off += rup(P.bsplit.partial_bytes, 256);
     P.bcnt_off = off;
@@ -295,10 +298,13 @@ uint8_t *at(void *base, size_t off) { return static_cast<uint8_t *>(base) + off;
 
 // ---------------------------------------------------------------- bf16 path
 // sH = s X A^T into saved (row-major [M][r_pad]) and its transpose.
+// feeds_gemm: the forward GEMM follows and may start beside this pass.
 lora_status_t down_fwd_bf16(const DevInfo &di, const Plan &P, const void *X, const void *A,
                             float s, int r, int64_t M, int64_t d_in, void *saved,
-                            cudaStream_t st, unsigned *zero_ptr = nullptr, int zero_words = 0) {
+                            cudaStream_t st, unsigned *zero_ptr = nullptr, int zero_words = 0,
+                            bool feeds_gemm = false) {
   SkinnyArgs f1;
+  f1.feeds_gemm = feeds_gemm ? 1 : 0;
   f1.zero_ptr = zero_ptr;
   f1.zero_words = zero_words;
   LORA_TRY(tmap(&f1.tmA, X, d_in, M, d_in * 2, 64, 128, "X"));
@@ -323,7 +329,8 @@ lora_status_t fwd_bf16(const void *X, const void *W, const void *A, const void *
                        void *ws, size_t ws_bytes, cudaStream_t st, const Q4W *q4 = nullptr) {
   DevInfo di;
   LORA_TRY(device_info(di));
-  Plan P = make_plan(M, d_in, d_out, r, LORA_BF16, main_gemm_pairs(false, di.sms));
+  Plan P = make_plan(M, d_in, d_out, r, LORA_BF16, main_gemm_pairs(false, di.sms), q4 == nullptr);
+  const bool wide = P.fsplit.wide;
   const bool split = P.fsplit.k > 1 && ws != nullptr && ws_bytes >= P.fwd_ws;
   if (!split) P = make_plan(M, d_in, d_out, r, LORA_BF16);  // layout without the split region
   unsigned *counters = split ? reinterpret_cast<unsigned *>(at(ws, P.fcnt_off)) : nullptr;
@@ -339,7 +346,7 @@ lora_status_t fwd_bf16(const void *X, const void *W, const void *A, const void *
     b_inner = P.r_pad;
   }
   LORA_TRY(down_fwd_bf16(di, P, X, A, s, r, M, d_in, saved, st, counters,
-                         split ? 2 * P.fsplit.rem : 0));
+                         split ? 2 * P.fsplit.rem : 0, true));
   MainGemmArgs f2;
   if (split) {
     f2.split_k = P.fsplit.k;
@@ -367,6 +374,7 @@ lora_status_t fwd_bf16(const void *X, const void *W, const void *A, const void *
   f2.out = Y;
   f2.ldo = d_out;
   f2.b_mn = false;
+  f2.wide = wide;
   f2.dev_status = di.status;
   return run(LORA_K_MAIN_FWD, st, "forward GEMM", [&] { return launch_main_gemm(f2, di.sms, st); });
 }
@@ -377,7 +385,8 @@ lora_status_t bwd_bf16(const void *dY, const void *X, const void *W, const void 
                        cudaStream_t st, const Q4W *q4 = nullptr) {
   DevInfo di;
   LORA_TRY(device_info(di));
-  Plan P = make_plan(M, d_in, d_out, r, LORA_BF16, main_gemm_pairs(true, di.sms));
+  Plan P = make_plan(M, d_in, d_out, r, LORA_BF16, main_gemm_pairs(true, di.sms), q4 == nullptr);
+  const bool wide = P.bsplit.wide;
   // tail split of the dX GEMM only if the workspace holds its region (it sits
   // before the recompute room, so a saved buffer lets a shorter one suffice)
   const bool split = dX != nullptr && P.bsplit.k > 1 && ws != nullptr &&
@@ -386,15 +395,20 @@ lora_status_t bwd_bf16(const void *dY, const void *X, const void *W, const void 
   unsigned *counters = split ? reinterpret_cast<unsigned *>(at(ws, P.bcnt_off)) : nullptr;
   const float s = alpha / static_cast<float>(r);
   if (saved == nullptr) {  // recompute s X A^T into the workspace
+    // with the forward's launch shape, so that the bits are the forward's
     void *re = at(ws, P.resaved_off);
-    LORA_TRY(down_fwd_bf16(di, P, X, A, s, r, M, d_in, re, st));
+    LORA_TRY(down_fwd_bf16(di, P, X, A, s, r, M, d_in, re, st, nullptr, 0, true));
     saved = re;
   }
   const void *sHt = static_cast<const uint8_t *>(saved) + P.sHt_off;
   void *sG = at(ws, P.sg_off);
   void *sGt = at(ws, P.sgt_off);
 
-  // sG = s dY B (and its transpose), and dB = dY^T sH: one launch, both read dY
+  // sG = s dY B (and its transpose) alone; it feeds the dX GEMM (on few
+  // SMs, beside the GEMM's start).  dB = dY^T sH runs after the GEMM
+  // together with dA, on the SMs the GEMM's last wave leaves idle.  The
+  // launches are the same without dX (no GEMM between them), so dA and dB
+  // are the same bits either way (each launch's split of K is its own).
   SkinnyArgs g[2];
   SkinnyArgs &b1 = g[0];
   LORA_TRY(tmap(&b1.tmA, dY, d_out, M, d_out * 2, 64, 128, "dY"));
@@ -436,8 +450,9 @@ lora_status_t bwd_bf16(const void *dY, const void *X, const void *W, const void 
   b4.ld0 = r;
   b4.n0 = r;
   b4.dev_status = di.status;
-  LORA_TRY(run(LORA_K_DOWN_BWD_GRAD_B, st, "s dY B and dB pass",
-               [&] { return launch_skinny(g, 2, di.sms, st); }));
+  b1.feeds_gemm = 1;
+  LORA_TRY(run(LORA_K_DOWN_BWD, st, "s dY B pass",
+               [&] { return launch_skinny(&b1, 1, di.sms, st); }));
 
   // dX = [dY | sG] . [W ; A]
   if (dX != nullptr) {
@@ -462,6 +477,7 @@ lora_status_t bwd_bf16(const void *dY, const void *X, const void *W, const void 
     b2.out = dX;
     b2.ldo = d_in;
     b2.b_mn = true;
+    b2.wide = wide;
     b2.dev_status = di.status;
     if (split) {
       b2.split_k = P.bsplit.k;
@@ -490,7 +506,11 @@ lora_status_t bwd_bf16(const void *dY, const void *X, const void *W, const void 
   while (pending > 0 && !g_withhold.compare_exchange_weak(pending, pending - 1)) {
   }
   b3.withhold_first_stage = pending > 0 ? 1 : 0;
-  return run(LORA_K_GRAD_A, st, "dA pass", [&] { return launch_skinny(&b3, 1, di.sms, st); });
+  // dA and dB in one launch (dA first: the test hook's problem)
+  b4.after_gemm = b3.after_gemm;
+  SkinnyArgs ab[2] = {b3, b4};
+  return run(LORA_K_GRAD_A_B, st, "dA and dB pass",
+             [&] { return launch_skinny(ab, 2, di.sms, st); });
 }
 
 // ---------------------------------------------------------------- fp32 path
@@ -1682,6 +1702,14 @@ lora_status_t lora_q4_bwd(const void *dY, const void *X, const void *codes, cons
   q4.scales = scales;
   return bwd_bf16(dY, X, nullptr, A, B, saved, alpha, r, M, d_in, d_out, dX, dA, dB, workspace,
                   workspace_bytes, st, &q4);
+}
+
+lora_status_t lora_debug_gemm_width(int width) {
+  t_err.clear();
+  if (width != 0 && width != 256 && width != 512)
+    return fail(LORA_ERR_INVALID_ARG, "width %d is not 0, 256 or 512", width);
+  main_gemm_force_width(width);
+  return LORA_OK;
 }
 
 lora_status_t lora_debug_withhold_arrive(int n) {

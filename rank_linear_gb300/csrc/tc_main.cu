@@ -41,8 +41,18 @@
 //          in the epilogue;
 //   Q4     a 4-bit W: each stage carries packed codes and bf16 group scales,
 //          and six groups of two extra warps (one per ring stage) expand
-//          them into the bf16 B tile in shared memory.
+//          them into the bf16 B tile in shared memory;
+//   WIDE   256 x 512 pair tiles for the plain layer: each K step issues two
+//          N = 256 pair MMAs that share the stage's A tile, into the two
+//          256-column halves of TMEM (one accumulator, no double buffer).
+//          Per SM a K block then moves A 16 KB + B 32 KB for 1024 MMA cycles
+//          (48 B/clock) instead of 32 KB for 512 (64 B/clock, above the
+//          ~58 B/clock the TMA feed sustains).  Eight epilogue warps drain
+//          half 0 first, so the next tile's half-0 MMAs start while half 1
+//          is still being written out.
 #include <cuda_bf16.h>
+
+#include <atomic>
 
 #include "internal.h"
 #include "ptx.cuh"
@@ -55,6 +65,7 @@ constexpr int CLUSTER = 2;                   // the CTA pair
 constexpr uint16_t PAIR_MASK = 0x3;
 constexpr uint32_t A_BYTES = BM * BK * 2;    // 16 KB: this CTA's 128 rows of A
 constexpr int NUM_THREADS = 192;             // producer warp, MMA warp, 4 epilogue warps
+constexpr int WIDE_THREADS = 320;            // producer warp, MMA warp, 8 epilogue warps
 // 4-bit W: warps expanding codes to bf16, one group of them per ring stage
 // (a stage is 128 lines of 64 weights)
 constexpr int DQ_GROUP_WARPS = 2;
@@ -74,13 +85,17 @@ constexpr uint32_t RAW_CODE_BYTES = 4096, RAW_BYTES = RAW_CODE_BYTES + 256;
 constexpr int GROUP_M_MIN = 8, GROUP_M_MAX = 16;
 constexpr int64_t kGroupABytes = 60ll << 20;
 constexpr int EPI_ARRIVALS = 4 * CLUSTER;    // epilogue warps of both CTAs
+constexpr int WIDE_EPI_ARRIVALS = 8 * CLUSTER;  // wide tiles: per accumulator half
 constexpr size_t kStageBudget = 192 * 1024;  // shared memory for the stage ring
 
-// Tile geometry for a pair tile of 256 x BN (BN = 128 or 256); Q4 adds the
-// raw 4-bit codes and scales of a stage.
-template <int BN, bool Q4 = false>
+// Tile geometry for a pair tile of 256 x BN (BN = 128 or 256), or 256 x 2 BN
+// (WIDE: two MMAs of width BN per K step); Q4 adds the raw 4-bit codes and
+// scales of a stage.
+template <int BN, bool Q4 = false, bool WIDE = false>
 struct Geo {
-  static constexpr uint32_t B_BYTES = BN / 2 * BK * 2;  // this CTA's half of B
+  static constexpr int HALVES = WIDE ? 2 : 1;           // MMAs per K step
+  static constexpr uint32_t B_HALF = BN / 2 * BK * 2;   // this CTA's share of one MMA's B
+  static constexpr uint32_t B_BYTES = HALVES * B_HALF;
   static constexpr uint32_t STAGE_BYTES = A_BYTES + B_BYTES + (Q4 ? RAW_BYTES : 0);
   // bytes a stage's pair-TMA loads bring to the even CTA's barrier
   static constexpr uint32_t PAIR_TX = CLUSTER * (A_BYTES + B_BYTES);
@@ -88,7 +103,8 @@ struct Geo {
   // 4-bit W: six stages (its chain from load to MMA is longer), in the room
   // the shared-memory limit leaves
   static constexpr int STAGES = Q4 ? 6 : (STAGES_RAW > 8 ? 8 : STAGES_RAW);
-  static constexpr uint32_t TMEM_COLS = 2 * BN;  // two accumulators
+  static constexpr uint32_t TMEM_COLS = 2 * BN;  // two accumulators, or one wide one
+  static constexpr int EPI_WARPS = WIDE ? 8 : 4;
 };
 
 // One dequantising group per stage of the 4-bit ring, so that each group
@@ -121,15 +137,17 @@ struct __align__(16) MainTail {
 // all 32 banks.
 constexpr uint32_t EPI_PITCH = 64;
 constexpr uint32_t EPI_WARP_BYTES = 32 * EPI_PITCH;
-constexpr uint32_t EPI_BYTES = 4 * EPI_WARP_BYTES;
 
-template <int BN, bool Q4 = false>
+template <int BN, bool Q4 = false, bool WIDE = false>
 constexpr size_t smem_bytes() {
-  return 1024 + size_t(Geo<BN, Q4>::STAGES) * Geo<BN, Q4>::STAGE_BYTES + EPI_BYTES +
-         sizeof(MainTail<Geo<BN, Q4>::STAGES>);
+  using G = Geo<BN, Q4, WIDE>;
+  return 1024 + size_t(G::STAGES) * G::STAGE_BYTES + G::EPI_WARPS * EPI_WARP_BYTES +
+         sizeof(MainTail<G::STAGES>);
 }
-static_assert(smem_bytes<256, true>() <= 227 * 1024 && smem_bytes<256>() <= 227 * 1024,
+static_assert(smem_bytes<256, true>() <= 227 * 1024 && smem_bytes<256>() <= 227 * 1024 &&
+                  smem_bytes<256, false, true>() <= 227 * 1024,
               "shared memory per CTA");
+static_assert(Geo<256, false, true>::STAGES == 4, "wide ring: four 48 KB stages");
 
 // Work item -> tile and K-block range.  Items below split_first are whole
 // tiles; the rest are range `chunk` of split tile `rel` (tile split_first+rel).
@@ -247,8 +265,8 @@ __device__ __forceinline__ void store_gated(const float (&g)[32], const float (&
   store_chunk(pk, stage, lane, out, ldo, row0, col0, M, N);
 }
 
-template <bool B_MN, int BN, bool SPLIT, bool GATED, bool DUAL_B, bool FP8, bool Q4>
-__global__ void __launch_bounds__(Q4 ? Q4_THREADS : NUM_THREADS, 1)
+template <bool B_MN, int BN, bool SPLIT, bool GATED, bool DUAL_B, bool FP8, bool Q4, bool WIDE>
+__global__ void __launch_bounds__(Q4 ? Q4_THREADS : WIDE ? WIDE_THREADS : NUM_THREADS, 1)
     k_main_gemm(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                 const __grid_constant__ CUtensorMap tmA2, const __grid_constant__ CUtensorMap tmB2,
                 const __grid_constant__ CUtensorMap tmB3, const __grid_constant__ CUtensorMap tmB4,
@@ -260,16 +278,19 @@ __global__ void __launch_bounds__(Q4 ? Q4_THREADS : NUM_THREADS, 1)
   static_assert(!(GATED && B_MN), "the gated pair reads K-major B");
   static_assert(!(FP8 && (B_MN || GATED || DUAL_B)), "the fp8 product reads K-major operands");
   static_assert(!(Q4 && (GATED || DUAL_B || FP8)), "4-bit W: plain layer only");
-  constexpr int TN = GATED ? BN / 2 : BN;  // output columns per pair tile
-  using G = Geo<BN, Q4>;
+  static_assert(!(WIDE && (SPLIT || GATED || DUAL_B || FP8 || Q4)), "wide tiles: plain layer, no split");
+  // output columns per pair tile
+  constexpr int TN = GATED ? BN / 2 : WIDE ? 2 * BN : BN;
+  using G = Geo<BN, Q4, WIDE>;
   constexpr int STAGES = G::STAGES;
   constexpr uint32_t B_BYTES = G::B_BYTES, STAGE_BYTES = G::STAGE_BYTES, PAIR_TX = G::PAIR_TX;
+  constexpr uint32_t B_HALF = G::B_HALF;
   constexpr uint32_t TMEM_COLS = G::TMEM_COLS;
   extern __shared__ uint8_t smem_raw[];
   const uint32_t raw = smem_u32(smem_raw);
   const uint32_t base = (raw + 1023u) & ~1023u;  // 128-B swizzle atoms need 1 KB alignment
   uint8_t *epi_stage = smem_raw + (base - raw) + STAGES * STAGE_BYTES;
-  auto *tail = reinterpret_cast<MainTail<STAGES> *>(epi_stage + EPI_BYTES);
+  auto *tail = reinterpret_cast<MainTail<STAGES> *>(epi_stage + G::EPI_WARPS * EPI_WARP_BYTES);
   const uint32_t sA = base;
   const uint32_t sB = base + STAGES * A_BYTES;
   const uint32_t sRaw = sB + STAGES * B_BYTES;  // 4-bit W: codes and scales per stage
@@ -302,8 +323,10 @@ __global__ void __launch_bounds__(Q4 ? Q4_THREADS : NUM_THREADS, 1)
       mbar_init(smem_u32(&tail->empty[s]), 1);  // the even CTA's multicast commit
     }
     for (int a = 0; a < 2; ++a) {
+      // wide: tfull[0] marks the accumulator complete, tempty[h] its half h
+      // drained
       mbar_init(smem_u32(&tail->tfull[a]), 1);
-      mbar_init(smem_u32(&tail->tempty[a]), EPI_ARRIVALS);
+      mbar_init(smem_u32(&tail->tempty[a]), WIDE ? WIDE_EPI_ARRIVALS : EPI_ARRIVALS);
     }
     mbar_init(smem_u32(&tail->drain), 1);
     mbar_init(smem_u32(&tail->ebar), 4);
@@ -355,9 +378,10 @@ __global__ void __launch_bounds__(Q4 ? Q4_THREADS : NUM_THREADS, 1)
         int mp, nb;
         tile_coords(tile, m_pairs, n_tiles, group_m, mp, nb);
         const int m0 = (2 * mp + q) * BM;
-        // this CTA's half of the B tile: columns q*BN/2.. of the tile, or for
-        // the gated pair the same TN rows of its own projection
-        const int n0 = GATED ? nb * TN : nb * BN + q * (BN / 2);
+        // this CTA's half of the B tile: columns q*BN/2.. of the tile (of
+        // each of its two BN-wide halves, wide), or for the gated pair the
+        // same TN rows of its own projection
+        const int n0 = GATED ? nb * TN : nb * TN + q * (BN / 2);
         for (int kb = kb_lo; kb < kb_hi; ++kb) {
           if (!mbar_wait(smem_u32(&tail->empty[stage]), phase ^ 1u, abort_flag, dev_status)) {
             ok = false;
@@ -424,12 +448,16 @@ __global__ void __launch_bounds__(Q4 ? Q4_THREADS : NUM_THREADS, 1)
             }
           }
           tma_load_2d_pair(sA + stage * A_BYTES, ta, full, k0, m0);
-          if (B_MN) {  // BN/128 boxes of [64 K x 64 N]
 #pragma unroll
-            for (int j = 0; j < BN / 128; ++j)
-              tma_load_2d_pair(sB + stage * B_BYTES + j * 8192u, tb, full, n0 + 64 * j, kB);
-          } else {  // BN/2 rows of [N x 64 K]
-            tma_load_2d_pair(sB + stage * B_BYTES, tb, full, kB, n0);
+          for (int h = 0; h < G::HALVES; ++h) {  // wide: half h is BN columns further
+            const uint32_t b_dst = sB + stage * B_BYTES + h * B_HALF;
+            if (B_MN) {  // BN/128 boxes of [64 K x 64 N]
+#pragma unroll
+              for (int j = 0; j < BN / 128; ++j)
+                tma_load_2d_pair(b_dst + j * 8192u, tb, full, n0 + h * BN + 64 * j, kB);
+            } else {  // BN/2 rows of [N x 64 K]
+              tma_load_2d_pair(b_dst, tb, full, kB, n0 + h * BN);
+            }
           }
           issued[stage] += 1;
           if (++stage == STAGES) {
@@ -491,14 +519,17 @@ __global__ void __launch_bounds__(Q4 ? Q4_THREADS : NUM_THREADS, 1)
       for (int item = pair_id; item < num_items && ok; item += num_pairs, ++t) {
         int tile, kb_lo, kb_hi, chunk, rel;
         item_range(item, split_first, split_k, split_rem, kb_total, tile, kb_lo, kb_hi, chunk, rel);
-        const int acc = t & 1;
-        const uint32_t use = static_cast<uint32_t>(t >> 1);
+        // wide: one accumulator (both TMEM halves), its half h free once
+        // tempty[h] completes; half 1 is awaited just before its first MMA
+        const int acc = WIDE ? 0 : (t & 1);
+        const uint32_t use = static_cast<uint32_t>(WIDE ? t : (t >> 1));
         if (!mbar_wait(smem_u32(&tail->tempty[acc]), (use & 1u) ^ 1u, abort_flag, dev_status)) {
           ok = false;
           break;
         }
         tc_fence_after();
         const uint32_t d = tmem_base + acc * BN;
+        bool half1_free = !WIDE;
         // Descriptors of the current stage, advanced by addition: the
         // start-address field is the low 14 bits (address / 16) and every
         // stage lies below 256 KB, so the sums never carry out of it.
@@ -516,6 +547,7 @@ __global__ void __launch_bounds__(Q4 ? Q4_THREADS : NUM_THREADS, 1)
             break;
           }
           tc_fence_after();
+          const int nk = kb < kb_main ? BK / 16 : min(BK / 16, (k_ext - (kb - kb_main) * BK) / 16);
           if (kb < kb_main) {
             // fp8: four K = 32 steps of 32 bytes each, like bf16's K = 16
 #pragma unroll
@@ -526,9 +558,30 @@ __global__ void __launch_bounds__(Q4 ? Q4_THREADS : NUM_THREADS, 1)
                 tc_mma_bf16_pair(d, ad + kk * A_STEP, bd + kk * B_STEP, idesc, kk ? 1u : accum);
             }
           } else {
-            const int nk = min(BK / 16, (k_ext - (kb - kb_main) * BK) / 16);
             for (int kk = 0; kk < nk; ++kk)
               tc_mma_bf16_pair(d, ad + kk * A_STEP, bd + kk * B_STEP, idesc, kk ? 1u : accum);
+          }
+          if constexpr (WIDE) {  // the same A tile against the second half of B
+            if (!half1_free) {
+              if (!mbar_wait(smem_u32(&tail->tempty[1]), (use & 1u) ^ 1u, abort_flag,
+                             dev_status)) {
+                ok = false;
+                break;
+              }
+              tc_fence_after();
+              half1_free = true;
+            }
+            const uint64_t bd1 = bd + (B_HALF >> 4);
+            if (kb < kb_main) {
+#pragma unroll
+              for (int kk = 0; kk < BK / 16; ++kk)
+                tc_mma_bf16_pair(d + BN, ad + kk * A_STEP, bd1 + kk * B_STEP, idesc,
+                                 kk ? 1u : accum);
+            } else {
+              for (int kk = 0; kk < nk; ++kk)
+                tc_mma_bf16_pair(d + BN, ad + kk * A_STEP, bd1 + kk * B_STEP, idesc,
+                                 kk ? 1u : accum);
+            }
           }
           accum = 1u;
           tc_commit_pair_mc(smem_u32(&tail->empty[stage]), PAIR_MASK);  // free in both CTAs
@@ -648,8 +701,8 @@ __global__ void __launch_bounds__(Q4 ? Q4_THREADS : NUM_THREADS, 1)
       int tile, kb_lo, kb_hi, chunk, rel;
       item_range(item, split_first, split_k, split_rem, kb_total, tile, kb_lo, kb_hi, chunk, rel);
       const bool split = SPLIT && item >= split_first;
-      const int acc = t & 1;
-      const uint32_t use = static_cast<uint32_t>(t >> 1);
+      const int acc = WIDE ? 0 : (t & 1);
+      const uint32_t use = static_cast<uint32_t>(WIDE ? t : (t >> 1));
       int mp, nb;
       tile_coords(tile, m_pairs, n_tiles, group_m, mp, nb);
       const bool got = mbar_wait(smem_u32(&tail->tfull[acc]), use & 1u, abort_flag, dev_status);
@@ -663,6 +716,32 @@ __global__ void __launch_bounds__(Q4 ? Q4_THREADS : NUM_THREADS, 1)
       if constexpr (FP8) {
         const int row = row0 + lane;
         sc = (row < M ? __ldg(row_scale + row) : 0.f) * (w_scale != nullptr ? __ldg(w_scale) : 1.f);
+      }
+      if constexpr (WIDE) {
+        // Eight warps: warp w drains its lane quadrant's rows, columns
+        // [h*BN + p*BN/2, +BN/2) of half h (p = which of the two warps of
+        // the quadrant), half 0 first; each half is released to the MMA
+        // issuer as soon as all sixteen warps of the pair have drained it.
+        const int ew = warp - 2;
+        const int cpart = ew >> 2;
+        uint8_t *wstage = epi_stage + ew * EPI_WARP_BYTES;
+#pragma unroll 1
+        for (int h = 0; h < 2; ++h) {
+#pragma unroll 1
+          for (int c = 0; c < BN / 64; ++c) {
+            const int col = h * BN + cpart * (BN / 2) + c * 32;
+            float v[32];
+            tmem_ld_32cols(taddr + col, v);
+            uint32_t pk[16];
+#pragma unroll
+            for (int i = 0; i < 16; ++i) pk[i] = pack_bf16x2(v[2 * i], v[2 * i + 1]);
+            store_chunk(pk, wstage, lane, out, ldo, row0, nb * TN + col, M, N);
+          }
+          tc_fence_before();
+          __syncwarp();
+          if (lane == 0) mbar_arrive_cluster(dsmem_map(smem_u32(&tail->tempty[h]), 0));
+        }
+        continue;
       }
       if (!SPLIT || !split) {
         if constexpr (GATED) {  // columns [0, TN) gate, [TN, 2 TN) up
@@ -801,26 +880,26 @@ __global__ void __launch_bounds__(Q4 ? Q4_THREADS : NUM_THREADS, 1)
 }
 
 template <bool B_MN, int BN, bool SPLIT, bool GATED = false, bool DUAL_B = false,
-          bool FP8 = false, bool Q4 = false>
+          bool FP8 = false, bool Q4 = false, bool WIDE = false>
 constexpr auto kernel_of() {
-  return &k_main_gemm<B_MN, BN, SPLIT, GATED, DUAL_B, FP8, Q4>;
+  return &k_main_gemm<B_MN, BN, SPLIT, GATED, DUAL_B, FP8, Q4, WIDE>;
 }
 
-int g_max_clusters[64][4] = {};
+int g_max_clusters[64][8] = {};
 
 // Largest number of two-CTA clusters of a kernel variant that can be
 // resident at once (queried once per device; the variant's shared-memory
 // attribute must already be set).
-template <bool B_MN, int BN, bool Q4 = false>
+template <bool B_MN, int BN, bool Q4 = false, bool WIDE = false>
 int max_clusters(int num_sms) {
   int dev = 0;
   cudaGetDevice(&dev);
-  int &n = g_max_clusters[dev & 63][(B_MN ? 1 : 0) + (Q4 ? 2 : 0)];
+  int &n = g_max_clusters[dev & 63][(B_MN ? 1 : 0) + (Q4 ? 2 : 0) + (WIDE ? 4 : 0)];
   if (n == 0) {
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(static_cast<unsigned>(num_sms / CLUSTER * CLUSTER), 1, 1);
-    cfg.blockDim = dim3(Q4 ? Q4_THREADS : NUM_THREADS, 1, 1);
-    cfg.dynamicSmemBytes = smem_bytes<BN, Q4>();
+    cfg.blockDim = dim3(Q4 ? Q4_THREADS : WIDE ? WIDE_THREADS : NUM_THREADS, 1, 1);
+    cfg.dynamicSmemBytes = smem_bytes<BN, Q4, WIDE>();
     cudaLaunchAttribute attr[1];
     attr[0].id = cudaLaunchAttributeClusterDimension;
     attr[0].val.clusterDim.x = CLUSTER;
@@ -829,8 +908,8 @@ int max_clusters(int num_sms) {
     cfg.attrs = attr;
     cfg.numAttrs = 1;
     int c = 0;
-    if (cudaOccupancyMaxActiveClusters(&c, kernel_of<B_MN, BN, false, false, false, false, Q4>(),
-                                       &cfg) != cudaSuccess ||
+    if (cudaOccupancyMaxActiveClusters(
+            &c, kernel_of<B_MN, BN, false, false, false, false, Q4, WIDE>(), &cfg) != cudaSuccess ||
         c < 1) {
       cudaGetLastError();  // clear; fall back to one cluster per SM pair
       c = num_sms / CLUSTER;
@@ -849,22 +928,22 @@ int main_gemm_group_m(int kb_main) {
 }
 
 template <bool B_MN, int BN, bool SPLIT, bool GATED, bool DUAL_B, bool FP8 = false,
-          bool Q4 = false>
+          bool Q4 = false, bool WIDE = false>
 cudaError_t launch_variant(const MainGemmArgs &a, int num_sms, cudaStream_t s) {
-  constexpr int TN = GATED ? BN / 2 : BN;
+  constexpr int TN = GATED ? BN / 2 : WIDE ? 2 * BN : BN;
   const int m_tiles = (a.M + BM - 1) / BM, n_tiles = (a.N + TN - 1) / TN;
   const int tiles = ((m_tiles + 1) / 2) * n_tiles;  // pair tiles
   if (tiles == 0) return cudaSuccess;
-  auto kern = kernel_of<B_MN, BN, SPLIT, GATED, DUAL_B, FP8, Q4>();
-  constexpr size_t smem = smem_bytes<BN, Q4>();
+  auto kern = kernel_of<B_MN, BN, SPLIT, GATED, DUAL_B, FP8, Q4, WIDE>();
+  constexpr size_t smem = smem_bytes<BN, Q4, WIDE>();
   cudaError_t e =
       cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));
   if (e != cudaSuccess) return e;
-  const int maxc = max_clusters<B_MN, BN, Q4>(num_sms);
+  const int maxc = max_clusters<B_MN, BN, Q4, WIDE>(num_sms);
   const int clusters = tiles < maxc ? tiles : maxc;
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(static_cast<unsigned>(clusters * CLUSTER), 1, 1);
-  cfg.blockDim = dim3(Q4 ? Q4_THREADS : NUM_THREADS, 1, 1);
+  cfg.blockDim = dim3(Q4 ? Q4_THREADS : WIDE ? WIDE_THREADS : NUM_THREADS, 1, 1);
   cfg.dynamicSmemBytes = smem;
   cfg.stream = s;
   cudaLaunchAttribute attr[2];
@@ -898,6 +977,8 @@ int main_gemm_pairs(bool b_mn, int num_sms) {
   return b_mn ? max_clusters<true, 256>(num_sms) : max_clusters<false, 256>(num_sms);
 }
 
+std::atomic<int> g_force_width{0};
+
 MainSplit main_gemm_split(int M, int N, int pairs) {
   MainSplit sp;
   if (pairs < 2) return sp;
@@ -918,11 +999,44 @@ MainSplit main_gemm_split(int M, int N, int pairs) {
 // well under half the tensor rate of 256-wide ones on GB300.
 int main_gemm_pick_bn(int, int, int) { return 256; }
 
+// Time of one 256 x 512 tile in units of one 256 x 256 tile.  The narrow
+// tile is bound by the TMA feed (~684 cycles per 64-wide K block against
+// 512 of MMA); the wide one by its MMAs (1024 cycles per K block) plus the
+// drain of the half the next tile waits for.
+constexpr double kWideTileCost = 1.6;
+// Cost of a split tile's fix-up (partials out and in, the combine and the
+// drain), in 256 x 256 tile times.
+constexpr double kSplitFixupCost = 0.35;
+
+MainSplit main_gemm_plan(int M, int N, int pairs, bool allow_wide) {
+  MainSplit narrow = main_gemm_split(M, N, pairs);
+  const int force = g_force_width.load();
+  if (!allow_wide || pairs < 1 || force == 256) return narrow;
+  const int m_pairs = ((M + BM - 1) / BM + 1) / 2;
+  const int tn = m_pairs * ((N + 255) / 256), tw = m_pairs * ((N + 511) / 512);
+  const int rem = tn % pairs;
+  const double cost_n = tn / pairs + (rem == 0 ? 0.0 : narrow.k > 1 ? 0.5 + kSplitFixupCost : 1.0);
+  const double cost_w = ((tw + pairs - 1) / pairs) * kWideTileCost;
+  if (force == 512 || cost_w < cost_n) {
+    MainSplit w;
+    w.wide = true;
+    return w;
+  }
+  return narrow;
+}
+
+void main_gemm_force_width(int w) { g_force_width.store(w); }
+
 cudaError_t launch_main_gemm(const MainGemmArgs &a, int num_sms, cudaStream_t s) {
   // Every pair tile ends in the K extension, where the producer waits for the
   // preceding kernel and signals the next one.
   if (a.k_ext <= 0) return cudaErrorInvalidValue;
   const bool split = a.split_k > 1 && a.split_rem > 0;
+  if (a.wide) {  // 256 x 512 pair tiles: plain bf16 layer, whole tiles only
+    if (split || a.q4 || a.fp8 || a.gated || a.kb_switch >= 0) return cudaErrorInvalidValue;
+    return a.b_mn ? launch_variant<true, 256, false, false, false, false, false, true>(a, num_sms, s)
+                  : launch_variant<false, 256, false, false, false, false, false, true>(a, num_sms, s);
+  }
   if (a.q4) {  // 4-bit W: codes in tmB, bf16 group scales in tmB3
     if (a.fp8 || a.gated || a.kb_switch >= 0) return cudaErrorInvalidValue;
     if (a.b_mn)

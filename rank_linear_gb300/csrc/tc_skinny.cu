@@ -462,7 +462,10 @@ cudaError_t launch_skinny(const SkinnyArgs *probs, int nprob, int num_sms, cudaS
     const int kb = (use[i]->K + BK - 1) / BK;
     max_kb = kb > max_kb ? kb : max_kb;
   }
-  const int S = skinny_split_launch(total_mt, max_kb, num_sms);
+  bool feeds = true;
+  for (int i = 0; i < P.nprob; ++i) feeds = feeds && use[i]->feeds_gemm != 0;
+  const int S = (feeds && total_mt <= kSkinnyFeedMaxCtas) ? 1
+                                                          : skinny_split_launch(total_mt, max_kb, num_sms);
   P.S = S;
   size_t smem = 0;
   unsigned grid = 0;

@@ -48,6 +48,29 @@ def check_full(t, alpha, dt):
     return errs
 
 
+def check_full_mm(t, alpha):
+    """Every element, the frozen-W products of the oracle taken by its
+    matmul step (the plain loops would stream W once per row)."""
+    Y, dX, dA, dB = run_gpu(t, alpha)
+    S = oracle.Sampled(t["X"], t["W"], t["A"], t["B"], t["dY"], alpha)
+    rows = np.arange(t["X"].shape[0])
+    errs = {"Y": rel_err(Y, S.y_rows_mm(rows)), "dX": rel_err(dX, S.dx_rows_mm(rows)),
+            "dA": rel_err(dA, S.dA()), "dB": rel_err(dB, S.dB())}
+    for k, e in errs.items():
+        assert e <= TOL["bf16"], f"{k}: {e:.3e} ({errs})"
+    return Y, dX, dA, dB
+
+
+@pytest.fixture
+def gemm_width():
+    """Forces the main GEMMs' tile width for one test, then restores the
+    cost model's choice."""
+    from rank_linear_gb300 import _lib
+    L = _lib.lib()
+    yield lambda w: _lib.check(L.lora_debug_gemm_width(w), "gemm width")
+    L.lora_debug_gemm_width(0)
+
+
 # M, d_in, d_out, r, alpha: several tiles in every dimension plus ragged tails
 SMALL_BF16 = [
     (300, 392, 264, 16, 32.0),     # M, K and N all ragged
@@ -66,6 +89,33 @@ SMALL_BF16 = [
 def test_bf16_elementwise(M, d_in, d_out, r, alpha):
     t = make_inputs(M, d_in, d_out, r, "bf16", seed=M + r)
     check_full(t, alpha, "bf16")
+
+
+@pytest.mark.parametrize("width", [256, 512])
+@pytest.mark.parametrize("M,d_in,d_out,r,alpha", SMALL_BF16)
+def test_bf16_each_tile_width(M, d_in, d_out, r, alpha, width, gemm_width):
+    """Both GEMMs with 256 x 256 pair tiles (tail split where it applies) and
+    with 256 x 512 pair tiles (half of the last tile's columns, or all of
+    its second half, past N), element by element."""
+    gemm_width(width)
+    t = make_inputs(M, d_in, d_out, r, "bf16", seed=M + r + width)
+    check_full(t, alpha, "bf16")
+
+
+@pytest.mark.parametrize("M,d_in,d_out,r,alpha", [
+    (2000, 1000, 5000, 24, 48.0),   # forward: 80 wide tiles (pairs take two); ragged M, K, N
+    (2000, 5000, 1000, 40, 80.0),   # dX GEMM: 80 wide tiles, MN-major B; ragged everything
+])
+def test_wide_tiles_several_per_pair(M, d_in, d_out, r, alpha, gemm_width):
+    """256 x 512 tiles with more tiles than CTA pairs, so a pair starts its
+    next tile's half-0 MMAs while its epilogue still drains half 1 of the
+    last: every element against the oracle, and bitwise repeatable."""
+    gemm_width(512)
+    t = make_inputs(M, d_in, d_out, r, "bf16", seed=M + d_in + r)
+    a = check_full_mm(t, alpha)
+    b = run_gpu(t, alpha)
+    for x, y in zip(a, b):
+        assert torch.equal(x, y)
 
 
 @pytest.mark.parametrize("M,d_in,d_out,r,alpha", [
@@ -207,7 +257,7 @@ def test_timing_hook_records_every_launch():
     torch.cuda.synchronize()
     assert used == rl.launch_count() - n0 == 5
     assert [_lib.KERNEL_KINDS[k] for k in kinds[:used]] == [
-        "down_fwd", "main_fwd", "down_bwd_grad_b", "main_bwd", "grad_a"]
+        "down_fwd", "main_fwd", "down_bwd", "main_bwd", "grad_a_b"]
     for j in range(used):
         assert evs[2 * j].elapsed_time(evs[2 * j + 1]) > 0
 
@@ -220,17 +270,18 @@ def test_timing_hook_rejects_uncreated_events():
 
 
 def test_tail_split_path():
-    """M = d_in = d_out = 4096: the main GEMMs' last wave is split across CTA
-    pairs (given the full workspace).  The split results are bitwise
+    """M = 4096, d_in = d_out = 2816: the cost model keeps both GEMMs at
+    256 x 256 tiles, whose last wave (24 of 76 pairs' tiles) is split across
+    CTA pairs given the full workspace.  The split results are bitwise
     repeatable, agree with the unsplit ones (minimal workspace) and with the
     oracle on sampled rows."""
-    M = d = 4096
+    M, d = 4096, 2816
     r, alpha = 16, 16.0
     t = make_inputs(M, d, d, r, "bf16", seed=12, device=DEV)
     X, W, A, B, dY = t["X"], t["W"], t["A"], t["B"], t["dY"]
     full = torch.empty(rl.workspace_bytes(M, d, d, r, torch.bfloat16), dtype=torch.uint8,
                        device=DEV)
-    minimal = torch.empty(3 * 16 * 4096 * 2, dtype=torch.uint8, device=DEV)  # B^T, sG, sG^T
+    minimal = torch.empty(16 * d * 2 + 2 * 16 * M * 2, dtype=torch.uint8, device=DEV)  # B^T, sG, sG^T
     assert full.numel() > minimal.numel()
 
     def run(ws):
@@ -245,6 +296,7 @@ def test_tail_split_path():
         assert torch.equal(a, b)
     for a, b in zip(s1, u):
         assert rel_err(a, b.double().cpu().numpy()) <= 4e-3
+    assert not torch.equal(s1[0], u[0]) and not torch.equal(s1[1], u[1])  # the split ran
     host = {k: v.cpu() for k, v in t.items()}
     S = oracle.Sampled(host["X"], host["W"], host["A"], host["B"], host["dY"], alpha)
     rows = np.array([0, 2047, 3071, 3584, 4095])  # include rows of the split tiles

@@ -100,16 +100,25 @@ def test_small_against_oracle(shape):
 @pytest.mark.parametrize("shape", [SMALL[0], SMALL[4], SMALL[6]],
                          ids=lambda s: "x".join(map(str, s[:4])))
 def test_same_bits_as_the_bf16_layer_on_dequantised_w(shape):
+    """The bf16 layer runs with 256 x 256 tiles here, the only width of the
+    dequantising GEMM, so both run the same tiles and splits in the same
+    order."""
+    from rank_linear_gb300 import _lib
     M, d_in, d_out, r, alpha = shape
     t = inputs(M, d_in, d_out, r, seed=7 + sum(shape[:4]))
     g = {k: v.to(DEV) for k, v in t.items()}
     qw = rl.quantize_w_q4(g["W"])
     Wd = rl.dequantize_w_q4(qw)
-    Y4, s4 = rl.q4_forward(g["X"], qw, g["A"], g["B"], alpha)
-    Y16, s16 = rl.forward(g["X"], Wd, g["A"], g["B"], alpha)
-    dX4, _, _ = rl.q4_backward(g["dY"], g["X"], qw, g["A"], g["B"], alpha, s4)
-    dX16, _, _ = rl.backward(g["dY"], g["X"], Wd, g["A"], g["B"], alpha, s16)
-    torch.cuda.synchronize()
+    L = _lib.lib()
+    _lib.check(L.lora_debug_gemm_width(256), "gemm width")
+    try:
+        Y4, s4 = rl.q4_forward(g["X"], qw, g["A"], g["B"], alpha)
+        Y16, s16 = rl.forward(g["X"], Wd, g["A"], g["B"], alpha)
+        dX4, _, _ = rl.q4_backward(g["dY"], g["X"], qw, g["A"], g["B"], alpha, s4)
+        dX16, _, _ = rl.backward(g["dY"], g["X"], Wd, g["A"], g["B"], alpha, s16)
+        torch.cuda.synchronize()
+    finally:
+        L.lora_debug_gemm_width(0)
     rl.device_status()
     assert torch.equal(Y4, Y16)
     assert torch.equal(dX4, dX16)

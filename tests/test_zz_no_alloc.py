@@ -57,9 +57,10 @@ def _rel(got, ref):
     return float(np.abs(got - ref).max() / (den if den > 0 else 1.0))
 
 
-# M = d_in = d_out = 4096, r = 16: on a GB300 (76 CTA pairs) the dX GEMM's
-# last wave is split two ways, and its split region fits in the array
-SPLIT_PROBLEM = (4096, 4096, 4096, 16, 16.0)
+# M = 4096, d_in = 2816, d_out = 4096, r = 16: on a GB300 (76 CTA pairs)
+# the dX GEMM (N = d_in) runs 256 x 256 tiles whose last wave is split two
+# ways, and its split region fits in the array
+SPLIT_PROBLEM = (4096, 2816, 4096, 16, 16.0)
 
 
 def _rows_per_m_tile(M, seed):
