@@ -269,12 +269,13 @@ def test_timing_hook_rejects_uncreated_events():
     assert _lib.lib().lora_set_timing_events(arr, None, 1) == _lib.LORA_ERR_INVALID_ARG
 
 
-def test_tail_split_path():
-    """M = 4096, d_in = d_out = 2816: the cost model keeps both GEMMs at
-    256 x 256 tiles, whose last wave (24 of 76 pairs' tiles) is split across
-    CTA pairs given the full workspace.  The split results are bitwise
-    repeatable, agree with the unsplit ones (minimal workspace) and with the
-    oracle on sampled rows."""
+def test_tail_split_path(gemm_width):
+    """M = 4096, d_in = d_out = 2816 with 256 x 256 tiles (the width of the
+    SwiGLU, fp8 and 4-bit GEMMs, forced here for the plain layer): the last
+    wave (24 of 76 pairs' tiles) is split across CTA pairs given the full
+    workspace.  The split results are bitwise repeatable, agree with the
+    unsplit ones (minimal workspace) and with the oracle on sampled rows."""
+    gemm_width(256)
     M, d = 4096, 2816
     r, alpha = 16, 16.0
     t = make_inputs(M, d, d, r, "bf16", seed=12, device=DEV)

@@ -57,8 +57,9 @@ def _rel(got, ref):
     return float(np.abs(got - ref).max() / (den if den > 0 else 1.0))
 
 
-# M = 4096, d_in = 2816, d_out = 4096, r = 16: on a GB300 (76 CTA pairs)
-# the dX GEMM (N = d_in) runs 256 x 256 tiles whose last wave is split two
+# M = 4096, d_in = 2816, d_out = 4096, r = 16: on a GB300 (76 CTA pairs),
+# with 256 x 256 tiles (forced through the library's test hook; the width
+# of the SwiGLU, fp8 and 4-bit GEMMs), the dX GEMM's last wave is split two
 # ways, and its split region fits in the array
 SPLIT_PROBLEM = (4096, 2816, 4096, 16, 16.0)
 
@@ -77,6 +78,15 @@ def test_split_problem_twice_in_a_row():
     path ran -- which differ from the unsplit (minimal-workspace) bits, and
     agrees with the oracle on all of dA and dB and one row of dX per 128-row
     m-tile."""
+    L = _lib.lib()
+    _lib.check(L.lora_debug_gemm_width(256), "gemm width")
+    try:
+        _split_problem_twice_in_a_row()
+    finally:
+        L.lora_debug_gemm_width(0)
+
+
+def _split_problem_twice_in_a_row():
     import oracle
     M, d_in, d_out, r, alpha = SPLIT_PROBLEM
     bf = torch.bfloat16
