@@ -226,6 +226,60 @@ __global__ void __launch_bounds__(1024) k_quant_rows(const __nv_bfloat16 *__rest
   }
 }
 
+// The same quantisation for rows of at most 4096 columns: one warp per row
+// holds the whole row in registers (16 bytes x 16 per lane), so the row's
+// maximum is a warp shuffle and four rows share a block with no block-wide
+// barrier.  Rows this short left the block-per-row kernel latency-bound
+// (two warps per block, a barrier between the maximum and the stores).
+constexpr int kQuantWarpMaxCols = 4096;
+__global__ void __launch_bounds__(128) k_quant_rows_warp(const __nv_bfloat16 *__restrict__ x,
+                                                         int64_t rows, int64_t cols,
+                                                         uint8_t *__restrict__ q,
+                                                         float *__restrict__ scale,
+                                                         const float *__restrict__ mul) {
+  griddep_wait();
+  griddep_launch_dependents();
+  const int lane = threadIdx.x & 31;
+  const int64_t row = int64_t(blockIdx.x) * 4 + (threadIdx.x >> 5);
+  if (row >= rows) return;
+  const __nv_bfloat16 *xr = x + row * cols;
+  constexpr int V = kQuantWarpMaxCols / (32 * 8);
+  uint4 v[V];
+  float a = 0.f;
+#pragma unroll
+  for (int j = 0; j < V; ++j) {
+    const int64_t c = (lane + int64_t(j) * 32) * 8;
+    v[j] = c < cols ? *reinterpret_cast<const uint4 *>(xr + c) : make_uint4(0u, 0u, 0u, 0u);
+    const __nv_bfloat162 *h = reinterpret_cast<const __nv_bfloat162 *>(&v[j]);
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      const float2 f = __bfloat1622float2(h[i]);
+      a = fmaxf(a, fmaxf(fabsf(f.x), fabsf(f.y)));
+    }
+  }
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) a = fmaxf(a, __shfl_xor_sync(0xffffffffu, a, o));
+  const int e = pow2_exponent(a);
+  const float inv = ldexpf(1.f, -e);
+  if (lane == 0) scale[row] = ldexpf(1.f, e) * (mul != nullptr ? mul[0] : 1.f);
+  uint8_t *qr = q + row * cols;
+#pragma unroll
+  for (int j = 0; j < V; ++j) {
+    const int64_t c = (lane + int64_t(j) * 32) * 8;
+    if (c >= cols) break;
+    const __nv_bfloat162 *h = reinterpret_cast<const __nv_bfloat162 *>(&v[j]);
+    uint32_t lo = 0, hi = 0;
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      const float2 f = __bfloat1622float2(h[i]);
+      const uint32_t pair = to_e4m3(f.x * inv) | (uint32_t(to_e4m3(f.y * inv)) << 8);
+      if (i < 2) lo |= pair << (16 * i);
+      else hi |= pair << (16 * (i - 2));
+    }
+    *reinterpret_cast<uint2 *>(qr + c) = make_uint2(lo, hi);
+  }
+}
+
 // amax_bits |= the bit pattern of max |w| (non-negative floats order like
 // their bit patterns, so an unsigned atomicMax finds the largest).
 __global__ void k_absmax_all(const __nv_bfloat16 *__restrict__ w, int64_t n,
@@ -398,6 +452,10 @@ cudaError_t launch_quant_rows_e4m3(const void *x, int64_t rows, int64_t cols, vo
                                    float *scale, const float *mul, cudaStream_t s) {
   if (rows <= 0) return cudaSuccess;
   if (cols > 1024 * 64) return cudaErrorInvalidValue;
+  if (cols <= kQuantWarpMaxCols)
+    return launch_pdl(k_quant_rows_warp, dim3(static_cast<unsigned>((rows + 3) / 4)), dim3(128), s,
+                      static_cast<const __nv_bfloat16 *>(x), rows, cols, static_cast<uint8_t *>(q),
+                      scale, mul);
   const int threads = static_cast<int>(((cols + 63) / 64 + 31) / 32 * 32);
   return launch_pdl(k_quant_rows, dim3(static_cast<unsigned>(rows)), dim3(threads), s,
                     static_cast<const __nv_bfloat16 *>(x), cols, static_cast<uint8_t *>(q), scale,
