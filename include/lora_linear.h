@@ -221,9 +221,10 @@ int lora_timing_used(void);
 /*
  * Test hook for the bounded device-side waits (the pages have no
  * counterpart; it exists so that the timeout path can be exercised without
- * faulting or hanging a GPU).  The next n bf16 backward dA-and-dB passes
- * (the last launch of lora_linear_bwd) launched by this process (any
- * thread) leave the first pipeline stage of their first dA CTA unfilled.  That CTA's MMA
+ * faulting or hanging a GPU).  The next n bf16 backward dA passes (the last
+ * launch of lora_linear_bwd, which carries dB as well when the GEMMs run
+ * 256 x 512 tiles) launched by this process (any thread) leave the first
+ * pipeline stage of their first dA CTA unfilled.  That CTA's MMA
  * wait then runs out after the wait limit (about 2 s), the kernel leaves
  * through its abort path (no fault, no hang), the caller's next
  * lora_device_status() returns LORA_ERR_TIMEOUT, and dA of that call is

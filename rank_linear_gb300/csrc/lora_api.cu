@@ -345,8 +345,10 @@ lora_status_t fwd_bf16(const void *X, const void *W, const void *A, const void *
     Bsrc = Bp;
     b_inner = P.r_pad;
   }
+  // with 256 x 512 tiles (about 33 us each at K = 4096) the pass can run
+  // beside the GEMM's start: the pairs that start late have a tile's slack
   LORA_TRY(down_fwd_bf16(di, P, X, A, s, r, M, d_in, saved, st, counters,
-                         split ? 2 * P.fsplit.rem : 0, true));
+                         split ? 2 * P.fsplit.rem : 0, wide));
   MainGemmArgs f2;
   if (split) {
     f2.split_k = P.fsplit.k;
@@ -396,19 +398,26 @@ lora_status_t bwd_bf16(const void *dY, const void *X, const void *W, const void 
   const float s = alpha / static_cast<float>(r);
   if (saved == nullptr) {  // recompute s X A^T into the workspace
     // with the forward's launch shape, so that the bits are the forward's
+    const bool fwd_wide =
+        main_gemm_plan(static_cast<int>(M), static_cast<int>(d_out), main_gemm_pairs(false, di.sms),
+                       q4 == nullptr)
+            .wide;
     void *re = at(ws, P.resaved_off);
-    LORA_TRY(down_fwd_bf16(di, P, X, A, s, r, M, d_in, re, st, nullptr, 0, true));
+    LORA_TRY(down_fwd_bf16(di, P, X, A, s, r, M, d_in, re, st, nullptr, 0, fwd_wide));
     saved = re;
   }
   const void *sHt = static_cast<const uint8_t *>(saved) + P.sHt_off;
   void *sG = at(ws, P.sg_off);
   void *sGt = at(ws, P.sgt_off);
 
-  // sG = s dY B (and its transpose) alone; it feeds the dX GEMM (on few
-  // SMs, beside the GEMM's start).  dB = dY^T sH runs after the GEMM
-  // together with dA, on the SMs the GEMM's last wave leaves idle.  The
-  // launches are the same without dX (no GEMM between them), so dA and dB
-  // are the same bits either way (each launch's split of K is its own).
+  // With 256 x 512 tiles: sG = s dY B (and its transpose) alone, on few SMs
+  // beside the dX GEMM's start; dB = dY^T sH after the GEMM together with
+  // dA, on the SMs the GEMM's short last wave leaves idle.  With 256 x 256
+  // tiles (whose tail split already fills the last wave): sG and dB in one
+  // launch (both read dY), then dA beside the GEMM's last wave.  The choice
+  // depends on the shape only, not on dX: the launches are the same without
+  // dX (no GEMM between them), so dA and dB are the same bits either way
+  // (each launch's split of K is its own).
   SkinnyArgs g[2];
   SkinnyArgs &b1 = g[0];
   LORA_TRY(tmap(&b1.tmA, dY, d_out, M, d_out * 2, 64, 128, "dY"));
@@ -450,9 +459,14 @@ lora_status_t bwd_bf16(const void *dY, const void *X, const void *W, const void 
   b4.ld0 = r;
   b4.n0 = r;
   b4.dev_status = di.status;
-  b1.feeds_gemm = 1;
-  LORA_TRY(run(LORA_K_DOWN_BWD, st, "s dY B pass",
-               [&] { return launch_skinny(&b1, 1, di.sms, st); }));
+  if (wide) {
+    b1.feeds_gemm = 1;
+    LORA_TRY(run(LORA_K_DOWN_BWD, st, "s dY B pass",
+                 [&] { return launch_skinny(&b1, 1, di.sms, st); }));
+  } else {
+    LORA_TRY(run(LORA_K_DOWN_BWD_GRAD_B, st, "s dY B and dB pass",
+                 [&] { return launch_skinny(g, 2, di.sms, st); }));
+  }
 
   // dX = [dY | sG] . [W ; A]
   if (dX != nullptr) {
@@ -506,6 +520,8 @@ lora_status_t bwd_bf16(const void *dY, const void *X, const void *W, const void 
   while (pending > 0 && !g_withhold.compare_exchange_weak(pending, pending - 1)) {
   }
   b3.withhold_first_stage = pending > 0 ? 1 : 0;
+  if (!wide)
+    return run(LORA_K_GRAD_A, st, "dA pass", [&] { return launch_skinny(&b3, 1, di.sms, st); });
   // dA and dB in one launch (dA first: the test hook's problem)
   b4.after_gemm = b3.after_gemm;
   SkinnyArgs ab[2] = {b3, b4};

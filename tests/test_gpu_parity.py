@@ -173,7 +173,9 @@ def test_bitwise_deterministic():
         assert torch.equal(x, y)
 
 
-def test_recompute_when_saved_is_null():
+@pytest.mark.parametrize("width", [256, 512])
+def test_recompute_when_saved_is_null(width, gemm_width):
+    gemm_width(width)
     t = make_inputs(300, 392, 264, 16, "bf16", seed=5)
     a = run_gpu(t, 32.0)
     b = run_gpu(t, 32.0, saved_none=True)
@@ -181,7 +183,11 @@ def test_recompute_when_saved_is_null():
         assert torch.equal(x, y)
 
 
-def test_skip_dx():
+@pytest.mark.parametrize("width", [256, 512])
+def test_skip_dx(width, gemm_width):
+    """dA and dB do not depend on whether dX is computed (each tile width
+    has its own launch grouping, the same with and without dX)."""
+    gemm_width(width)
     t = make_inputs(300, 392, 264, 16, "bf16", seed=5)
     a = run_gpu(t, 32.0)
     b = run_gpu(t, 32.0, need_dX=False)
@@ -242,22 +248,28 @@ def test_autograd_function():
     assert rel_err(B.grad, dBr) <= 1e-2
 
 
-def test_timing_hook_records_every_launch():
+@pytest.mark.parametrize("width,kinds", [
+    (512, ["down_fwd", "main_fwd", "down_bwd", "main_bwd", "grad_a_b"]),
+    (256, ["down_fwd", "main_fwd", "down_bwd_grad_b", "main_bwd", "grad_a"]),
+])
+def test_timing_hook_records_every_launch(width, kinds, gemm_width):
+    """Five launches a step; with 256 x 512 tiles dB runs after the dX GEMM
+    beside dA, with 256 x 256 tiles beside s dY B before it."""
     from rank_linear_gb300 import _lib
+    gemm_width(width)
     t = make_inputs(300, 392, 264, 16, "bf16", seed=5)
     g = {k: v.to(DEV) for k, v in t.items()}
-    evs, arr, kinds = rl.timing_events(8)
+    evs, arr, kinds_out = rl.timing_events(8)
     L = _lib.lib()
     n0 = rl.launch_count()
-    assert L.lora_set_timing_events(arr, kinds, 8) == 0
+    assert L.lora_set_timing_events(arr, kinds_out, 8) == 0
     Y, saved = rl.forward(g["X"], g["W"], g["A"], g["B"], 32.0)
     rl.backward(g["dY"], g["X"], g["W"], g["A"], g["B"], 32.0, saved)
     used = L.lora_timing_used()
     L.lora_set_timing_events(None, None, 0)
     torch.cuda.synchronize()
     assert used == rl.launch_count() - n0 == 5
-    assert [_lib.KERNEL_KINDS[k] for k in kinds[:used]] == [
-        "down_fwd", "main_fwd", "down_bwd", "main_bwd", "grad_a_b"]
+    assert [_lib.KERNEL_KINDS[k] for k in kinds_out[:used]] == kinds
     for j in range(used):
         assert evs[2 * j].elapsed_time(evs[2 * j + 1]) > 0
 
