@@ -234,6 +234,19 @@ int lora_timing_used(void);
 lora_status_t lora_debug_withhold_arrive(int n);
 
 /*
+ * Test hook for the main GEMM's abort path (the pages have no counterpart).
+ * The next n bf16 backward dX GEMMs (not the 4-bit layer's) launched by this
+ * process leave one pipeline stage of the first CTA pair half filled: the
+ * odd CTA never loads its first stage.  The MMA wait for it runs out after
+ * the wait limit (about 2 s); both CTAs leave through their abort paths,
+ * the even CTA first settling every phase of the pair's stage ring, so that
+ * no copy is in flight when either CTA exits (no fault, no hang).  The
+ * caller's next lora_device_status() returns LORA_ERR_TIMEOUT; dX of that
+ * call is undefined.  n = 0 cancels; LORA_ERR_INVALID_ARG for n < 0.
+ */
+lora_status_t lora_debug_withhold_gemm_stage(int n);
+
+/*
  * Test hook of the main GEMMs' tile width (the pages have no counterpart).
  * The plain bf16 layer's two GEMMs run 256 x 512 or 256 x 256 pair tiles
  * (the latter with the split of a short last wave), chosen per shape by a

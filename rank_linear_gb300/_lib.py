@@ -37,6 +37,7 @@ SIGNATURES = {
     "lora_set_timing_events": ([ctypes.POINTER(_vp), ctypes.POINTER(_int), _int], _int),
     "lora_debug_withhold_arrive": ([_int], _int),
     "lora_debug_gemm_width": ([_int], _int),
+    "lora_debug_withhold_gemm_stage": ([_int], _int),
     "lora_timing_used": ([], _int),
     "lora_fp8_quantize_w_workspace_bytes": ([], _sz),
     "lora_fp8_quantize_w": ([_vp, _i64, _i64, _vp, _vp, _vp, _vp, _sz, _vp], _int),

@@ -59,6 +59,9 @@ struct MainGemmArgs {
   // 256 x 512 pair tiles (two N = 256 MMAs per K step sharing A; plain bf16
   // layer only, no tail split); from main_gemm_plan
   bool wide = false;
+  // Test hook of the abort path (not with 4-bit W): the odd CTA of the first
+  // pair never loads its first stage.
+  int withhold = 0;
 };
 constexpr int kMainBM = 128, kMainBK = 64;
 int main_gemm_pick_bn(int M, int N, int num_sms);

@@ -35,6 +35,16 @@ thread_local TimingHook t_hook;
 std::atomic<uint64_t> g_launches{0};
 // backward dA passes still to launch with a withheld stage (test hook)
 std::atomic<int> g_withhold{0};
+// backward dX GEMMs still to launch with a withheld stage (test hook)
+std::atomic<int> g_withhold_gemm{0};
+
+// Takes one pending use of a test hook's counter; 1 if there was one.
+int take_one(std::atomic<int> &counter) {
+  int pending = counter.load();
+  while (pending > 0 && !counter.compare_exchange_weak(pending, pending - 1)) {
+  }
+  return pending > 0 ? 1 : 0;
+}
 
 lora_status_t fail(lora_status_t st, const char *fmt, ...) {
   char buf[512];
@@ -499,6 +509,7 @@ lora_status_t bwd_bf16(const void *dY, const void *X, const void *W, const void 
       b2.partials = reinterpret_cast<float *>(at(ws, P.bsplit_off));
       b2.counters = counters;
     }
+    if (q4 == nullptr) b2.withhold = take_one(g_withhold_gemm);  // test hook
     LORA_TRY(run(LORA_K_MAIN_BWD, st, "dX GEMM", [&] { return launch_main_gemm(b2, di.sms, st); }));
   }
 
@@ -516,10 +527,7 @@ lora_status_t bwd_bf16(const void *dY, const void *X, const void *W, const void 
   b3.n1 = r;
   b3.dev_status = di.status;
   b3.after_gemm = dX != nullptr;  // overlaps the dX GEMM's last wave
-  int pending = g_withhold.load();  // test hook of the bounded waits
-  while (pending > 0 && !g_withhold.compare_exchange_weak(pending, pending - 1)) {
-  }
-  b3.withhold_first_stage = pending > 0 ? 1 : 0;
+  b3.withhold_first_stage = take_one(g_withhold);  // test hook of the bounded waits
   if (!wide)
     return run(LORA_K_GRAD_A, st, "dA pass", [&] { return launch_skinny(&b3, 1, di.sms, st); });
   // dA and dB in one launch (dA first: the test hook's problem)
@@ -1725,6 +1733,13 @@ lora_status_t lora_debug_gemm_width(int width) {
   if (width != 0 && width != 256 && width != 512)
     return fail(LORA_ERR_INVALID_ARG, "width %d is not 0, 256 or 512", width);
   main_gemm_force_width(width);
+  return LORA_OK;
+}
+
+lora_status_t lora_debug_withhold_gemm_stage(int n) {
+  t_err.clear();
+  if (n < 0) return fail(LORA_ERR_INVALID_ARG, "n = %d is negative", n);
+  g_withhold_gemm.store(n);
   return LORA_OK;
 }
 

@@ -98,12 +98,19 @@ __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, volatil
 
 // Bounded wait that ignores the abort flag: used on the way out of an
 // aborted CTA to let its own copies and MMAs in flight finish.
+template <bool kCluster = false>
 __device__ __forceinline__ bool mbar_wait_drain(uint32_t bar, uint32_t parity) {
   const uint64_t t0 = globaltimer_ns();
-  while (!mbar_test(bar, parity)) {
+  while (!mbar_test<kCluster>(bar, parity)) {
     if (globaltimer_ns() - t0 > kWaitLimitNs) return false;
   }
   return true;
+}
+// Counts `bytes` of transactions as complete on this CTA's mbarrier, as if
+// a copy had delivered them (settles a phase whose copies will never come).
+__device__ __forceinline__ void mbar_complete_tx(uint32_t bar, uint32_t bytes) {
+  asm volatile("mbarrier.complete_tx.relaxed.cta.shared::cta.b64 [%0], %1;" ::"r"(bar), "r"(bytes)
+               : "memory");
 }
 
 // ---------------------------------------------------------------- named barriers
@@ -377,6 +384,9 @@ __device__ __forceinline__ uint32_t dsmem_map(uint32_t addr, uint32_t rank) {
   uint32_t out;
   asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(out) : "r"(addr), "r"(rank));
   return out;
+}
+__device__ __forceinline__ void dsmem_st_u32(uint32_t addr, uint32_t v) {
+  asm volatile("st.shared::cluster.u32 [%0], %1;" ::"r"(addr), "r"(v) : "memory");
 }
 __device__ __forceinline__ void dsmem_st_f4(uint32_t addr, float4 v) {
   asm volatile("st.shared::cluster.v4.f32 [%0], {%1, %2, %3, %4};" ::"r"(addr), "f"(v.x),

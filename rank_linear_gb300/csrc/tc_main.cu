@@ -122,11 +122,14 @@ struct __align__(16) MainTail {
   uint64_t tfull[2];        // each CTA: an accumulator is complete
   uint64_t tempty[2];       // even CTA: both CTAs drained an accumulator
   uint64_t drain;
+  uint64_t peer_done;       // even CTA: the odd CTA's issue counts are in peer_issued
+  uint64_t settled;         // odd CTA: the even CTA saw every copy of the pair land
   uint64_t ebar;            // each CTA: the four epilogue warps meet (tail split)
   uint64_t fix;             // each CTA: the other K range's partial landed (tail split)
   uint32_t tmem_base;
   int abort_flag;
   int split_last;
+  uint32_t peer_issued[STAGES];  // even CTA: phases the odd CTA loaded, per stage
   // 4-bit W: target of the odd CTA's 16-byte "stage expanded" copies
   alignas(16) uint8_t sig[16];
 };
@@ -274,7 +277,8 @@ __global__ void __launch_bounds__(Q4 ? Q4_THREADS : WIDE ? WIDE_THREADS : NUM_TH
                 __nv_bfloat16 *__restrict__ out, __nv_bfloat16 *__restrict__ aux0,
                 __nv_bfloat16 *__restrict__ aux1, int64_t ldo, int split_k, int split_rem,
                 float *__restrict__ partials, unsigned *counters, unsigned *dev_status,
-                const float *__restrict__ row_scale, const float *__restrict__ w_scale) {
+                const float *__restrict__ row_scale, const float *__restrict__ w_scale,
+                int withhold) {
   static_assert(!(GATED && B_MN), "the gated pair reads K-major B");
   static_assert(!(FP8 && (B_MN || GATED || DUAL_B)), "the fp8 product reads K-major operands");
   static_assert(!(Q4 && (GATED || DUAL_B || FP8)), "4-bit W: plain layer only");
@@ -329,6 +333,8 @@ __global__ void __launch_bounds__(Q4 ? Q4_THREADS : WIDE ? WIDE_THREADS : NUM_TH
       mbar_init(smem_u32(&tail->tempty[a]), WIDE ? WIDE_EPI_ARRIVALS : EPI_ARRIVALS);
     }
     mbar_init(smem_u32(&tail->drain), 1);
+    mbar_init(smem_u32(&tail->peer_done), 1);
+    mbar_init(smem_u32(&tail->settled), 1);
     mbar_init(smem_u32(&tail->ebar), 4);
     mbar_init(smem_u32(&tail->fix), 1);
     tail->abort_flag = 0;
@@ -386,6 +392,16 @@ __global__ void __launch_bounds__(Q4 ? Q4_THREADS : WIDE ? WIDE_THREADS : NUM_TH
           if (!mbar_wait(smem_u32(&tail->empty[stage]), phase ^ 1u, abort_flag, dev_status)) {
             ok = false;
             break;
+          }
+          if (!Q4 && withhold && blockIdx.x == 1 && item == pair_id && kb == kb_lo) {
+            // test hook: the odd CTA of the first pair never loads its first
+            // stage, so the MMA thread's wait for it runs out and both CTAs
+            // leave through their abort paths
+            if (++stage == STAGES) {
+              stage = 0;
+              phase ^= 1u;
+            }
+            continue;
           }
           const uint32_t full_local = smem_u32(&tail->full[stage]);
           const uint32_t full = dsmem_map(full_local, 0);  // the even CTA's barrier
@@ -487,18 +503,42 @@ __global__ void __launch_bounds__(Q4 ? Q4_THREADS : WIDE ? WIDE_THREADS : NUM_TH
           const uint64_t t0 = globaltimer_ns();
           while (globaltimer_ns() - t0 < 100000ull) {
           }
-        } else if (leader) {
-          // a phase the even CTA armed completes when both CTAs' bytes landed
-          for (int s = 0; s < STAGES; ++s)
-            if (issued[s]) mbar_wait_drain(smem_u32(&tail->full[s]), (issued[s] - 1u) & 1u);
+        }
+      }
+      if constexpr (!Q4) {
+        // Both CTAs' copies complete on the even CTA's full barriers, which
+        // only the even CTA can poll.  The odd CTA hands over how many
+        // phases of each stage it loaded and, when aborting, stays until the
+        // even CTA has seen every copy of the pair land.  Per stage at most
+        // the last phase can be outstanding (a producer re-arms a stage only
+        // after the MMAs consumed its previous phase, which needs both CTAs'
+        // copies), and the two counts differ by at most one: the even CTA
+        // settles a phase it armed but the odd CTA never loaded by counting
+        // the odd CTA's bytes itself, arms a phase only the odd CTA loaded
+        // for the odd CTA's bytes, and waits for the phase to complete.
+        constexpr uint32_t CTA_TX = PAIR_TX / CLUSTER;
+        if (!leader) {
+          const uint32_t pi = smem_u32(tail->peer_issued);
+          for (int s = 0; s < STAGES; ++s) dsmem_st_u32(dsmem_map(pi + 4u * s, 0), issued[s]);
+          mbar_arrive_cluster(dsmem_map(smem_u32(&tail->peer_done), 0));  // release: the counts
+          if (!clean) mbar_wait_drain(smem_u32(&tail->settled), 0);
         } else {
-          // The odd CTA's copies complete on the even CTA's barriers, which it
-          // cannot poll; one it issued for a phase the even CTA never armed
-          // is not covered above.  A copy lands within microseconds: wait
-          // 100 us before leaving.
-          const uint64_t t0 = globaltimer_ns();
-          while (globaltimer_ns() - t0 < 100000ull) {
+          if (!clean) {
+            const bool counts = mbar_wait_drain<true>(smem_u32(&tail->peer_done), 0);
+            for (int s = 0; s < STAGES; ++s) {
+              const uint32_t e = issued[s];
+              const uint32_t o = counts ? reinterpret_cast<volatile uint32_t *>(tail->peer_issued)[s] : e;
+              const uint32_t n = e > o ? e : o;
+              if (n == 0) continue;
+              const uint32_t fs = smem_u32(&tail->full[s]);
+              if (e == o + 1)
+                mbar_complete_tx(fs, CTA_TX);
+              else if (o == e + 1)
+                mbar_expect_tx(fs, CTA_TX);
+              mbar_wait_drain(fs, (n - 1u) & 1u);
+            }
           }
+          mbar_arrive_cluster(dsmem_map(smem_u32(&tail->settled), 1));
         }
       }
     }
@@ -964,7 +1004,8 @@ cudaError_t launch_variant(const MainGemmArgs &a, int num_sms, cudaStream_t s) {
                             static_cast<__nv_bfloat16 *>(a.out),
                             static_cast<__nv_bfloat16 *>(a.aux0),
                             static_cast<__nv_bfloat16 *>(a.aux1), a.ldo, a.split_k, a.split_rem,
-                            a.partials, a.counters, a.dev_status, a.row_scale, a.w_scale);
+                            a.partials, a.counters, a.dev_status, a.row_scale, a.w_scale,
+                            a.withhold);
 }
 
 }  // namespace
