@@ -57,7 +57,7 @@ struct MainGemmArgs {
   // memory before the MMAs read it.
   bool q4 = false;
   // 256 x 512 pair tiles (two N = 256 MMAs per K step sharing A; plain bf16
-  // layer only, no tail split); from main_gemm_plan
+  // layer only); from main_gemm_plan
   bool wide = false;
   // Test hook of the abort path (not with 4-bit W): the odd CTA of the first
   // pair never loads its first stage.
@@ -70,16 +70,18 @@ int main_gemm_pairs(bool b_mn, int num_sms);
 struct MainSplit {
   int k = 1, rem = 0;
   size_t partial_bytes = 0, counter_bytes = 0;
-  bool wide = false;  // 256 x 512 tiles (never split)
+  bool wide = false;  // 256 x 512 tiles
 };
-// Tail split for an M x N output on `pairs` CTA pairs: the last wave's rem
-// tiles are split two ways (K ranges) when 2 * rem <= pairs.  For the gated
-// pair pass N = 2 x roundup(output columns, 128) (tiles of 128 columns).
-MainSplit main_gemm_split(int M, int N, int pairs);
-// The plain layer's choice between 256 x 512 tiles and 256 x 256 tiles with
-// the tail split, by a cost model of the waves (allow_wide false: the
-// latter only, as main_gemm_split).
-MainSplit main_gemm_plan(int M, int N, int pairs, bool allow_wide);
+// Tail split for an M x N output on `pairs` CTA pairs in 256 x tile_n pair
+// tiles: the last wave's rem tiles are split two ways (K ranges) when
+// 2 * rem <= pairs.  For the gated pair pass N = 2 x roundup(output columns,
+// 128) (tiles of 128 columns).
+MainSplit main_gemm_split(int M, int N, int pairs, int tile_n = 256);
+// The plain layer's choice between 256 x 512 and 256 x 256 tiles, each with
+// its tail split where that applies, by a cost model of the waves that
+// weighs a split's fix-up against the tile's K blocks (kb_total, both
+// segments).  allow_wide false: 256-wide tiles only, as main_gemm_split.
+MainSplit main_gemm_plan(int M, int N, int pairs, bool allow_wide, int kb_total);
 // Test hook: 0 = choose by the cost model, 256 or 512 = that width only
 // (512 where allowed).
 void main_gemm_force_width(int w);
@@ -125,12 +127,19 @@ struct SkinnyArgs {
   int after_gemm = 0;
   // This pass feeds a main GEMM launched right after it, which needs its
   // result only at the end of each tile: when one CTA per 128 rows makes at
-  // most kSkinnyFeedMaxCtas CTAs, run that way (no K split, no cluster), so
-  // that the GEMM's CTA pairs start on the other SMs at once instead of
-  // waiting for this pass to leave them.
+  // most kSkinnyFeedMaxCtas CTAs and K spans at most kSkinnyFeedMaxKb
+  // blocks, run that way (no K split, no cluster), so that the GEMM's CTA
+  // pairs start on the other SMs at once instead of waiting for this pass to
+  // leave them.
   int feeds_gemm = 0;
 };
 constexpr int kSkinnyFeedMaxCtas = 64;
+// One CTA streams its 128 rows at about 40 GB/s, so a 128-block (K = 8192)
+// pass holds its SMs for ~50 us.  Longer, the pairs it delays start a full
+// pass behind the others, which costs more than the overlap saves (at
+// K = 14336 a 64-CTA pass held 64 SMs for ~90 us): such a pass runs split
+// over all SMs before the GEMM instead.
+constexpr int kSkinnyFeedMaxKb = 128;
 // Runs one or two independent problems in one launch.
 cudaError_t launch_skinny(const SkinnyArgs *probs, int nprob, int num_sms, cudaStream_t s);
 int skinny_split(int rows, int K, int num_sms);

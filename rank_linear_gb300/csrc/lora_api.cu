@@ -222,7 +222,10 @@ Plan make_plan(int64_t M, int64_t d_in, int64_t d_out, int r, lora_dtype_t dt, i
     // forward: [B padded (r % 8 != 0)] [split partials] [split counters]
     size_t off = (r % 8) ? rup(size_t(d_out) * P.r_pad * 2, 256) : 0;
     P.fwd_ws_min = off;
-    if (pairs > 0 && M > 0) P.fsplit = main_gemm_plan(int(M), int(d_out), pairs, allow_wide);
+    // K blocks of a tile (main segment and extension), for the cost model
+    const int kb_fwd = static_cast<int>((d_in + 63) / 64 + (P.r_pad + 63) / 64);
+    const int kb_bwd = static_cast<int>((d_out + 63) / 64 + (P.r_pad + 63) / 64);
+    if (pairs > 0 && M > 0) P.fsplit = main_gemm_plan(int(M), int(d_out), pairs, allow_wide, kb_fwd);
     P.fsplit_off = off;
     off += rup(P.fsplit.partial_bytes, 256);
     P.fcnt_off = off;
@@ -237,7 +240,7 @@ Plan make_plan(int64_t M, int64_t d_in, int64_t d_out, int r, lora_dtype_t dt, i
     P.sgt_off = off;
     off += rup(size_t(P.r_pad) * P.Mp * 2, 256);
     const size_t base_end = off;
-    if (pairs > 0 && M > 0) P.bsplit = main_gemm_plan(int(M), int(d_in), pairs, allow_wide);
+    if (pairs > 0 && M > 0) P.bsplit = main_gemm_plan(int(M), int(d_in), pairs, allow_wide, kb_bwd);
     P.bsplit_off = off;
     off += rup(P.bsplit.partial_bytes, 256);
     P.bcnt_off = off;
@@ -409,9 +412,8 @@ lora_status_t bwd_bf16(const void *dY, const void *X, const void *W, const void 
   if (saved == nullptr) {  // recompute s X A^T into the workspace
     // with the forward's launch shape, so that the bits are the forward's
     const bool fwd_wide =
-        main_gemm_plan(static_cast<int>(M), static_cast<int>(d_out), main_gemm_pairs(false, di.sms),
-                       q4 == nullptr)
-            .wide;
+        make_plan(M, d_in, d_out, r, LORA_BF16, main_gemm_pairs(false, di.sms), q4 == nullptr)
+            .fsplit.wide;
     void *re = at(ws, P.resaved_off);
     LORA_TRY(down_fwd_bf16(di, P, X, A, s, r, M, d_in, re, st, nullptr, 0, fwd_wide));
     saved = re;
@@ -1266,8 +1268,15 @@ size_t lora_linear_workspace_bytes(int64_t M, int64_t d_in, int64_t d_out, int r
       pairs = main_gemm_pairs(false, sms);
     cudaGetLastError();
   }
-  const Plan P = make_plan(M, d_in, d_out, r, dtype, pairs);
-  return P.fwd_ws > P.bwd_ws ? P.fwd_ws : P.bwd_ws;
+  // room for the tail split of either tile width (the 4-bit layer, sized
+  // here too, has 256-wide tiles only)
+  size_t need = 0;
+  for (int allow_wide = 0; allow_wide < 2; ++allow_wide) {
+    const Plan P = make_plan(M, d_in, d_out, r, dtype, pairs, allow_wide != 0);
+    need = P.fwd_ws > need ? P.fwd_ws : need;
+    need = P.bwd_ws > need ? P.bwd_ws : need;
+  }
+  return need;
 }
 
 lora_status_t lora_linear_fwd(const void *X, const void *W, const void *A, const void *B,

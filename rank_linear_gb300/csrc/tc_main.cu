@@ -49,7 +49,9 @@
 //          (48 B/clock) instead of 32 KB for 512 (64 B/clock, above the
 //          ~58 B/clock the TMA feed sustains).  Eight epilogue warps drain
 //          half 0 first, so the next tile's half-0 MMAs start while half 1
-//          is still being written out.
+//          is still being written out.  A split wide tile's partial holds
+//          both halves (256 x 512 fp32 per pair), and its fix-up brings the
+//          other range's in one half at a time through the stage ring.
 #include <cuda_bf16.h>
 
 #include <atomic>
@@ -282,7 +284,7 @@ __global__ void __launch_bounds__(Q4 ? Q4_THREADS : WIDE ? WIDE_THREADS : NUM_TH
   static_assert(!(GATED && B_MN), "the gated pair reads K-major B");
   static_assert(!(FP8 && (B_MN || GATED || DUAL_B)), "the fp8 product reads K-major operands");
   static_assert(!(Q4 && (GATED || DUAL_B || FP8)), "4-bit W: plain layer only");
-  static_assert(!(WIDE && (SPLIT || GATED || DUAL_B || FP8 || Q4)), "wide tiles: plain layer, no split");
+  static_assert(!(WIDE && (GATED || DUAL_B || FP8 || Q4)), "wide tiles: plain layer only");
   // output columns per pair tile
   constexpr int TN = GATED ? BN / 2 : WIDE ? 2 * BN : BN;
   using G = Geo<BN, Q4, WIDE>;
@@ -335,7 +337,7 @@ __global__ void __launch_bounds__(Q4 ? Q4_THREADS : WIDE ? WIDE_THREADS : NUM_TH
     mbar_init(smem_u32(&tail->drain), 1);
     mbar_init(smem_u32(&tail->peer_done), 1);
     mbar_init(smem_u32(&tail->settled), 1);
-    mbar_init(smem_u32(&tail->ebar), 4);
+    mbar_init(smem_u32(&tail->ebar), G::EPI_WARPS);
     mbar_init(smem_u32(&tail->fix), 1);
     tail->abort_flag = 0;
     fence_barrier_init();
@@ -757,14 +759,14 @@ __global__ void __launch_bounds__(Q4 ? Q4_THREADS : WIDE ? WIDE_THREADS : NUM_TH
         const int row = row0 + lane;
         sc = (row < M ? __ldg(row_scale + row) : 0.f) * (w_scale != nullptr ? __ldg(w_scale) : 1.f);
       }
-      if constexpr (WIDE) {
+      // wide: this warp's columns of each accumulator half (cpart)
+      const int cpart = (warp - 2) >> 2;
+      if (WIDE && (!SPLIT || !split)) {
         // Eight warps: warp w drains its lane quadrant's rows, columns
         // [h*BN + p*BN/2, +BN/2) of half h (p = which of the two warps of
         // the quadrant), half 0 first; each half is released to the MMA
         // issuer as soon as all sixteen warps of the pair have drained it.
-        const int ew = warp - 2;
-        const int cpart = ew >> 2;
-        uint8_t *wstage = epi_stage + ew * EPI_WARP_BYTES;
+        uint8_t *wstage = epi_stage + (warp - 2) * EPI_WARP_BYTES;
 #pragma unroll 1
         for (int h = 0; h < 2; ++h) {
 #pragma unroll 1
@@ -783,7 +785,7 @@ __global__ void __launch_bounds__(Q4 ? Q4_THREADS : WIDE ? WIDE_THREADS : NUM_TH
         }
         continue;
       }
-      if (!SPLIT || !split) {
+      if (!WIDE && (!SPLIT || !split)) {
         if constexpr (GATED) {  // columns [0, TN) gate, [TN, 2 TN) up
 #pragma unroll 1
           for (int c = 0; c < TN / 32; ++c) {
@@ -817,21 +819,32 @@ __global__ void __launch_bounds__(Q4 ? Q4_THREADS : WIDE ? WIDE_THREADS : NUM_TH
       // ---- tail-split item (the last item of this pair): write the partial
       // [col][row] fp32, count in; the second to arrive adds the other one.
       // The accumulator is released only at the end (no item follows).
-      float *slot_mine = partials + static_cast<size_t>((rel * 2 + chunk) * 2 + q) * BM * BN;
-      float *slot_other = partials + static_cast<size_t>((rel * 2 + (chunk ^ 1)) * 2 + q) * BM * BN;
+      // Wide: the partial holds both accumulator halves (2 BN columns), and
+      // each of the eight warps takes its columns of each half.
+      constexpr int AC = WIDE ? 2 * BN : BN;  // accumulator columns
+      constexpr int HALVES = WIDE ? 2 : 1;
+      constexpr int WCOLS = WIDE ? BN / 2 : BN;  // this warp's columns of a half
+      float *slot_mine = partials + static_cast<size_t>((rel * 2 + chunk) * 2 + q) * BM * AC;
+      float *slot_other = partials + static_cast<size_t>((rel * 2 + (chunk ^ 1)) * 2 + q) * BM * AC;
+      const int cbase = WIDE ? cpart * (BN / 2) : 0;  // first column of this warp in a half
+      uint8_t *sstage = epi_stage + (WIDE ? (warp - 2) : qd) * EPI_WARP_BYTES;
 #pragma unroll 1
-      for (int c = 0; c < BN / 32; ++c) {
-        float v[32];
-        tmem_ld_32cols(taddr + c * 32, v);
+      for (int h = 0; h < HALVES; ++h) {
+#pragma unroll 1
+        for (int c = 0; c < WCOLS / 32; ++c) {
+          const int col = h * BN + cbase + c * 32;
+          float v[32];
+          tmem_ld_32cols(taddr + col, v);
 #pragma unroll
-        for (int i = 0; i < 32; ++i) slot_mine[(c * 32 + i) * BM + rl] = v[i];
+          for (int i = 0; i < 32; ++i) slot_mine[(col + i) * BM + rl] = v[i];
+        }
       }
       if (!dep_done) {  // the counters were zeroed by the preceding kernel
         griddep_wait();
         dep_done = true;
       }
       __threadfence();            // this thread's partial is visible GPU-wide
-      bool sync_ok = epi_sync();  // ... and so are the other 127 threads'
+      bool sync_ok = epi_sync();  // ... and so are the other threads'
       if (sync_ok && et == 0) {
         const unsigned prev = atomicAdd(&counters[rel * 2 + q], 1u);
         *last_flag = (prev == 1u) ? 1 : 0;
@@ -839,60 +852,82 @@ __global__ void __launch_bounds__(Q4 ? Q4_THREADS : WIDE ? WIDE_THREADS : NUM_TH
       sync_ok = sync_ok && epi_sync();
       const bool last = sync_ok && *reinterpret_cast<volatile int *>(last_flag) != 0;
       if (last) {
-        // The other range's partial (BM x BN fp32, column-major) comes in
-        // with bulk copies on one barrier, into the stage ring: a split item
-        // is its pair's last, so the ring's loads have all been consumed by
-        // the MMAs that completed this accumulator.  One round trip instead
-        // of a dependent chain of global loads per column block.
-        constexpr uint32_t PART_BYTES = BM * BN * 4, PIECE = 16384;
-        static_assert(PART_BYTES <= STAGES * STAGE_BYTES, "partial must fit the stage ring");
+        // The other range's partial (BM x AC fp32, column-major) comes in
+        // with bulk copies on one barrier, into the stage ring, one half
+        // (BM x BN, 128 KB) at a time: a split item is its pair's last, so
+        // the ring's loads have all been consumed by the MMAs that completed
+        // this accumulator.  One round trip per half instead of a dependent
+        // chain of global loads per column block.
+        constexpr uint32_t HALF_BYTES = BM * BN * 4, PIECE = 16384;
+        static_assert(HALF_BYTES <= STAGES * STAGE_BYTES, "a half partial must fit the stage ring");
         const uint32_t fix = smem_u32(&tail->fix);
-        if (et == 0) {
-          __threadfence();             // acquire: the other range's partial is final
-          fence_proxy_async_global();  // ... and ordered before the bulk reads
-          mbar_expect_tx(fix, PART_BYTES);
-          for (uint32_t o = 0; o < PART_BYTES; o += PIECE)
-            bulk_load(base + o, reinterpret_cast<const uint8_t *>(slot_other) + o, PIECE, fix);
-        }
-        const bool landed = mbar_wait(fix, 0, abort_flag, dev_status);
-        if (!__all_sync(0xffffffffu, landed)) {
-          if (et == 0) mbar_wait_drain(fix, 0);  // the copies in flight land first
-          break;
-        }
         const float *part = reinterpret_cast<const float *>(smem_raw + (base - raw));
-        if constexpr (GATED) {
+        bool round_ok = true;
 #pragma unroll 1
-          for (int c = 0; c < TN / 32; ++c) {
-            float g[32], u[32];
-            tmem_ld_32cols(taddr + c * 32, g);
-            tmem_ld_32cols(taddr + TN + c * 32, u);
-#pragma unroll
-            for (int i = 0; i < 32; ++i) {
-              g[i] += part[(c * 32 + i) * BM + rl];
-              u[i] += part[(TN + c * 32 + i) * BM + rl];
+        for (int h = 0; h < HALVES && round_ok; ++h) {
+          if (h > 0) {
+            // every thread's reads of the previous half precede the copies
+            // that overwrite it (generic reads, async-proxy writes)
+            fence_proxy_async_smem();
+            if (!epi_sync()) {
+              round_ok = false;
+              break;
             }
-            store_gated(g, u, stage, lane, out, aux0, aux1, ldo, row0, nb * TN + c * 32, M, N);
           }
-        } else {
+          if (et == 0) {
+            if (h == 0) {
+              __threadfence();             // acquire: the other range's partial is final
+              fence_proxy_async_global();  // ... and ordered before the bulk reads
+            }
+            mbar_expect_tx(fix, HALF_BYTES);
+            const uint8_t *src = reinterpret_cast<const uint8_t *>(slot_other) + h * HALF_BYTES;
+            for (uint32_t o = 0; o < HALF_BYTES; o += PIECE) bulk_load(base + o, src + o, PIECE, fix);
+          }
+          const bool landed = mbar_wait(fix, static_cast<uint32_t>(h) & 1u, abort_flag, dev_status);
+          if (!__all_sync(0xffffffffu, landed)) {
+            if (et == 0) mbar_wait_drain(fix, static_cast<uint32_t>(h) & 1u);  // copies land first
+            round_ok = false;
+            break;
+          }
+          if constexpr (GATED) {
 #pragma unroll 1
-          for (int c = 0; c < BN / 32; ++c) {
-            float o[32];
+            for (int c = 0; c < TN / 32; ++c) {
+              float g[32], u[32];
+              tmem_ld_32cols(taddr + c * 32, g);
+              tmem_ld_32cols(taddr + TN + c * 32, u);
 #pragma unroll
-            for (int i = 0; i < 32; ++i) o[i] = part[(c * 32 + i) * BM + rl];
-            float v[32];
-            tmem_ld_32cols(taddr + c * 32, v);
-            uint32_t pk[16];
+              for (int i = 0; i < 32; ++i) {
+                g[i] += part[(c * 32 + i) * BM + rl];
+                u[i] += part[(TN + c * 32 + i) * BM + rl];
+              }
+              store_gated(g, u, sstage, lane, out, aux0, aux1, ldo, row0, nb * TN + c * 32, M, N);
+            }
+          } else {
+#pragma unroll 1
+            for (int c = 0; c < WCOLS / 32; ++c) {
+              const int lc = cbase + c * 32;  // column within the half
+              float o[32];
 #pragma unroll
-            for (int i = 0; i < 16; ++i)
-              pk[i] = pack_bf16x2((v[2 * i] + o[2 * i]) * sc, (v[2 * i + 1] + o[2 * i + 1]) * sc);
-            store_chunk(pk, stage, lane, out, ldo, row0, nb * BN + c * 32, M, N);
+              for (int i = 0; i < 32; ++i) o[i] = part[(lc + i) * BM + rl];
+              float v[32];
+              tmem_ld_32cols(taddr + h * BN + lc, v);
+              uint32_t pk[16];
+#pragma unroll
+              for (int i = 0; i < 16; ++i)
+                pk[i] = pack_bf16x2((v[2 * i] + o[2 * i]) * sc, (v[2 * i + 1] + o[2 * i + 1]) * sc);
+              store_chunk(pk, sstage, lane, out, ldo, row0, nb * TN + h * BN + lc, M, N);
+            }
           }
         }
+        if (!round_ok) break;
       }
       if (sync_ok) sync_ok = epi_sync();  // the flag word is free again
       tc_fence_before();
       __syncwarp();
-      if (lane == 0) mbar_arrive_cluster(dsmem_map(smem_u32(&tail->tempty[acc]), 0));
+      if (lane == 0) {
+        mbar_arrive_cluster(dsmem_map(smem_u32(&tail->tempty[acc]), 0));
+        if (WIDE) mbar_arrive_cluster(dsmem_map(smem_u32(&tail->tempty[1]), 0));
+      }
       if (!sync_ok) break;
       }  // SPLIT
     }
@@ -1020,18 +1055,18 @@ int main_gemm_pairs(bool b_mn, int num_sms) {
 
 std::atomic<int> g_force_width{0};
 
-MainSplit main_gemm_split(int M, int N, int pairs) {
+MainSplit main_gemm_split(int M, int N, int pairs, int tile_n) {
   MainSplit sp;
   if (pairs < 2) return sp;
   const int m_pairs = ((M + BM - 1) / BM + 1) / 2;
-  const int tiles = m_pairs * ((N + 255) / 256);
+  const int tiles = m_pairs * ((N + tile_n - 1) / tile_n);
   const int rem = tiles % pairs;
   if (tiles <= pairs || rem == 0) return sp;  // one partial wave only, or none
   if (2 * rem > pairs) return sp;  // splitting would not shorten the last wave
   const int k = 2;
   sp.k = k;
   sp.rem = rem;
-  sp.partial_bytes = static_cast<size_t>(rem) * k * 2 * BM * 256 * sizeof(float);
+  sp.partial_bytes = static_cast<size_t>(rem) * k * 2 * BM * tile_n * sizeof(float);
   sp.counter_bytes = static_cast<size_t>(rem) * 2 * sizeof(unsigned);
   return sp;
 }
@@ -1045,25 +1080,33 @@ int main_gemm_pick_bn(int, int, int) { return 256; }
 // 512 of MMA); the wide one by its MMAs (1024 cycles per K block) plus the
 // drain of the half the next tile waits for.
 constexpr double kWideTileCost = 1.6;
-// Cost of a split tile's fix-up (partials out and in, the combine and the
-// drain), in 256 x 256 tile times.
-constexpr double kSplitFixupCost = 0.35;
+// A split tile's fix-up (its partial out, the other in, the combine and the
+// drain), in microseconds, against a K block's time in the tile: 8 us
+// against ~0.34 us for a 256-wide tile, 17 us against ~0.55 us for a
+// 512-wide one (its partial is twice as large).
+constexpr double kFixupNarrowUs = 8.0, kKbNarrowUs = 0.34;
+constexpr double kFixupWideUs = 17.0, kKbWideUs = 0.55;
 
-MainSplit main_gemm_plan(int M, int N, int pairs, bool allow_wide) {
-  MainSplit narrow = main_gemm_split(M, N, pairs);
+MainSplit main_gemm_plan(int M, int N, int pairs, bool allow_wide, int kb_total) {
+  MainSplit narrow = main_gemm_split(M, N, pairs, 256);
   const int force = g_force_width.load();
   if (!allow_wide || pairs < 1 || force == 256) return narrow;
+  MainSplit wide = main_gemm_split(M, N, pairs, 512);
+  wide.wide = true;
+  if (force == 512) return wide;
+  const int kb = kb_total > 0 ? kb_total : 1;
   const int m_pairs = ((M + BM - 1) / BM + 1) / 2;
   const int tn = m_pairs * ((N + 255) / 256), tw = m_pairs * ((N + 511) / 512);
-  const int rem = tn % pairs;
-  const double cost_n = tn / pairs + (rem == 0 ? 0.0 : narrow.k > 1 ? 0.5 + kSplitFixupCost : 1.0);
-  const double cost_w = ((tw + pairs - 1) / pairs) * kWideTileCost;
-  if (force == 512 || cost_w < cost_n) {
-    MainSplit w;
-    w.wide = true;
-    return w;
-  }
-  return narrow;
+  const int rem = tn % pairs, rem_w = tw % pairs;
+  // in 256 x 256 tile times
+  const double cost_n =
+      tn / pairs +
+      (rem == 0 ? 0.0 : narrow.k > 1 ? 0.5 + kFixupNarrowUs / (kb * kKbNarrowUs) : 1.0);
+  const double cost_w =
+      kWideTileCost * (tw / pairs + (rem_w == 0 ? 0.0
+                                                : wide.k > 1 ? 0.5 + kFixupWideUs / (kb * kKbWideUs)
+                                                             : 1.0));
+  return cost_w < cost_n ? wide : narrow;
 }
 
 void main_gemm_force_width(int w) { g_force_width.store(w); }
@@ -1073,10 +1116,13 @@ cudaError_t launch_main_gemm(const MainGemmArgs &a, int num_sms, cudaStream_t s)
   // preceding kernel and signals the next one.
   if (a.k_ext <= 0) return cudaErrorInvalidValue;
   const bool split = a.split_k > 1 && a.split_rem > 0;
-  if (a.wide) {  // 256 x 512 pair tiles: plain bf16 layer, whole tiles only
-    if (split || a.q4 || a.fp8 || a.gated || a.kb_switch >= 0) return cudaErrorInvalidValue;
-    return a.b_mn ? launch_variant<true, 256, false, false, false, false, false, true>(a, num_sms, s)
-                  : launch_variant<false, 256, false, false, false, false, false, true>(a, num_sms, s);
+  if (a.wide) {  // 256 x 512 pair tiles: plain bf16 layer
+    if (a.q4 || a.fp8 || a.gated || a.kb_switch >= 0) return cudaErrorInvalidValue;
+    if (a.b_mn)
+      return split ? launch_variant<true, 256, true, false, false, false, false, true>(a, num_sms, s)
+                   : launch_variant<true, 256, false, false, false, false, false, true>(a, num_sms, s);
+    return split ? launch_variant<false, 256, true, false, false, false, false, true>(a, num_sms, s)
+                 : launch_variant<false, 256, false, false, false, false, false, true>(a, num_sms, s);
   }
   if (a.q4) {  // 4-bit W: codes in tmB, bf16 group scales in tmB3
     if (a.fp8 || a.gated || a.kb_switch >= 0) return cudaErrorInvalidValue;

@@ -464,8 +464,9 @@ cudaError_t launch_skinny(const SkinnyArgs *probs, int nprob, int num_sms, cudaS
   }
   bool feeds = true;
   for (int i = 0; i < P.nprob; ++i) feeds = feeds && use[i]->feeds_gemm != 0;
-  const int S = (feeds && total_mt <= kSkinnyFeedMaxCtas) ? 1
-                                                          : skinny_split_launch(total_mt, max_kb, num_sms);
+  const int S = (feeds && total_mt <= kSkinnyFeedMaxCtas && max_kb <= kSkinnyFeedMaxKb)
+                    ? 1
+                    : skinny_split_launch(total_mt, max_kb, num_sms);
   P.S = S;
   size_t smem = 0;
   unsigned grid = 0;

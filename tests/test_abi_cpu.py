@@ -53,9 +53,16 @@ def test_sizes():
     # counters) + room for a recomputed saved buffer
     split = 28 * 2 * 2 * 128 * 256 * 4 + 256
     assert ws == 3 * 4096 * 16 * 2 + split + 4096 * 16 * 2 * 2
-    # shapes whose last wave is nearly full are not split
+    base = 16 * 14336 * 2 + 2 * 8192 * 16 * 2 + 8192 * 16 * 2 * 2
+    # gate/up: the dX GEMM (N = 4096, K = 14336 + 64) takes 256 x 512 tiles,
+    # 256 of them, 28 in the last wave, split 2 ways: 28 x 2 ranges x 2 CTAs x
+    # 128 x 512 fp32 + the counters
     ws2 = L.lora_linear_workspace_bytes(8192, 4096, 14336, 16, _lib.LORA_BF16)
-    assert ws2 == 16 * 14336 * 2 + 2 * 8192 * 16 * 2 + 8192 * 16 * 2 * 2
+    assert ws2 == base + 28 * 2 * 2 * 128 * 512 * 4 + 256
+    # shapes whose last wave is more than half full at either tile width
+    # (1792 or 896 tiles: 44 or 60 in the last wave) are not split
+    ws3 = L.lora_linear_workspace_bytes(8192, 14336, 14336, 16, _lib.LORA_BF16)
+    assert ws3 == base
     assert L.lora_linear_workspace_bytes(0, 64, 64, 16, _lib.LORA_BF16) == 0
 
 

@@ -317,6 +317,47 @@ def test_tail_split_path(gemm_width):
     assert rel_err(s1[1][rows], S.dx_rows(rows)) <= TOL["bf16"]
 
 
+def test_wide_tail_split_path(gemm_width):
+    """M = 2000, d_in = 5896, d_out = 6000 with 256 x 512 tiles: each GEMM
+    has 8 x 12 = 96 tiles, so on 76 CTA pairs the last wave's 20 are split
+    two ways, each range's partial holding both accumulator halves (the last
+    tile column ends past N, the last m-tile past M).  Given the full
+    workspace the split results are bitwise repeatable and differ from the
+    unsplit ones (minimal workspace); both agree with the oracle on every
+    element."""
+    gemm_width(512)
+    M, d_in, d_out, r, alpha = 2000, 5896, 6000, 24, 48.0
+    t = make_inputs(M, d_in, d_out, r, "bf16", seed=17, device=DEV)
+    X, W, A, B, dY = t["X"], t["W"], t["A"], t["B"], t["dY"]
+    full = torch.empty(rl.workspace_bytes(M, d_in, d_out, r, torch.bfloat16),
+                       dtype=torch.uint8, device=DEV)
+    rup = lambda n: (n + 255) // 256 * 256
+    r_pad = 32  # the rank padded to a multiple of 16
+    minimal = torch.empty(rup(r_pad * d_out * 2) + 2 * rup(r_pad * M * 2), dtype=torch.uint8,
+                          device=DEV)  # B^T, sG, sG^T
+    assert full.numel() > minimal.numel()
+
+    def run(ws):
+        Y, saved = rl.forward(X, W, A, B, alpha, workspace=ws)
+        dX, dA, dB = rl.backward(dY, X, W, A, B, alpha, saved, workspace=ws)
+        torch.cuda.synchronize()
+        rl.device_status()
+        return Y, dX, dA, dB
+
+    s1, s2, u = run(full), run(full), run(minimal)
+    for a, b in zip(s1, s2):
+        assert torch.equal(a, b)
+    assert not torch.equal(s1[0], u[0]) and not torch.equal(s1[1], u[1])  # the split ran
+    host = {k: v.cpu() for k, v in t.items()}
+    S = oracle.Sampled(host["X"], host["W"], host["A"], host["B"], host["dY"], alpha)
+    rows = np.arange(M)
+    ref = {"Y": S.y_rows_mm(rows), "dX": S.dx_rows_mm(rows), "dA": S.dA(), "dB": S.dB()}
+    for got in (s1, u):
+        errs = {k: rel_err(g, ref[k]) for k, g in zip(("Y", "dX", "dA", "dB"), got)}
+        for k, e in errs.items():
+            assert e <= TOL["bf16"], f"{k}: {e:.3e} ({errs})"
+
+
 @pytest.mark.parametrize("M,d", [(2048, 2048), (4096, 4096)])
 def test_back_to_back_backward_calls(M, d):
     """The dA pass starts in the dX GEMM's last wave without waiting for the
