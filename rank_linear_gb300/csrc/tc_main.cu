@@ -354,13 +354,16 @@ __global__ void __launch_bounds__(Q4 ? Q4_THREADS : WIDE ? WIDE_THREADS : NUM_TH
   // skinny pass producing sH or sG) waited for its own predecessor before
   // letting this grid start, so everything this kernel reads except the
   // low-rank operand of the K extension is already final, and nothing this
-  // kernel writes is read by it.  Only the producer waits, right before its
-  // first load of the extension; the main K segment overlaps the tail of
-  // the preceding kernel.  The producer also signals the next kernel, and
-  // only after that wait: once every CTA has signalled (or left), every
-  // kernel before this one has finished, which lets the backward's dA pass
-  // (it reads what the pass before this GEMM wrote) start on the SMs this
-  // grid frees before the grid has ended.
+  // kernel writes is read by it.  The producer waits right before its first
+  // load of the extension, so the main K segment overlaps the tail of the
+  // preceding kernel.  One epilogue thread per CTA waits for the same
+  // condition at the start and then signals the next kernel: once every
+  // CTA has signalled (or left), every kernel before this one has finished,
+  // which lets the backward's dA pass (it reads what the pass before this
+  // GEMM wrote) start on the SMs this grid frees before the grid has ended.
+  // (Signalling from the producer instead would wait for the extension of
+  // each pair's first tile, a whole tile late in a pair that started after
+  // the preceding pass left its SMs.)
   if (warp == 1) {
     tmem_alloc_pair(smem_u32(&tail->tmem_base), TMEM_COLS);
     tmem_relinquish_pair();
@@ -443,7 +446,6 @@ __global__ void __launch_bounds__(Q4 ? Q4_THREADS : WIDE ? WIDE_THREADS : NUM_TH
           }
           if (ext && !dep_done) {  // sH / sG come from the preceding kernel
             griddep_wait();
-            griddep_launch_dependents();
             dep_done = true;
           }
           const CUtensorMap *ta = ext ? &tmA2 : &tmA;
@@ -727,6 +729,10 @@ __global__ void __launch_bounds__(Q4 ? Q4_THREADS : WIDE ? WIDE_THREADS : NUM_TH
     // ------------------------------------------------------ epilogue (both CTAs)
     const int qd = warp & 3;  // TMEM lane quadrant this warp may access
     const int et = threadIdx.x - 64;  // 0..127 across the four epilogue warps
+    if (warp == 2 && lane == 0) {  // signal the next kernel (see above)
+      griddep_wait();
+      griddep_launch_dependents();
+    }
     int *last_flag = &tail->split_last;
     bool dep_done = false;
     uint32_t eph = 0;  // phase of ebar (the same sequence in every epilogue thread)
@@ -1113,7 +1119,7 @@ void main_gemm_force_width(int w) { g_force_width.store(w); }
 
 cudaError_t launch_main_gemm(const MainGemmArgs &a, int num_sms, cudaStream_t s) {
   // Every pair tile ends in the K extension, where the producer waits for the
-  // preceding kernel and signals the next one.
+  // preceding kernel.
   if (a.k_ext <= 0) return cudaErrorInvalidValue;
   const bool split = a.split_k > 1 && a.split_rem > 0;
   if (a.wide) {  // 256 x 512 pair tiles: plain bf16 layer
