@@ -142,22 +142,23 @@ struct __align__(16) MainTail {
 // all 32 banks.
 constexpr uint32_t EPI_PITCH = 64;
 constexpr uint32_t EPI_WARP_BYTES = 32 * EPI_PITCH;
-// Wide tiles: per epilogue warp, one 32 x 64 bf16 chunk, 128 bytes a row
-// (16-byte segment i of row r at slot i ^ (r & 7)), so that each global
-// store instruction writes four whole 128-byte row segments instead of
-// eight half segments: the drain of a half of the accumulator, bound by
-// the SM's stores, took 2.0 instead of 2.6 us.
+// All but the 4-bit kernel (which has no shared memory to spare): per
+// epilogue warp, one 32 x 64 bf16 chunk, 128 bytes a row (16-byte segment i
+// of row r at slot i ^ (r & 7)), so that each global store instruction
+// writes four whole 128-byte row segments instead of eight half segments:
+// the drain of a 256-column accumulator half, bound by the SM's stores,
+// took 2.0 instead of 2.6 us.
 constexpr uint32_t EPI_PITCH_W = 128;
 constexpr uint32_t EPI_WARP_BYTES_W = 32 * EPI_PITCH_W;
-template <bool WIDE>
+template <bool Q4>
 __host__ __device__ constexpr uint32_t epi_warp_bytes() {
-  return WIDE ? EPI_WARP_BYTES_W : EPI_WARP_BYTES;
+  return Q4 ? EPI_WARP_BYTES : EPI_WARP_BYTES_W;
 }
 
 template <int BN, bool Q4 = false, bool WIDE = false>
 constexpr size_t smem_bytes() {
   using G = Geo<BN, Q4, WIDE>;
-  return 1024 + size_t(G::STAGES) * G::STAGE_BYTES + G::EPI_WARPS * epi_warp_bytes<WIDE>() +
+  return 1024 + size_t(G::STAGES) * G::STAGE_BYTES + G::EPI_WARPS * epi_warp_bytes<Q4>() +
          sizeof(MainTail<G::STAGES>);
 }
 static_assert(smem_bytes<256, true>() <= 227 * 1024 && smem_bytes<256>() <= 227 * 1024 &&
@@ -332,7 +333,7 @@ __global__ void __launch_bounds__(Q4 ? Q4_THREADS : WIDE ? WIDE_THREADS : NUM_TH
   const uint32_t raw = smem_u32(smem_raw);
   const uint32_t base = (raw + 1023u) & ~1023u;  // 128-B swizzle atoms need 1 KB alignment
   uint8_t *epi_stage = smem_raw + (base - raw) + STAGES * STAGE_BYTES;
-  constexpr uint32_t EPI_WB = epi_warp_bytes<WIDE>();  // staging bytes per epilogue warp
+  constexpr uint32_t EPI_WB = epi_warp_bytes<Q4>();  // staging bytes per epilogue warp
   auto *tail = reinterpret_cast<MainTail<STAGES> *>(epi_stage + G::EPI_WARPS * EPI_WB);
   const uint32_t sA = base;
   const uint32_t sB = base + STAGES * A_BYTES;
@@ -841,19 +842,36 @@ __global__ void __launch_bounds__(Q4 ? Q4_THREADS : WIDE ? WIDE_THREADS : NUM_TH
             tmem_ld_32cols(taddr + TN + c * 32, u);
             store_gated(g, u, stage, lane, out, aux0, aux1, ldo, row0, nb * TN + c * 32, M, N);
           }
-        } else {
+        } else if constexpr (Q4) {
 #pragma unroll 1
           for (int c = 0; c < BN / 32; ++c) {
             float v[32];
             tmem_ld_32cols(taddr + c * 32, v);
-            if constexpr (FP8) {
-#pragma unroll
-              for (int i = 0; i < 32; ++i) v[i] *= sc;
-            }
             uint32_t pk[16];
 #pragma unroll
             for (int i = 0; i < 16; ++i) pk[i] = pack_bf16x2(v[2 * i], v[2 * i + 1]);
             store_chunk(pk, stage, lane, out, ldo, row0, nb * BN + c * 32, M, N);
+          }
+        } else {
+#pragma unroll 1
+          for (int c = 0; c < BN / 64; ++c) {  // 64 columns at a time
+            float v[32], u[32];
+            tmem_ld_32cols(taddr + c * 64, v);
+            tmem_ld_32cols(taddr + c * 64 + 32, u);
+            if constexpr (FP8) {
+#pragma unroll
+              for (int i = 0; i < 32; ++i) {
+                v[i] *= sc;
+                u[i] *= sc;
+              }
+            }
+            uint32_t pk[32];
+#pragma unroll
+            for (int i = 0; i < 16; ++i) {
+              pk[i] = pack_bf16x2(v[2 * i], v[2 * i + 1]);
+              pk[16 + i] = pack_bf16x2(u[2 * i], u[2 * i + 1]);
+            }
+            store_chunk128(pk, stage, lane, out, ldo, row0, nb * BN + c * 64, M, N);
           }
         }
         tc_fence_before();
