@@ -57,7 +57,7 @@ struct MainGemmArgs {
   // memory before the MMAs read it.
   bool q4 = false;
   // 256 x 512 pair tiles (two N = 256 MMAs per K step sharing A; plain bf16
-  // layer only); from main_gemm_plan
+  // and fp8 layers); from main_gemm_plan
   bool wide = false;
   // Test hook of the abort path (not with 4-bit W): the odd CTA of the first
   // pair never loads its first stage.

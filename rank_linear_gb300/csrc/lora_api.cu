@@ -971,9 +971,15 @@ struct FpPlan {
   MainSplit fsplit, bsplit;
 };
 
-FpPlan make_fp_plan(int64_t M, int64_t d_in, int64_t d_out, int r, int pairs_f, int pairs_b) {
+FpPlan make_fp_plan(int64_t M, int64_t d_in, int64_t d_out, int r, int pairs_f, int pairs_b,
+                    bool allow_wide = true) {
   FpPlan P;
   P.r_pad = static_cast<int>(rup(r, 16));
+  // K blocks of a tile (128-wide e4m3 main segment, 64-wide extension), for
+  // the tile-width cost model: an e4m3 block of 128 takes the MMA time of a
+  // bf16 block of 64
+  const int kb_f = static_cast<int>((d_in + 127) / 128 + (P.r_pad + 63) / 64);
+  const int kb_b = static_cast<int>((d_out + 127) / 128 + (P.r_pad + 63) / 64);
   P.Mp = rup(M, 8);
   // forward: [X codes] [X scales] [B / w_scale, padded] [split partials] [counters]
   size_t off = 0;
@@ -984,7 +990,7 @@ FpPlan make_fp_plan(int64_t M, int64_t d_in, int64_t d_out, int r, int pairs_f, 
   P.bs_off = off;
   off += rup(size_t(d_out) * P.r_pad * 2, 256);
   P.fwd_ws_min = M > 0 ? off : 0;
-  if (pairs_f > 0 && M > 0) P.fsplit = main_gemm_split(int(M), int(d_out), pairs_f);
+  if (pairs_f > 0 && M > 0) P.fsplit = main_gemm_plan(int(M), int(d_out), pairs_f, allow_wide, kb_f);
   P.fsplit_off = off;
   off += rup(P.fsplit.partial_bytes, 256);
   P.fcnt_off = off;
@@ -1006,7 +1012,7 @@ FpPlan make_fp_plan(int64_t M, int64_t d_in, int64_t d_out, int r, int pairs_f, 
   P.bt_off = off;
   if (r % 8) off += rup(size_t(P.r_pad) * d_out * 2, 256);
   P.bwd_ws_min = M > 0 ? off : 0;
-  if (pairs_b > 0 && M > 0) P.bsplit = main_gemm_split(int(M), int(d_in), pairs_b);
+  if (pairs_b > 0 && M > 0) P.bsplit = main_gemm_plan(int(M), int(d_in), pairs_b, allow_wide, kb_b);
   P.bsplit_off = off;
   off += rup(P.bsplit.partial_bytes, 256);
   P.bcnt_off = off;
@@ -1021,6 +1027,7 @@ lora_status_t fp8_fwd(const void *X, const void *Wq, const float *w_scale, const
   DevInfo di;
   LORA_TRY(device_info(di));
   FpPlan P = make_fp_plan(M, d_in, d_out, r, main_gemm_pairs(false, di.sms), 0);
+  const bool wide = P.fsplit.wide;  // 256 x 512 tiles (with or without the split)
   const bool split = P.fsplit.k > 1 && ws != nullptr && ws_bytes >= P.fwd_ws;
   if (!split) P = make_fp_plan(M, d_in, d_out, r, 0, 0);
   unsigned *counters = split ? reinterpret_cast<unsigned *>(at(ws, P.fcnt_off)) : nullptr;
@@ -1065,6 +1072,7 @@ lora_status_t fp8_fwd(const void *X, const void *Wq, const float *w_scale, const
   MainGemmArgs g;
   g.fp8 = true;
   g.bn = 256;
+  g.wide = wide;
   LORA_TRY(tmap_u8(&g.tmA, xq, d_in, M, d_in, 128, "X (e4m3)"));
   LORA_TRY(tmap_u8(&g.tmB, Wq, d_in, d_out, d_in, 128, "W (e4m3)"));
   LORA_TRY(tmap(&g.tmA2, saved, P.r_pad, M, P.r_pad * 2, 64, 128, "sH / row scale"));
@@ -1093,6 +1101,7 @@ lora_status_t fp8_bwd(const void *dY, const void *X, const void *WqT, const floa
   DevInfo di;
   LORA_TRY(device_info(di));
   FpPlan P = make_fp_plan(M, d_in, d_out, r, 0, main_gemm_pairs(false, di.sms));
+  const bool wide = P.bsplit.wide;
   const bool split = dX != nullptr && P.bsplit.k > 1 && ws != nullptr && ws_bytes >= P.bwd_ws;
   if (!split) P = make_fp_plan(M, d_in, d_out, r, 0, 0);
   unsigned *counters = split ? reinterpret_cast<unsigned *>(at(ws, P.bcnt_off)) : nullptr;
@@ -1162,6 +1171,7 @@ lora_status_t fp8_bwd(const void *dY, const void *X, const void *WqT, const floa
     MainGemmArgs b2;
     b2.fp8 = true;
     b2.bn = 256;
+    b2.wide = wide;
     LORA_TRY(tmap_u8(&b2.tmA, dq, d_out, M, d_out, 128, "dY (e4m3)"));
     LORA_TRY(tmap_u8(&b2.tmB, WqT, d_out, d_in, d_out, 128, "W^T (e4m3)"));
     LORA_TRY(tmap(&b2.tmA2, sG, P.r_pad, M, P.r_pad * 2, 64, 128, "sG / row scale"));
@@ -1481,8 +1491,15 @@ lora_status_t lora_fp8_quantize_rows(const void *x, int64_t rows, int64_t cols, 
 
 size_t lora_fp8_workspace_bytes(int64_t M, int64_t d_in, int64_t d_out, int r) {
   if (M < 0 || d_in < 1 || d_out < 1 || r < 1 || r > 256) return 0;
-  const FpPlan P = make_fp_plan(M, d_in, d_out, r, current_pairs(false), current_pairs(false));
-  return P.fwd_ws > P.bwd_ws ? P.fwd_ws : P.bwd_ws;
+  // room for the tail split of either tile width
+  size_t need = 0;
+  for (int allow_wide = 0; allow_wide < 2; ++allow_wide) {
+    const FpPlan P = make_fp_plan(M, d_in, d_out, r, current_pairs(false), current_pairs(false),
+                                  allow_wide != 0);
+    need = P.fwd_ws > need ? P.fwd_ws : need;
+    need = P.bwd_ws > need ? P.bwd_ws : need;
+  }
+  return need;
 }
 
 lora_status_t lora_fp8_fwd(const void *X, const void *Wq, const float *w_scale, const void *A,

@@ -42,7 +42,7 @@
 //   Q4     a 4-bit W: each stage carries packed codes and bf16 group scales,
 //          and six groups of two extra warps (one per ring stage) expand
 //          them into the bf16 B tile in shared memory;
-//   WIDE   256 x 512 pair tiles for the plain layer: each K step issues two
+//   WIDE   256 x 512 pair tiles for the plain and fp8 layers: each K step issues two
 //          N = 256 pair MMAs that share the stage's A tile, into the two
 //          256-column halves of TMEM (one accumulator, no double buffer).
 //          Per SM a K block then moves A 16 KB + B 32 KB for 1024 MMA cycles
@@ -321,7 +321,7 @@ __global__ void __launch_bounds__(Q4 ? Q4_THREADS : WIDE ? WIDE_THREADS : NUM_TH
   static_assert(!(GATED && B_MN), "the gated pair reads K-major B");
   static_assert(!(FP8 && (B_MN || GATED || DUAL_B)), "the fp8 product reads K-major operands");
   static_assert(!(Q4 && (GATED || DUAL_B || FP8)), "4-bit W: plain layer only");
-  static_assert(!(WIDE && (GATED || DUAL_B || FP8 || Q4)), "wide tiles: plain layer only");
+  static_assert(!(WIDE && (GATED || DUAL_B || Q4)), "wide tiles: plain and fp8 layers only");
   // output columns per pair tile
   constexpr int TN = GATED ? BN / 2 : WIDE ? 2 * BN : BN;
   using G = Geo<BN, Q4, WIDE>;
@@ -656,9 +656,14 @@ __global__ void __launch_bounds__(Q4 ? Q4_THREADS : WIDE ? WIDE_THREADS : NUM_TH
             const uint64_t bd1 = bd + (B_HALF >> 4);
             if (kb < kb_main) {
 #pragma unroll
-              for (int kk = 0; kk < BK / 16; ++kk)
-                tc_mma_bf16_pair(d + BN, ad + kk * A_STEP, bd1 + kk * B_STEP, idesc,
+              for (int kk = 0; kk < BK / 16; ++kk) {
+                if constexpr (FP8)
+                  tc_mma_f8_pair(d + BN, ad + kk * A_STEP, bd1 + kk * B_STEP, idesc8,
                                  kk ? 1u : accum);
+                else
+                  tc_mma_bf16_pair(d + BN, ad + kk * A_STEP, bd1 + kk * B_STEP, idesc,
+                                   kk ? 1u : accum);
+              }
             } else {
               for (int kk = 0; kk < nk; ++kk)
                 tc_mma_bf16_pair(d + BN, ad + kk * A_STEP, bd1 + kk * B_STEP, idesc,
@@ -819,6 +824,13 @@ __global__ void __launch_bounds__(Q4 ? Q4_THREADS : WIDE ? WIDE_THREADS : NUM_TH
             float v[32], u[32];
             tmem_ld_32cols(taddr + col, v);
             tmem_ld_32cols(taddr + col + 32, u);
+            if constexpr (FP8) {
+#pragma unroll
+              for (int i = 0; i < 32; ++i) {
+                v[i] *= sc;
+                u[i] *= sc;
+              }
+            }
             uint32_t pk[32];
 #pragma unroll
             for (int i = 0; i < 16; ++i) {
@@ -1181,8 +1193,13 @@ cudaError_t launch_main_gemm(const MainGemmArgs &a, int num_sms, cudaStream_t s)
   // preceding kernel.
   if (a.k_ext <= 0) return cudaErrorInvalidValue;
   const bool split = a.split_k > 1 && a.split_rem > 0;
-  if (a.wide) {  // 256 x 512 pair tiles: plain bf16 layer
-    if (a.q4 || a.fp8 || a.gated || a.kb_switch >= 0) return cudaErrorInvalidValue;
+  if (a.wide) {  // 256 x 512 pair tiles: plain bf16 and fp8 layers
+    if (a.q4 || a.gated || a.kb_switch >= 0) return cudaErrorInvalidValue;
+    if (a.fp8) {
+      if (a.b_mn || !a.row_scale) return cudaErrorInvalidValue;
+      return split ? launch_variant<false, 256, true, false, false, true, false, true>(a, num_sms, s)
+                   : launch_variant<false, 256, false, false, false, true, false, true>(a, num_sms, s);
+    }
     if (a.b_mn)
       return split ? launch_variant<true, 256, true, false, false, false, false, true>(a, num_sms, s)
                    : launch_variant<true, 256, false, false, false, false, false, true>(a, num_sms, s);

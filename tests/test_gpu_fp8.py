@@ -81,8 +81,22 @@ SMALL = [
 ]
 
 
+@pytest.fixture
+def gemm_width():
+    """Forces the main GEMMs' tile width for one test, then restores the
+    cost model's choice."""
+    from rank_linear_gb300 import _lib
+    L = _lib.lib()
+    yield lambda w: _lib.check(L.lora_debug_gemm_width(w), "gemm width")
+    L.lora_debug_gemm_width(0)
+
+
+@pytest.mark.parametrize("width", [256, 512])
 @pytest.mark.parametrize("shape", SMALL, ids=lambda s: "x".join(map(str, s[:4])))
-def test_small_against_oracle(shape):
+def test_small_against_oracle(shape, width, gemm_width):
+    """Both GEMMs with 256 x 256 pair tiles (tail split where it applies) and
+    with 256 x 512 pair tiles."""
+    gemm_width(width)
     M, d_in, d_out, r, alpha = shape
     t = inputs(M, d_in, d_out, r, seed=sum(shape[:4]))
     got = run_gpu(t, alpha)
@@ -91,6 +105,47 @@ def test_small_against_oracle(shape):
     errs = {n: rel_err(g, e) for n, g, e in zip(("Y", "dX", "dA", "dB"), got, ref)}
     for n, e in errs.items():
         assert e <= TOL, f"{n}: {e:.3e} ({errs})"
+
+
+def test_wide_tail_split_path(gemm_width):
+    """M = 2000, d_in = 5888, d_out = 6000 with 256 x 512 tiles: each GEMM has
+    8 x 12 = 96 tiles, so on 76 CTA pairs the last wave's 20 are split in two
+    K ranges (e4m3 main segment, bf16 extension in the same accumulator, the
+    row scale applied after the two partials are added).  Given the full
+    workspace the results are bitwise repeatable and differ from the unsplit
+    ones (minimal workspace); both agree with the oracle on every element."""
+    gemm_width(512)
+    M, d_in, d_out, r, alpha = 2000, 5888, 6000, 24, 48.0
+    t = inputs(M, d_in, d_out, r, seed=23)
+    g = {k: v.to(DEV) for k, v in t.items()}
+    qw = rl.quantize_w_fp8(g["W"])
+    rup = lambda n: (n + 255) // 256 * 256
+    r_pad = 32
+    fwd_min = rup(M * d_in) + rup(M * 4) + rup(d_out * r_pad * 2)
+    bwd_min = (rup(M * d_out) + rup(M * 4) + rup(M * r_pad * 2) + rup(r_pad * M * 2)
+               + rup(d_in * r_pad * 2))
+    full = torch.empty(rl.fp8_workspace_bytes(M, d_in, d_out, r), dtype=torch.uint8, device=DEV)
+    minimal = torch.empty(max(fwd_min, bwd_min), dtype=torch.uint8, device=DEV)
+    assert full.numel() > minimal.numel()
+
+    def run(ws):
+        Y, saved = rl.fp8_forward(g["X"], qw, g["A"], g["B"], alpha, workspace=ws)
+        dX, dA, dB = rl.fp8_backward(g["dY"], g["X"], qw, g["A"], g["B"], alpha, saved,
+                                     workspace=ws)
+        torch.cuda.synchronize()
+        rl.device_status()
+        return Y, dX, dA, dB
+
+    s1, s2, u = run(full), run(full), run(minimal)
+    for a, b in zip(s1, s2):
+        assert torch.equal(a, b)
+    assert not torch.equal(s1[0], u[0]) and not torch.equal(s1[1], u[1])  # the split ran
+    _, Yr = ofp8.forward(t["X"], t["W"], t["A"], t["B"], alpha)
+    ref = (Yr,) + tuple(ofp8.backward(t["dY"], t["X"], t["W"], t["A"], t["B"], alpha))
+    for got in (s1, u):
+        errs = {n: rel_err(x, e) for n, x, e in zip(("Y", "dX", "dA", "dB"), got, ref)}
+        for n, e in errs.items():
+            assert e <= TOL, f"{n}: {e:.3e} ({errs})"
 
 
 def test_q_proj_shape_full_size():
