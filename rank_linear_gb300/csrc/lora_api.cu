@@ -667,11 +667,14 @@ struct SwPlan {
   MainSplit fsplit, bsplit;
 };
 
-SwPlan make_sw_plan(int64_t M, int64_t d_in, int64_t d_ff, int r, int pairs_f, int pairs_b) {
+SwPlan make_sw_plan(int64_t M, int64_t d_in, int64_t d_ff, int r, int pairs_f, int pairs_b,
+                    bool allow_wide = true) {
   SwPlan P;
   P.r_pad = static_cast<int>(rup(r, 16));
   P.Mp = rup(M, 8);
   P.half = rup(d_ff, 64);
+  // K blocks of a dX GEMM tile, [d_gate | d_up] and the extension [sG_g | sG_u]
+  const int kb_b = static_cast<int>(2 * P.half / 64 + (2 * P.r_pad + 63) / 64);
   const size_t act = rup(size_t(M) * d_ff * 2, 256);
   const size_t tr = rup(size_t(P.r_pad) * P.Mp * 2, 256);
   // saved: [gate] [up] [sH_g | sH_u] [sH_g^T] [sH_u^T]
@@ -721,7 +724,7 @@ SwPlan make_sw_plan(int64_t M, int64_t d_in, int64_t d_ff, int r, int pairs_f, i
     if (r % 8) off += rup(size_t(P.r_pad) * d_ff * 2, 256);
   }
   P.bwd_ws_min = M > 0 ? off : 0;
-  if (pairs_b > 0 && M > 0) P.bsplit = main_gemm_split(int(M), int(d_in), pairs_b);
+  if (pairs_b > 0 && M > 0) P.bsplit = main_gemm_plan(int(M), int(d_in), pairs_b, allow_wide, kb_b);
   P.bsplit_off = off;
   off += rup(P.bsplit.partial_bytes, 256);
   P.bcnt_off = off;
@@ -819,6 +822,7 @@ lora_status_t sw_bwd_bf16(const void *dH, const void *X, const void *Wg, const v
   DevInfo di;
   LORA_TRY(device_info(di));
   SwPlan P = make_sw_plan(M, d_in, d_ff, r, 0, main_gemm_pairs(true, di.sms));
+  const bool wide = P.bsplit.wide;  // the dX GEMM's tile width (with or without the split)
   const bool split = dX != nullptr && P.bsplit.k > 1 && ws != nullptr && ws_bytes >= P.bwd_ws;
   if (!split) P = make_sw_plan(M, d_in, d_ff, r, 0, 0);
   unsigned *counters = split ? reinterpret_cast<unsigned *>(at(ws, P.bcnt_off)) : nullptr;
@@ -895,6 +899,7 @@ lora_status_t sw_bwd_bf16(const void *dH, const void *X, const void *Wg, const v
     }));
     MainGemmArgs b2;
     b2.bn = 256;
+    b2.wide = wide;
     LORA_TRY(tmap(&b2.tmA, D, 2 * half, M, 2 * half * 2, 64, 128, "[d_gate | d_up]"));
     LORA_TRY(tmap(&b2.tmB, Wg, d_in, d_ff, d_in * 2, 64, 64, "Wg (MN-major)"));
     LORA_TRY(tmap(&b2.tmB3, Wu, d_in, d_ff, d_in * 2, 64, 64, "Wu (MN-major)"));
@@ -1584,8 +1589,15 @@ size_t lora_swiglu_saved_bytes(int64_t M, int64_t d_ff, int r) {
 
 size_t lora_swiglu_workspace_bytes(int64_t M, int64_t d_in, int64_t d_ff, int r) {
   if (M < 0 || d_in < 1 || d_ff < 1 || r < 1 || r > 256) return 0;
-  const SwPlan P = make_sw_plan(M, d_in, d_ff, r, current_pairs(false), current_pairs(true));
-  return P.fwd_ws > P.bwd_ws ? P.fwd_ws : P.bwd_ws;
+  // room for the dX GEMM's tail split at either tile width
+  size_t need = 0;
+  for (int allow_wide = 0; allow_wide < 2; ++allow_wide) {
+    const SwPlan P = make_sw_plan(M, d_in, d_ff, r, current_pairs(false), current_pairs(true),
+                                  allow_wide != 0);
+    need = P.fwd_ws > need ? P.fwd_ws : need;
+    need = P.bwd_ws > need ? P.bwd_ws : need;
+  }
+  return need;
 }
 
 lora_status_t lora_swiglu_fwd(const void *X, const void *Wg, const void *Ag, const void *Bg,

@@ -42,7 +42,7 @@
 //   Q4     a 4-bit W: each stage carries packed codes and bf16 group scales,
 //          and six groups of two extra warps (one per ring stage) expand
 //          them into the bf16 B tile in shared memory;
-//   WIDE   256 x 512 pair tiles for the plain and fp8 layers: each K step issues two
+//   WIDE   256 x 512 pair tiles (plain and fp8 layers, DUAL_B): each K step issues two
 //          N = 256 pair MMAs that share the stage's A tile, into the two
 //          256-column halves of TMEM (one accumulator, no double buffer).
 //          Per SM a K block then moves A 16 KB + B 32 KB for 1024 MMA cycles
@@ -321,7 +321,7 @@ __global__ void __launch_bounds__(Q4 ? Q4_THREADS : WIDE ? WIDE_THREADS : NUM_TH
   static_assert(!(GATED && B_MN), "the gated pair reads K-major B");
   static_assert(!(FP8 && (B_MN || GATED || DUAL_B)), "the fp8 product reads K-major operands");
   static_assert(!(Q4 && (GATED || DUAL_B || FP8)), "4-bit W: plain layer only");
-  static_assert(!(WIDE && (GATED || DUAL_B || Q4)), "wide tiles: plain and fp8 layers only");
+  static_assert(!(WIDE && (GATED || Q4)), "wide tiles: not the gated or 4-bit GEMMs");
   // output columns per pair tile
   constexpr int TN = GATED ? BN / 2 : WIDE ? 2 * BN : BN;
   using G = Geo<BN, Q4, WIDE>;
@@ -1193,8 +1193,13 @@ cudaError_t launch_main_gemm(const MainGemmArgs &a, int num_sms, cudaStream_t s)
   // preceding kernel.
   if (a.k_ext <= 0) return cudaErrorInvalidValue;
   const bool split = a.split_k > 1 && a.split_rem > 0;
-  if (a.wide) {  // 256 x 512 pair tiles: plain bf16 and fp8 layers
-    if (a.q4 || a.gated || a.kb_switch >= 0) return cudaErrorInvalidValue;
+  if (a.wide) {  // 256 x 512 pair tiles: plain bf16 and fp8 layers, the gated pair's dX GEMM
+    if (a.q4 || a.gated) return cudaErrorInvalidValue;
+    if (a.kb_switch >= 0) {
+      if (!a.b_mn || a.fp8) return cudaErrorInvalidValue;
+      return split ? launch_variant<true, 256, true, false, true, false, false, true>(a, num_sms, s)
+                   : launch_variant<true, 256, false, false, true, false, false, true>(a, num_sms, s);
+    }
     if (a.fp8) {
       if (a.b_mn || !a.row_scale) return cudaErrorInvalidValue;
       return split ? launch_variant<false, 256, true, false, false, true, false, true>(a, num_sms, s)

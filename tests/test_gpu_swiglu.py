@@ -103,8 +103,20 @@ SMALL = [
 ]
 
 
+@pytest.fixture
+def gemm_width():
+    """Forces the tile width of the GEMMs that may take 256 x 512 tiles (here
+    the dX GEMM) for one test, then restores the cost model's choice."""
+    from rank_linear_gb300 import _lib
+    L = _lib.lib()
+    yield lambda w: _lib.check(L.lora_debug_gemm_width(w), "gemm width")
+    L.lora_debug_gemm_width(0)
+
+
+@pytest.mark.parametrize("width", [256, 512])
 @pytest.mark.parametrize("shape", SMALL, ids=lambda s: "x".join(map(str, s[:4])))
-def test_small_against_oracle(shape):
+def test_small_against_oracle(shape, width, gemm_width):
+    gemm_width(width)
     M, d_in, d_ff, r, alpha = shape
     t = make_pair(M, d_in, d_ff, r, seed=sum(shape[:4]))
     got = run_gpu(t, alpha)
@@ -113,6 +125,49 @@ def test_small_against_oracle(shape):
     errs = {n: rel_err(g, e) for n, g, e in zip(NAMES, got, ref)}
     for n, g, e, b in zip(NAMES, got, ref, bound):
         assert meets_bar(g, e, b), f"{n}: {errs[n]:.3e} ({errs})"
+
+
+def test_wide_dx_tail_split(gemm_width):
+    """M = 2000, d_in = 6000, d_ff = 1024: the dX GEMM over [d_gate | d_up]
+    (its B map switching from Wg to Wu mid-K) with 256 x 512 tiles has 8 x 12
+    = 96 tiles, so on 76 CTA pairs the last wave's 20 are split in two K
+    ranges.  Given the full workspace the results are bitwise repeatable and
+    dX differs from the unsplit one (minimal workspace); both agree with the
+    oracle on every element."""
+    gemm_width(512)
+    M, d_in, d_ff, r, alpha = 2000, 6000, 1024, 24, 48.0
+    t = make_pair(M, d_in, d_ff, r, seed=71)
+    g = {k: v.to(DEV) for k, v in t.items()}
+    args = [g[k] for k in ("Wg", "Ag", "Bg", "Wu", "Au", "Bu")]
+    rup = lambda n: (n + 255) // 256 * 256
+    half, r_pad = 1024, 32
+    bwd_min = (rup(M * 2 * half * 2) + rup(M * 2 * r_pad * 2) + 2 * rup(r_pad * M * 2)
+               + rup(2 * r_pad * d_in * 2))
+    full = torch.empty(rl.swiglu_workspace_bytes(M, d_in, d_ff, r), dtype=torch.uint8, device=DEV)
+    minimal = torch.empty(bwd_min, dtype=torch.uint8, device=DEV)
+    assert full.numel() > minimal.numel()
+    H, saved = rl.swiglu_forward(g["X"], *args, alpha, workspace=full)
+
+    def run(ws):
+        grads = rl.swiglu_backward(g["dH"], g["X"], *args, alpha, saved, workspace=ws)
+        torch.cuda.synchronize()
+        rl.device_status()
+        return grads
+
+    s1, s2, u = run(full), run(full), run(minimal)
+    for a, b in zip(s1, s2):
+        assert torch.equal(a, b)
+    assert not torch.equal(s1[0], u[0])  # the split ran
+    hargs = [t[k] for k in ("X", "Wg", "Ag", "Bg", "Wu", "Au", "Bu")]
+    smp = osw.SampledRows(*hargs, t["dH"], alpha)
+    rows = np.arange(M)
+    ref_h = smp.h_rows_mm(rows)
+    ref = (smp.dx_rows_mm(rows),) + tuple(osw.adapter_grads_mm(t["dH"], *hargs, alpha))
+    assert rel_err(H, ref_h) <= TOL
+    for got in (s1, u):
+        errs = {n: rel_err(x, e) for n, x, e in zip(NAMES[1:], got, ref)}
+        for n, e in errs.items():
+            assert e <= TOL, f"{n}: {e:.3e} ({errs})"
 
 
 def test_full_gate_up():
