@@ -56,8 +56,8 @@ struct MainGemmArgs {
   // 64 x 2).  Each CTA dequantises its half of the B tile to bf16 in shared
   // memory before the MMAs read it.
   bool q4 = false;
-  // 256 x 512 pair tiles (two N = 256 MMAs per K step sharing A; plain bf16
-  // and fp8 layers); from main_gemm_plan
+  // 256 x 512 pair tiles (two N = 256 MMAs per K step sharing A; all but the
+  // 4-bit W; gated: 256 outputs of both projections); from main_gemm_plan
   bool wide = false;
   // Test hook of the abort path (not with 4-bit W): the odd CTA of the first
   // pair never loads its first stage.
@@ -75,7 +75,8 @@ struct MainSplit {
 // Tail split for an M x N output on `pairs` CTA pairs in 256 x tile_n pair
 // tiles: the last wave's rem tiles are split two ways (K ranges) when
 // 2 * rem <= pairs.  For the gated pair pass N = 2 x roundup(output columns,
-// 128) (tiles of 128 columns).
+// 128): a pair tile of 256 (512) columns holds 128 (256) outputs of both
+// projections.
 MainSplit main_gemm_split(int M, int N, int pairs, int tile_n = 256);
 // The plain layer's choice between 256 x 512 and 256 x 256 tiles, each with
 // its tail split where that applies, by a cost model of the waves that

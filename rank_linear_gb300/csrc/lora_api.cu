@@ -673,7 +673,9 @@ SwPlan make_sw_plan(int64_t M, int64_t d_in, int64_t d_ff, int r, int pairs_f, i
   P.r_pad = static_cast<int>(rup(r, 16));
   P.Mp = rup(M, 8);
   P.half = rup(d_ff, 64);
-  // K blocks of a dX GEMM tile, [d_gate | d_up] and the extension [sG_g | sG_u]
+  // K blocks of a tile, for the tile-width cost model: the gated GEMM's X and
+  // [sH_g | sH_u], the dX GEMM's [d_gate | d_up] and [sG_g | sG_u]
+  const int kb_f = static_cast<int>((d_in + 63) / 64 + (2 * P.r_pad + 63) / 64);
   const int kb_b = static_cast<int>(2 * P.half / 64 + (2 * P.r_pad + 63) / 64);
   const size_t act = rup(size_t(M) * d_ff * 2, 256);
   const size_t tr = rup(size_t(P.r_pad) * P.Mp * 2, 256);
@@ -700,7 +702,8 @@ SwPlan make_sw_plan(int64_t M, int64_t d_in, int64_t d_ff, int r, int pairs_f, i
   P.shws_off = off;
   off += rup(size_t(M) * 2 * P.r_pad * 2, 256);
   P.fwd_ws_min = M > 0 ? off : 0;
-  if (pairs_f > 0 && M > 0) P.fsplit = main_gemm_split(int(M), int(2 * rup(d_ff, 128)), pairs_f);
+  if (pairs_f > 0 && M > 0)
+    P.fsplit = main_gemm_plan(int(M), int(2 * rup(d_ff, 128)), pairs_f, allow_wide, kb_f);
   P.fsplit_off = off;
   off += rup(P.fsplit.partial_bytes, 256);
   P.fcnt_off = off;
@@ -740,6 +743,7 @@ lora_status_t sw_fwd_bf16(const void *X, const void *Wg, const void *Ag, const v
   DevInfo di;
   LORA_TRY(device_info(di));
   SwPlan P = make_sw_plan(M, d_in, d_ff, r, main_gemm_pairs(false, di.sms), 0);
+  const bool wide = P.fsplit.wide;  // the gated GEMM's tile width
   const bool split = P.fsplit.k > 1 && ws != nullptr && ws_bytes >= P.fwd_ws;
   if (!split) P = make_sw_plan(M, d_in, d_ff, r, 0, 0);
   unsigned *counters = split ? reinterpret_cast<unsigned *>(at(ws, P.fcnt_off)) : nullptr;
@@ -788,6 +792,7 @@ lora_status_t sw_fwd_bf16(const void *X, const void *Wg, const void *Ag, const v
   MainGemmArgs g;
   g.gated = true;
   g.bn = 256;
+  g.wide = wide;
   LORA_TRY(tmap(&g.tmA, X, d_in, M, d_in * 2, 64, 128, "X"));
   LORA_TRY(tmap(&g.tmB, Wg, d_in, d_ff, d_in * 2, 64, 128, "Wg"));
   LORA_TRY(tmap(&g.tmB3, Wu, d_in, d_ff, d_in * 2, 64, 128, "Wu"));

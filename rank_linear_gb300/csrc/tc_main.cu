@@ -42,7 +42,8 @@
 //   Q4     a 4-bit W: each stage carries packed codes and bf16 group scales,
 //          and six groups of two extra warps (one per ring stage) expand
 //          them into the bf16 B tile in shared memory;
-//   WIDE   256 x 512 pair tiles (plain and fp8 layers, DUAL_B): each K step issues two
+//   WIDE   256 x 512 pair tiles (all but Q4; gated: 256 outputs of both
+//          projections, half h the gate and up of 128): each K step issues two
 //          N = 256 pair MMAs that share the stage's A tile, into the two
 //          256-column halves of TMEM (one accumulator, no double buffer).
 //          Per SM a K block then moves A 16 KB + B 32 KB for 1024 MMA cycles
@@ -321,9 +322,11 @@ __global__ void __launch_bounds__(Q4 ? Q4_THREADS : WIDE ? WIDE_THREADS : NUM_TH
   static_assert(!(GATED && B_MN), "the gated pair reads K-major B");
   static_assert(!(FP8 && (B_MN || GATED || DUAL_B)), "the fp8 product reads K-major operands");
   static_assert(!(Q4 && (GATED || DUAL_B || FP8)), "4-bit W: plain layer only");
-  static_assert(!(WIDE && (GATED || Q4)), "wide tiles: not the gated or 4-bit GEMMs");
-  // output columns per pair tile
-  constexpr int TN = GATED ? BN / 2 : WIDE ? 2 * BN : BN;
+  static_assert(!(WIDE && Q4), "wide tiles: not the 4-bit GEMM");
+  // output columns per pair tile; the gated pair's accumulator half h holds
+  // gate (columns h*BN + [0, GH)) and up (h*BN + [GH, BN)) of GH outputs
+  constexpr int GH = BN / 2;
+  constexpr int TN = GATED ? GH * (WIDE ? 2 : 1) : WIDE ? 2 * BN : BN;
   using G = Geo<BN, Q4, WIDE>;
   constexpr int STAGES = G::STAGES;
   constexpr uint32_t B_BYTES = G::B_BYTES, STAGE_BYTES = G::STAGE_BYTES, PAIR_TX = G::PAIR_TX;
@@ -514,7 +517,7 @@ __global__ void __launch_bounds__(Q4 ? Q4_THREADS : WIDE ? WIDE_THREADS : NUM_TH
               for (int j = 0; j < BN / 128; ++j)
                 tma_load_2d_pair(b_dst + j * 8192u, tb, full, n0 + h * BN + 64 * j, kB);
             } else {  // BN/2 rows of [N x 64 K]
-              tma_load_2d_pair(b_dst, tb, full, kB, n0 + h * BN);
+              tma_load_2d_pair(b_dst, tb, full, kB, n0 + h * (GATED ? GH : BN));
             }
           }
           issued[stage] += 1;
@@ -810,7 +813,27 @@ __global__ void __launch_bounds__(Q4 ? Q4_THREADS : WIDE ? WIDE_THREADS : NUM_TH
       }
       // wide: this warp's columns of each accumulator half (cpart)
       const int cpart = (warp - 2) >> 2;
-      if (WIDE && (!SPLIT || !split)) {
+      if (WIDE && GATED && (!SPLIT || !split)) {
+        // as below, each half's GH outputs in four 32-column chunks, two
+        // per warp of the quadrant: silu(gate) * up, gate, up
+        uint8_t *wstage = epi_stage + (warp - 2) * EPI_WB;
+#pragma unroll 1
+        for (int h = 0; h < 2; ++h) {
+#pragma unroll 1
+          for (int c = cpart * (GH / 64); c < (cpart + 1) * (GH / 64); ++c) {
+            float g[32], u[32];
+            tmem_ld_32cols(taddr + h * BN + c * 32, g);
+            tmem_ld_32cols(taddr + h * BN + GH + c * 32, u);
+            store_gated(g, u, wstage, lane, out, aux0, aux1, ldo, row0, nb * TN + h * GH + c * 32,
+                        M, N);
+          }
+          tc_fence_before();
+          __syncwarp();
+          if (lane == 0) mbar_arrive_cluster(dsmem_map(smem_u32(&tail->tempty[h]), 0));
+        }
+        continue;
+      }
+      if (WIDE && !GATED && (!SPLIT || !split)) {
         // Eight warps: warp w drains its lane quadrant's rows, columns
         // [h*BN + p*BN/2, +BN/2) of half h (p = which of the two warps of
         // the quadrant), half 0 first; each half is released to the MMA
@@ -966,18 +989,20 @@ __global__ void __launch_bounds__(Q4 ? Q4_THREADS : WIDE ? WIDE_THREADS : NUM_TH
             round_ok = false;
             break;
           }
-          if constexpr (GATED) {
+          if constexpr (GATED) {  // half h: gate, then up, of GH outputs
+            const int c0 = WIDE ? cpart * (GH / 64) : 0, c1 = WIDE ? c0 + GH / 64 : GH / 32;
 #pragma unroll 1
-            for (int c = 0; c < TN / 32; ++c) {
+            for (int c = c0; c < c1; ++c) {
               float g[32], u[32];
-              tmem_ld_32cols(taddr + c * 32, g);
-              tmem_ld_32cols(taddr + TN + c * 32, u);
+              tmem_ld_32cols(taddr + h * BN + c * 32, g);
+              tmem_ld_32cols(taddr + h * BN + GH + c * 32, u);
 #pragma unroll
               for (int i = 0; i < 32; ++i) {
                 g[i] += part[(c * 32 + i) * BM + rl];
-                u[i] += part[(TN + c * 32 + i) * BM + rl];
+                u[i] += part[(GH + c * 32 + i) * BM + rl];
               }
-              store_gated(g, u, sstage, lane, out, aux0, aux1, ldo, row0, nb * TN + c * 32, M, N);
+              store_gated(g, u, sstage, lane, out, aux0, aux1, ldo, row0,
+                          nb * TN + h * GH + c * 32, M, N);
             }
           } else {
 #pragma unroll 1
@@ -1082,7 +1107,7 @@ int main_gemm_group_m(int kb_main) {
 template <bool B_MN, int BN, bool SPLIT, bool GATED, bool DUAL_B, bool FP8 = false,
           bool Q4 = false, bool WIDE = false>
 cudaError_t launch_variant(const MainGemmArgs &a, int num_sms, cudaStream_t s) {
-  constexpr int TN = GATED ? BN / 2 : WIDE ? 2 * BN : BN;
+  constexpr int TN = GATED ? (BN / 2) * (WIDE ? 2 : 1) : WIDE ? 2 * BN : BN;
   const int m_tiles = (a.M + BM - 1) / BM, n_tiles = (a.N + TN - 1) / TN;
   const int tiles = ((m_tiles + 1) / 2) * n_tiles;  // pair tiles
   if (tiles == 0) return cudaSuccess;
@@ -1193,8 +1218,13 @@ cudaError_t launch_main_gemm(const MainGemmArgs &a, int num_sms, cudaStream_t s)
   // preceding kernel.
   if (a.k_ext <= 0) return cudaErrorInvalidValue;
   const bool split = a.split_k > 1 && a.split_rem > 0;
-  if (a.wide) {  // 256 x 512 pair tiles: plain bf16 and fp8 layers, the gated pair's dX GEMM
-    if (a.q4 || a.gated) return cudaErrorInvalidValue;
+  if (a.wide) {  // 256 x 512 pair tiles: not the 4-bit layer
+    if (a.q4) return cudaErrorInvalidValue;
+    if (a.gated) {
+      if (a.b_mn || a.kb_switch >= 0 || a.fp8) return cudaErrorInvalidValue;
+      return split ? launch_variant<false, 256, true, true, false, false, false, true>(a, num_sms, s)
+                   : launch_variant<false, 256, false, true, false, false, false, true>(a, num_sms, s);
+    }
     if (a.kb_switch >= 0) {
       if (!a.b_mn || a.fp8) return cudaErrorInvalidValue;
       return split ? launch_variant<true, 256, true, false, true, false, false, true>(a, num_sms, s)

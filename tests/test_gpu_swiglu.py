@@ -170,6 +170,39 @@ def test_wide_dx_tail_split(gemm_width):
             assert e <= TOL, f"{n}: {e:.3e} ({errs})"
 
 
+def test_wide_gated_tail_split(gemm_width):
+    """M = 2000, d_in = 1024, d_ff = 3000: the gated GEMM with 256 x 512 tiles
+    (256 outputs of both projections each, the last tile column ragged) has
+    8 x 12 = 96 tiles, so on 76 CTA pairs the last wave's 20 are split in two
+    K ranges, each range's partial holding gate and up of both halves.  Given
+    the full workspace H (and the saved gate and up) are bitwise repeatable and
+    differ from the unsplit ones (minimal workspace); both agree with the
+    oracle on every element."""
+    gemm_width(512)
+    M, d_in, d_ff, r, alpha = 2000, 1024, 3000, 24, 48.0
+    t = make_pair(M, d_in, d_ff, r, seed=72)
+    g = {k: v.to(DEV) for k, v in t.items()}
+    args = [g[k] for k in ("Wg", "Ag", "Bg", "Wu", "Au", "Bu")]
+    rup = lambda n: (n + 255) // 256 * 256
+    full = torch.empty(rl.swiglu_workspace_bytes(M, d_in, d_ff, r), dtype=torch.uint8, device=DEV)
+    minimal = torch.empty(rup(M * 2 * 32 * 2), dtype=torch.uint8, device=DEV)  # [sH_g | sH_u]
+    assert full.numel() > minimal.numel()
+
+    def run(ws):
+        H, saved = rl.swiglu_forward(g["X"], *args, alpha, workspace=ws)
+        torch.cuda.synchronize()
+        rl.device_status()
+        return H, saved
+
+    (h1, s1), (h2, s2), (hu, su) = run(full), run(full), run(minimal)
+    assert torch.equal(h1, h2) and torch.equal(s1, s2)
+    assert not torch.equal(h1, hu)  # the split ran
+    hargs = [t[k] for k in ("X", "Wg", "Ag", "Bg", "Wu", "Au", "Bu")]
+    ref = osw.SampledRows(*hargs, t["dH"], alpha).h_rows_mm(np.arange(M))
+    for H in (h1, hu):
+        assert rel_err(H, ref) <= TOL, f"H: {rel_err(H, ref):.3e}"
+
+
 def test_full_gate_up():
     """Llama-3-8B MLP gate/up shape (M = 8192 tokens, d_in = 4096,
     d_ff = 14336, r = 16): H and dX on one row of every 128-row m-tile, and
