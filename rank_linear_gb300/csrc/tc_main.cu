@@ -279,11 +279,21 @@ __device__ __forceinline__ void store_chunk128(const uint32_t (&pk)[32], uint8_t
   __syncwarp();
 }
 
+// silu(g) * u in fp32, silu(z) = z / (1 + e^-z), the one expression both
+// gated drains use: with the hardware exponential and division (__expf,
+// __fdividef: relative error of order 1e-6, far below the result's one bf16
+// rounding).  With expf and an IEEE division the SiLU's instructions, not
+// the stores, bounded the wide gated tile's drain.  For g < -87 the
+// exponential overflows and the quotient is 0, the limit of silu.
+__device__ __forceinline__ float silu_mul(float g, float u) {
+  return __fdividef(g * u, 1.f + __expf(-g));
+}
+
 // Gated (SwiGLU) epilogue of one 32-column chunk (ch05 "Acceleration
 // principles: Triton kernels and fused LoRA", §5.6: SiLU and the elementwise
 // product fused into the matmul epilogue): from fp32 gate g and up u, writes
 // bf16 silu(g) * u to out, and g and u themselves (kept for the backward) to
-// aux0 and aux1 (skipped when null).  silu(z) = z / (1 + e^-z).
+// aux0 and aux1 (skipped when null).
 __device__ __forceinline__ void store_gated(const float (&g)[32], const float (&u)[32],
                                            uint8_t *stage, int lane, __nv_bfloat16 *out,
                                            __nv_bfloat16 *aux0, __nv_bfloat16 *aux1,
@@ -300,12 +310,45 @@ __device__ __forceinline__ void store_gated(const float (&g)[32], const float (&
     store_chunk(pk, stage, lane, aux1, ldo, row0, col0, M, N);
   }
 #pragma unroll
-  for (int i = 0; i < 16; ++i) {
-    const float h0 = g[2 * i] / (1.f + expf(-g[2 * i])) * u[2 * i];
-    const float h1 = g[2 * i + 1] / (1.f + expf(-g[2 * i + 1])) * u[2 * i + 1];
-    pk[i] = pack_bf16x2(h0, h1);
-  }
+  for (int i = 0; i < 16; ++i) pk[i] = pack_bf16x2(silu_mul(g[2 * i], u[2 * i]),
+                                                   silu_mul(g[2 * i + 1], u[2 * i + 1]));
   store_chunk(pk, stage, lane, out, ldo, row0, col0, M, N);
+}
+
+// The wide gated drain of one warp's 64 outputs: gate columns g_col.., up
+// columns u_col.. of TMEM; gate, up and silu(gate) * up each through
+// 128-byte staging rows (store_chunk128), one output at a time (TMEM is
+// read again for the last, which keeps the live registers to one chunk).
+__device__ __forceinline__ void drain_gated64(uint32_t g_col, uint32_t u_col, uint8_t *stage,
+                                              int lane, __nv_bfloat16 *out, __nv_bfloat16 *aux0,
+                                              __nv_bfloat16 *aux1, int64_t ldo, int row0,
+                                              int col0, int M, int N) {
+  uint32_t pk[32];
+  __nv_bfloat16 *dst[2] = {aux0, aux1};
+  const uint32_t src[2] = {g_col, u_col};
+#pragma unroll 1
+  for (int o = 0; o < 2; ++o) {
+    if (dst[o] == nullptr) continue;
+#pragma unroll
+    for (int part = 0; part < 2; ++part) {
+      float v[32];
+      tmem_ld_32cols(src[o] + part * 32, v);
+#pragma unroll
+      for (int i = 0; i < 16; ++i) pk[part * 16 + i] = pack_bf16x2(v[2 * i], v[2 * i + 1]);
+    }
+    store_chunk128(pk, stage, lane, dst[o], ldo, row0, col0, M, N);
+  }
+#pragma unroll
+  for (int part = 0; part < 2; ++part) {
+    float g[32], u[32];
+    tmem_ld_32cols(g_col + part * 32, g);
+    tmem_ld_32cols(u_col + part * 32, u);
+#pragma unroll
+    for (int i = 0; i < 16; ++i)
+      pk[part * 16 + i] =
+          pack_bf16x2(silu_mul(g[2 * i], u[2 * i]), silu_mul(g[2 * i + 1], u[2 * i + 1]));
+  }
+  store_chunk128(pk, stage, lane, out, ldo, row0, col0, M, N);
 }
 
 template <bool B_MN, int BN, bool SPLIT, bool GATED, bool DUAL_B, bool FP8, bool Q4, bool WIDE>
@@ -814,19 +857,15 @@ __global__ void __launch_bounds__(Q4 ? Q4_THREADS : WIDE ? WIDE_THREADS : NUM_TH
       // wide: this warp's columns of each accumulator half (cpart)
       const int cpart = (warp - 2) >> 2;
       if (WIDE && GATED && (!SPLIT || !split)) {
-        // as below, each half's GH outputs in four 32-column chunks, two
-        // per warp of the quadrant: silu(gate) * up, gate, up
+        // as below; each warp of a quadrant drains 64 of a half's GH
+        // outputs: silu(gate) * up, gate, up
+        static_assert(GH == 128, "two warps of 64 outputs per half");
         uint8_t *wstage = epi_stage + (warp - 2) * EPI_WB;
 #pragma unroll 1
         for (int h = 0; h < 2; ++h) {
-#pragma unroll 1
-          for (int c = cpart * (GH / 64); c < (cpart + 1) * (GH / 64); ++c) {
-            float g[32], u[32];
-            tmem_ld_32cols(taddr + h * BN + c * 32, g);
-            tmem_ld_32cols(taddr + h * BN + GH + c * 32, u);
-            store_gated(g, u, wstage, lane, out, aux0, aux1, ldo, row0, nb * TN + h * GH + c * 32,
-                        M, N);
-          }
+          const int c = cpart * 64;
+          drain_gated64(taddr + h * BN + c, taddr + h * BN + GH + c, wstage, lane, out, aux0, aux1,
+                        ldo, row0, nb * TN + h * GH + c, M, N);
           tc_fence_before();
           __syncwarp();
           if (lane == 0) mbar_arrive_cluster(dsmem_map(smem_u32(&tail->tempty[h]), 0));
