@@ -326,7 +326,7 @@ __device__ __forceinline__ void drain_gated64(uint32_t g_col, uint32_t u_col, ui
   uint32_t pk[32];
   __nv_bfloat16 *dst[2] = {aux0, aux1};
   const uint32_t src[2] = {g_col, u_col};
-#pragma unroll 1
+#pragma unroll  // static indices: dst and src stay in registers
   for (int o = 0; o < 2; ++o) {
     if (dst[o] == nullptr) continue;
 #pragma unroll
