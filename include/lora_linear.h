@@ -248,14 +248,14 @@ lora_status_t lora_debug_withhold_gemm_stage(int n);
 
 /*
  * Test hook of the main GEMMs' tile width (the pages have no counterpart).
- * The plain bf16 layer's two GEMMs run 256 x 512 or 256 x 256 pair tiles
- * (the latter with the split of a short last wave), chosen per shape by a
- * cost model of the waves.  width = 256 or 512 forces that width for every
- * later call in this process (512 only where it is built: not for the
- * 4-bit, fp8 or SwiGLU GEMMs); 0 restores the cost model.  Results differ
- * between widths only by the rounding order of the split tiles.  Workspace
- * sizes do not depend on it.  Returns LORA_ERR_INVALID_ARG for any other
- * width.
+ * The GEMMs of the bf16, fp8 and SwiGLU layers run 256 x 512 or 256 x 256
+ * pair tiles (either with the split of a short last wave where it applies),
+ * chosen per GEMM and shape by a cost model of the waves.  width = 256 or
+ * 512 forces that width for every later call in this process (512 only
+ * where it is built: not for the 4-bit layer's GEMMs); 0 restores the cost
+ * model.  Results differ between widths only by the rounding order of the
+ * split tiles.  Workspace sizes do not depend on it.  Returns
+ * LORA_ERR_INVALID_ARG for any other width.
  */
 lora_status_t lora_debug_gemm_width(int width);
 
