@@ -59,6 +59,10 @@ struct MainGemmArgs {
   // 256 x 512 pair tiles (two N = 256 MMAs per K step sharing A; all but the
   // 4-bit W; gated: 256 outputs of both projections); from main_gemm_plan
   bool wide = false;
+  // The output as a TMA map (bf16 [M][N] with row pitch ldo, box 64 x 32,
+  // 128-byte swizzle): the wide tiles' drain (not the gated one) writes
+  // through it.  Needed when wide && !gated.
+  CUtensorMap tmOut;
   // Test hook of the abort path (not with 4-bit W): the odd CTA of the first
   // pair never loads its first stage.
   int withhold = 0;

@@ -134,6 +134,15 @@ lora_status_t tmap(CUtensorMap *tm, const void *ptr, uint64_t inner, uint64_t ou
   return LORA_OK;
 }
 
+// The output map of a main GEMM whose 256 x 512 tiles drain through TMA
+// stores (wide and not gated): bf16 [M][N] with row pitch ldo, boxes of 64
+// columns x 32 rows in the 128-byte swizzle of the drain's staging rows.
+lora_status_t out_map(MainGemmArgs &a) {
+  if (!a.wide || a.gated) return LORA_OK;
+  return tmap(&a.tmOut, a.out, static_cast<uint64_t>(a.N), static_cast<uint64_t>(a.M),
+              static_cast<uint64_t>(a.ldo) * 2, 64, 32, "output");
+}
+
 // Map without swizzle over a row-major [outer][inner] tensor of `dt`
 // elements (the 4-bit W's packed codes and group scales, staged raw).
 lora_status_t tmap_plain(CUtensorMap *tm, CUtensorMapDataType dt, const void *ptr, uint64_t inner,
@@ -391,6 +400,7 @@ lora_status_t fwd_bf16(const void *X, const void *W, const void *A, const void *
   f2.b_mn = false;
   f2.wide = wide;
   f2.dev_status = di.status;
+  LORA_TRY(out_map(f2));
   return run(LORA_K_MAIN_FWD, st, "forward GEMM", [&] { return launch_main_gemm(f2, di.sms, st); });
 }
 
@@ -512,6 +522,7 @@ lora_status_t bwd_bf16(const void *dY, const void *X, const void *W, const void 
       b2.counters = counters;
     }
     if (q4 == nullptr) b2.withhold = take_one(g_withhold_gemm);  // test hook
+    LORA_TRY(out_map(b2));
     LORA_TRY(run(LORA_K_MAIN_BWD, st, "dX GEMM", [&] { return launch_main_gemm(b2, di.sms, st); }));
   }
 
@@ -816,6 +827,7 @@ lora_status_t sw_fwd_bf16(const void *X, const void *Wg, const void *Ag, const v
     g.partials = reinterpret_cast<float *>(at(ws, P.fsplit_off));
     g.counters = counters;
   }
+  LORA_TRY(out_map(g));
   return run(LORA_K_MAIN_FWD, st, "gated GEMM", [&] { return launch_main_gemm(g, di.sms, st); });
 }
 
@@ -925,6 +937,7 @@ lora_status_t sw_bwd_bf16(const void *dH, const void *X, const void *Wg, const v
       b2.partials = reinterpret_cast<float *>(at(ws, P.bsplit_off));
       b2.counters = counters;
     }
+    LORA_TRY(out_map(b2));
     LORA_TRY(run(LORA_K_MAIN_BWD, st, "gated dX GEMM",
                  [&] { return launch_main_gemm(b2, di.sms, st); }));
   }
@@ -1101,6 +1114,7 @@ lora_status_t fp8_fwd(const void *X, const void *Wq, const float *w_scale, const
     g.partials = reinterpret_cast<float *>(at(ws, P.fsplit_off));
     g.counters = counters;
   }
+  LORA_TRY(out_map(g));
   return run(LORA_K_MAIN_FWD, st, "fp8 forward GEMM", [&] { return launch_main_gemm(g, di.sms, st); });
 }
 
@@ -1200,6 +1214,7 @@ lora_status_t fp8_bwd(const void *dY, const void *X, const void *WqT, const floa
       b2.partials = reinterpret_cast<float *>(at(ws, P.bsplit_off));
       b2.counters = counters;
     }
+    LORA_TRY(out_map(b2));
     LORA_TRY(run(LORA_K_MAIN_BWD, st, "fp8 dX GEMM",
                  [&] { return launch_main_gemm(b2, di.sms, st); }));
   }

@@ -190,6 +190,28 @@ __device__ __forceinline__ void tma_load_2d_pair(uint32_t dst, const CUtensorMap
 __device__ __forceinline__ void fence_proxy_async_smem() {
   asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
 }
+// 2-D tiled store of a box from this CTA's shared memory (in the tensor
+// map's swizzled layout) to global memory, in the issuing thread's bulk
+// group; the copy writes only the part of the box inside the tensor.  x *
+// element size must be a multiple of 16 bytes, and x, y non-negative.
+__device__ __forceinline__ void tma_store_2d(const CUtensorMap *tm, uint32_t src, int32_t x,
+                                             int32_t y) {
+  asm volatile("cp.async.bulk.tensor.2d.global.shared::cta.bulk_group [%0, {%2, %3}], [%1];" ::"l"(
+                   reinterpret_cast<uint64_t>(tm)),
+               "r"(src), "r"(x), "r"(y)
+               : "memory");
+}
+__device__ __forceinline__ void bulk_commit_group() {
+  asm volatile("cp.async.bulk.commit_group;" ::: "memory");
+}
+// The thread's committed bulk stores have read their shared-memory sources.
+__device__ __forceinline__ void bulk_wait_group_read0() {
+  asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory");
+}
+// The thread's committed bulk stores are complete (their writes performed).
+__device__ __forceinline__ void bulk_wait_group0() {
+  asm volatile("cp.async.bulk.wait_group 0;" ::: "memory");
+}
 
 // ---------------------------------------------------------------- tcgen05
 // Allocation (whole warp): writes the TMEM base address to shared memory.

@@ -254,16 +254,23 @@ __device__ __forceinline__ void store_chunk(const uint32_t (&pk)[16], uint8_t *s
   __syncwarp();
 }
 
-// As store_chunk for a 32 x 64 chunk (32 packed words per lane), through
-// 128-byte staging rows: eight lanes store one row's 128 bytes.
-__device__ __forceinline__ void store_chunk128(const uint32_t (&pk)[32], uint8_t *stage, int lane,
-                                              __nv_bfloat16 *out, int64_t ldo, int row0,
-                                              int col0, int M, int N) {
+// Lane r's 64 packed bf16 (32 words) as row r of a 32 x 64 staging chunk of
+// 128-byte rows, 16-byte segment i at slot i ^ (r & 7): the layout of a TMA
+// map's 128-byte swizzle.
+__device__ __forceinline__ void stage_chunk128(const uint32_t (&pk)[32], uint8_t *stage,
+                                              int lane) {
   uint4 *my = reinterpret_cast<uint4 *>(stage + lane * EPI_PITCH_W);
   const int lsw = lane & 7;
 #pragma unroll
   for (int i = 0; i < 8; ++i)
     my[i ^ lsw] = make_uint4(pk[4 * i], pk[4 * i + 1], pk[4 * i + 2], pk[4 * i + 3]);
+}
+// As store_chunk for a 32 x 64 chunk (32 packed words per lane), through
+// 128-byte staging rows: eight lanes store one row's 128 bytes.
+__device__ __forceinline__ void store_chunk128(const uint32_t (&pk)[32], uint8_t *stage, int lane,
+                                              __nv_bfloat16 *out, int64_t ldo, int row0,
+                                              int col0, int M, int N) {
+  stage_chunk128(pk, stage, lane);
   __syncwarp();
   const int seg = lane & 7;  // 16-byte segment (8 columns) of a row
   const int col = col0 + seg * 8;
@@ -356,6 +363,7 @@ __global__ void __launch_bounds__(Q4 ? Q4_THREADS : WIDE ? WIDE_THREADS : NUM_TH
     k_main_gemm(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                 const __grid_constant__ CUtensorMap tmA2, const __grid_constant__ CUtensorMap tmB2,
                 const __grid_constant__ CUtensorMap tmB3, const __grid_constant__ CUtensorMap tmB4,
+                const __grid_constant__ CUtensorMap tmOut,
                 int M, int N, int kb_main, int k_ext, int kb_switch, int ext_shift, int group_m,
                 __nv_bfloat16 *__restrict__ out, __nv_bfloat16 *__restrict__ aux0,
                 __nv_bfloat16 *__restrict__ aux1, int64_t ldo, int split_k, int split_rem,
@@ -877,6 +885,10 @@ __global__ void __launch_bounds__(Q4 ? Q4_THREADS : WIDE ? WIDE_THREADS : NUM_TH
         // [h*BN + p*BN/2, +BN/2) of half h (p = which of the two warps of
         // the quadrant), half 0 first; each half is released to the MMA
         // issuer as soon as all sixteen warps of the pair have drained it.
+        // Each 32 x 64 chunk goes out as one TMA store of the warp's staging
+        // buffer (its layout is the map's 128-byte swizzle; the copy writes
+        // only rows < M and columns < N); before the buffer is refilled the
+        // previous store has read it.
         uint8_t *wstage = epi_stage + (warp - 2) * EPI_WB;
 #pragma unroll 1
         for (int h = 0; h < 2; ++h) {
@@ -899,7 +911,15 @@ __global__ void __launch_bounds__(Q4 ? Q4_THREADS : WIDE ? WIDE_THREADS : NUM_TH
               pk[i] = pack_bf16x2(v[2 * i], v[2 * i + 1]);
               pk[16 + i] = pack_bf16x2(u[2 * i], u[2 * i + 1]);
             }
-            store_chunk128(pk, wstage, lane, out, ldo, row0, nb * TN + col, M, N);
+            if (lane == 0) bulk_wait_group_read0();
+            __syncwarp();
+            stage_chunk128(pk, wstage, lane);
+            fence_proxy_async_smem();  // this lane's stores, visible to the TMA
+            __syncwarp();
+            if (lane == 0 && nb * TN + col < N && row0 < M) {  // a box with any element in
+              tma_store_2d(&tmOut, smem_u32(wstage), nb * TN + col, row0);
+              bulk_commit_group();
+            }
           }
           tc_fence_before();
           __syncwarp();
@@ -960,6 +980,10 @@ __global__ void __launch_bounds__(Q4 ? Q4_THREADS : WIDE ? WIDE_THREADS : NUM_TH
       // The accumulator is released only at the end (no item follows).
       // Wide: the partial holds both accumulator halves (2 BN columns), and
       // each of the eight warps takes its columns of each half.
+      if (WIDE && !GATED) {  // the staging buffer's last TMA store has read it
+        if (lane == 0) bulk_wait_group_read0();
+        __syncwarp();
+      }
       constexpr int AC = WIDE ? 2 * BN : BN;  // accumulator columns
       constexpr int HALVES = WIDE ? 2 : 1;
       constexpr int WCOLS = WIDE ? BN / 2 : BN;  // this warp's columns of a half
@@ -1072,6 +1096,8 @@ __global__ void __launch_bounds__(Q4 ? Q4_THREADS : WIDE ? WIDE_THREADS : NUM_TH
       if (!sync_ok) break;
       }  // SPLIT
     }
+    // this warp's TMA stores of the output are complete before the CTA leaves
+    if (WIDE && !GATED && lane == 0) bulk_wait_group0();
   }
 
   // Both CTAs are done with TMEM and with each other's barriers before the
@@ -1175,7 +1201,8 @@ cudaError_t launch_variant(const MainGemmArgs &a, int num_sms, cudaStream_t s) {
   const int kb_switch = a.kb_switch >= 0 ? a.kb_switch : (1 << 30);
   const CUtensorMap &tmB3 = (GATED || Q4 || a.kb_switch >= 0) ? a.tmB3 : a.tmB;
   const CUtensorMap &tmB4 = GATED ? a.tmB4 : a.tmB2;
-  return cudaLaunchKernelEx(&cfg, kern, a.tmA, a.tmB, a.tmA2, a.tmB2, tmB3, tmB4, a.M, a.N,
+  const CUtensorMap &tmOut = (WIDE && !GATED) ? a.tmOut : a.tmA;  // unused otherwise
+  return cudaLaunchKernelEx(&cfg, kern, a.tmA, a.tmB, a.tmA2, a.tmB2, tmB3, tmB4, tmOut, a.M, a.N,
                             a.kb_main, a.k_ext, kb_switch, a.ext_shift, main_gemm_group_m(a.kb_main),
                             static_cast<__nv_bfloat16 *>(a.out),
                             static_cast<__nv_bfloat16 *>(a.aux0),
