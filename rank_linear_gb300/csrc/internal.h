@@ -60,9 +60,10 @@ struct MainGemmArgs {
   // 4-bit W; gated: 256 outputs of both projections); from main_gemm_plan
   bool wide = false;
   // The output as a TMA map (bf16 [M][N] with row pitch ldo, box 64 x 32,
-  // 128-byte swizzle): the wide tiles' drain (not the gated one) writes
-  // through it.  Needed when wide && !gated.
-  CUtensorMap tmOut;
+  // 128-byte swizzle): the wide tiles' drain writes through it, and the
+  // gated pair's through tmAux0 / tmAux1 (the same over aux0 / aux1) too.
+  // Needed when wide (tmAux0 / tmAux1: when gated and aux0 / aux1 given).
+  CUtensorMap tmOut, tmAux0, tmAux1;
   // Test hook of the abort path (not with 4-bit W): the odd CTA of the first
   // pair never loads its first stage.
   int withhold = 0;

@@ -134,13 +134,20 @@ lora_status_t tmap(CUtensorMap *tm, const void *ptr, uint64_t inner, uint64_t ou
   return LORA_OK;
 }
 
-// The output map of a main GEMM whose 256 x 512 tiles drain through TMA
-// stores (wide and not gated): bf16 [M][N] with row pitch ldo, boxes of 64
-// columns x 32 rows in the 128-byte swizzle of the drain's staging rows.
+// The output maps of a main GEMM whose 256 x 512 tiles drain through TMA
+// stores: bf16 [M][N] with row pitch ldo, boxes of 64 columns x 32 rows in
+// the 128-byte swizzle of the drain's staging rows; for the gated pair also
+// over gate (aux0) and up (aux1) when they are kept.
 lora_status_t out_map(MainGemmArgs &a) {
-  if (!a.wide || a.gated) return LORA_OK;
-  return tmap(&a.tmOut, a.out, static_cast<uint64_t>(a.N), static_cast<uint64_t>(a.M),
-              static_cast<uint64_t>(a.ldo) * 2, 64, 32, "output");
+  if (!a.wide) return LORA_OK;
+  const uint64_t n = static_cast<uint64_t>(a.N), m = static_cast<uint64_t>(a.M);
+  const uint64_t pitch = static_cast<uint64_t>(a.ldo) * 2;
+  lora_status_t e = tmap(&a.tmOut, a.out, n, m, pitch, 64, 32, "output");
+  if (e == LORA_OK && a.gated && a.aux0 != nullptr)
+    e = tmap(&a.tmAux0, a.aux0, n, m, pitch, 64, 32, "gate");
+  if (e == LORA_OK && a.gated && a.aux1 != nullptr)
+    e = tmap(&a.tmAux1, a.aux1, n, m, pitch, 64, 32, "up");
+  return e;
 }
 
 // Map without swizzle over a row-major [outer][inner] tensor of `dt`

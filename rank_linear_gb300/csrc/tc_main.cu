@@ -322,16 +322,34 @@ __device__ __forceinline__ void store_gated(const float (&g)[32], const float (&
   store_chunk(pk, stage, lane, out, ldo, row0, col0, M, N);
 }
 
+// One 32 x 64 staged chunk out through a TMA store (lane 0 issues it into
+// its bulk group): first the buffer's previous store must have read it; a
+// box wholly outside [M, N) is not issued.
+__device__ __forceinline__ void tma_chunk128(const uint32_t (&pk)[32], uint8_t *stage, int lane,
+                                             const CUtensorMap *tm, int col0, int row0, int M,
+                                             int N) {
+  if (lane == 0) bulk_wait_group_read0();
+  __syncwarp();
+  stage_chunk128(pk, stage, lane);
+  fence_proxy_async_smem();  // this lane's stores, visible to the TMA
+  __syncwarp();
+  if (lane == 0 && col0 < N && row0 < M) {
+    tma_store_2d(tm, smem_u32(stage), col0, row0);
+    bulk_commit_group();
+  }
+}
+
 // The wide gated drain of one warp's 64 outputs: gate columns g_col.., up
-// columns u_col.. of TMEM; gate, up and silu(gate) * up each through
-// 128-byte staging rows (store_chunk128), one output at a time (TMEM is
-// read again for the last, which keeps the live registers to one chunk).
+// columns u_col.. of TMEM; gate, up (when their maps are given) and
+// silu(gate) * up, each through the staging buffer and a TMA store, one
+// output at a time (TMEM is read again for the last, which keeps the live
+// registers to one chunk).
 __device__ __forceinline__ void drain_gated64(uint32_t g_col, uint32_t u_col, uint8_t *stage,
-                                              int lane, __nv_bfloat16 *out, __nv_bfloat16 *aux0,
-                                              __nv_bfloat16 *aux1, int64_t ldo, int row0,
-                                              int col0, int M, int N) {
+                                              int lane, const CUtensorMap *tm_gate,
+                                              const CUtensorMap *tm_up, const CUtensorMap *tm_out,
+                                              int col0, int row0, int M, int N) {
   uint32_t pk[32];
-  __nv_bfloat16 *dst[2] = {aux0, aux1};
+  const CUtensorMap *dst[2] = {tm_gate, tm_up};
   const uint32_t src[2] = {g_col, u_col};
 #pragma unroll  // static indices: dst and src stay in registers
   for (int o = 0; o < 2; ++o) {
@@ -343,7 +361,7 @@ __device__ __forceinline__ void drain_gated64(uint32_t g_col, uint32_t u_col, ui
 #pragma unroll
       for (int i = 0; i < 16; ++i) pk[part * 16 + i] = pack_bf16x2(v[2 * i], v[2 * i + 1]);
     }
-    store_chunk128(pk, stage, lane, dst[o], ldo, row0, col0, M, N);
+    tma_chunk128(pk, stage, lane, dst[o], col0, row0, M, N);
   }
 #pragma unroll
   for (int part = 0; part < 2; ++part) {
@@ -355,7 +373,7 @@ __device__ __forceinline__ void drain_gated64(uint32_t g_col, uint32_t u_col, ui
       pk[part * 16 + i] =
           pack_bf16x2(silu_mul(g[2 * i], u[2 * i]), silu_mul(g[2 * i + 1], u[2 * i + 1]));
   }
-  store_chunk128(pk, stage, lane, out, ldo, row0, col0, M, N);
+  tma_chunk128(pk, stage, lane, tm_out, col0, row0, M, N);
 }
 
 template <bool B_MN, int BN, bool SPLIT, bool GATED, bool DUAL_B, bool FP8, bool Q4, bool WIDE>
@@ -364,6 +382,7 @@ __global__ void __launch_bounds__(Q4 ? Q4_THREADS : WIDE ? WIDE_THREADS : NUM_TH
                 const __grid_constant__ CUtensorMap tmA2, const __grid_constant__ CUtensorMap tmB2,
                 const __grid_constant__ CUtensorMap tmB3, const __grid_constant__ CUtensorMap tmB4,
                 const __grid_constant__ CUtensorMap tmOut,
+                const __grid_constant__ CUtensorMap tmAux0, const __grid_constant__ CUtensorMap tmAux1,
                 int M, int N, int kb_main, int k_ext, int kb_switch, int ext_shift, int group_m,
                 __nv_bfloat16 *__restrict__ out, __nv_bfloat16 *__restrict__ aux0,
                 __nv_bfloat16 *__restrict__ aux1, int64_t ldo, int split_k, int split_rem,
@@ -872,8 +891,9 @@ __global__ void __launch_bounds__(Q4 ? Q4_THREADS : WIDE ? WIDE_THREADS : NUM_TH
 #pragma unroll 1
         for (int h = 0; h < 2; ++h) {
           const int c = cpart * 64;
-          drain_gated64(taddr + h * BN + c, taddr + h * BN + GH + c, wstage, lane, out, aux0, aux1,
-                        ldo, row0, nb * TN + h * GH + c, M, N);
+          drain_gated64(taddr + h * BN + c, taddr + h * BN + GH + c, wstage, lane,
+                        aux0 != nullptr ? &tmAux0 : nullptr, aux1 != nullptr ? &tmAux1 : nullptr,
+                        &tmOut, nb * TN + h * GH + c, row0, M, N);
           tc_fence_before();
           __syncwarp();
           if (lane == 0) mbar_arrive_cluster(dsmem_map(smem_u32(&tail->tempty[h]), 0));
@@ -911,15 +931,7 @@ __global__ void __launch_bounds__(Q4 ? Q4_THREADS : WIDE ? WIDE_THREADS : NUM_TH
               pk[i] = pack_bf16x2(v[2 * i], v[2 * i + 1]);
               pk[16 + i] = pack_bf16x2(u[2 * i], u[2 * i + 1]);
             }
-            if (lane == 0) bulk_wait_group_read0();
-            __syncwarp();
-            stage_chunk128(pk, wstage, lane);
-            fence_proxy_async_smem();  // this lane's stores, visible to the TMA
-            __syncwarp();
-            if (lane == 0 && nb * TN + col < N && row0 < M) {  // a box with any element in
-              tma_store_2d(&tmOut, smem_u32(wstage), nb * TN + col, row0);
-              bulk_commit_group();
-            }
+            tma_chunk128(pk, wstage, lane, &tmOut, nb * TN + col, row0, M, N);
           }
           tc_fence_before();
           __syncwarp();
@@ -980,7 +992,7 @@ __global__ void __launch_bounds__(Q4 ? Q4_THREADS : WIDE ? WIDE_THREADS : NUM_TH
       // The accumulator is released only at the end (no item follows).
       // Wide: the partial holds both accumulator halves (2 BN columns), and
       // each of the eight warps takes its columns of each half.
-      if (WIDE && !GATED) {  // the staging buffer's last TMA store has read it
+      if (WIDE) {  // the staging buffer's last TMA store has read it
         if (lane == 0) bulk_wait_group_read0();
         __syncwarp();
       }
@@ -1096,8 +1108,8 @@ __global__ void __launch_bounds__(Q4 ? Q4_THREADS : WIDE ? WIDE_THREADS : NUM_TH
       if (!sync_ok) break;
       }  // SPLIT
     }
-    // this warp's TMA stores of the output are complete before the CTA leaves
-    if (WIDE && !GATED && lane == 0) bulk_wait_group0();
+    // this warp's TMA stores of the outputs are complete before the CTA leaves
+    if (WIDE && lane == 0) bulk_wait_group0();
   }
 
   // Both CTAs are done with TMEM and with each other's barriers before the
@@ -1201,8 +1213,12 @@ cudaError_t launch_variant(const MainGemmArgs &a, int num_sms, cudaStream_t s) {
   const int kb_switch = a.kb_switch >= 0 ? a.kb_switch : (1 << 30);
   const CUtensorMap &tmB3 = (GATED || Q4 || a.kb_switch >= 0) ? a.tmB3 : a.tmB;
   const CUtensorMap &tmB4 = GATED ? a.tmB4 : a.tmB2;
-  const CUtensorMap &tmOut = (WIDE && !GATED) ? a.tmOut : a.tmA;  // unused otherwise
-  return cudaLaunchKernelEx(&cfg, kern, a.tmA, a.tmB, a.tmA2, a.tmB2, tmB3, tmB4, tmOut, a.M, a.N,
+  // (the output maps are read only by the wide drains)
+  const CUtensorMap &tmOut = WIDE ? a.tmOut : a.tmA;
+  const CUtensorMap &tmAux0 = (WIDE && GATED && a.aux0 != nullptr) ? a.tmAux0 : a.tmA;
+  const CUtensorMap &tmAux1 = (WIDE && GATED && a.aux1 != nullptr) ? a.tmAux1 : a.tmA;
+  return cudaLaunchKernelEx(&cfg, kern, a.tmA, a.tmB, a.tmA2, a.tmB2, tmB3, tmB4, tmOut, tmAux0,
+                            tmAux1, a.M, a.N,
                             a.kb_main, a.k_ext, kb_switch, a.ext_shift, main_gemm_group_m(a.kb_main),
                             static_cast<__nv_bfloat16 *>(a.out),
                             static_cast<__nv_bfloat16 *>(a.aux0),
