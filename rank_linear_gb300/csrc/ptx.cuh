@@ -76,6 +76,20 @@ __device__ __forceinline__ bool mbar_test(uint32_t bar, uint32_t parity) {
   return done != 0;
 }
 
+// Non-blocking probe of the phase with the given parity: the thread is never
+// suspended (try_wait may be), so a caller with other work can come back.
+__device__ __forceinline__ bool mbar_peek(uint32_t bar, uint32_t parity) {
+  uint32_t done;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "mbarrier.test_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+      "selp.b32 %0, 1, 0, p;\n\t}"
+      : "=r"(done)
+      : "r"(bar), "r"(parity)
+      : "memory");
+  return done != 0;
+}
+
 // Bounded wait shared by the roles of one CTA.  Returns false (without
 // completing) when another role of the CTA already gave up, or when the
 // time limit passes -- then it raises the CTA's abort flag and ORs

@@ -667,6 +667,24 @@ __global__ void __launch_bounds__(Q4 ? Q4_THREADS : WIDE ? WIDE_THREADS : NUM_TH
       constexpr uint64_t A_STEP = 32 >> 4, B_STEP = B_MN ? (2048 >> 4) : (32 >> 4);
       const uint64_t a_desc0 = sdesc_sw128(sA, 16, 1024);
       const uint64_t b_desc0 = B_MN ? sdesc_sw128(sB, 8192, 1024) : sdesc_sw128(sB, 16, 1024);
+      // One K block's MMAs into accumulator columns dcol, from the stage
+      // whose descriptors are ad / bd (fp8: four K = 32 steps of 32 bytes
+      // each, like bf16's K = 16; the bf16 extension may be shorter).
+      auto issue = [&](uint32_t dcol, uint64_t ad, uint64_t bd, int kb, uint32_t accum) {
+        if (kb < kb_main) {
+#pragma unroll
+          for (int kk = 0; kk < BK / 16; ++kk) {
+            if constexpr (FP8)
+              tc_mma_f8_pair(dcol, ad + kk * A_STEP, bd + kk * B_STEP, idesc8, kk ? 1u : accum);
+            else
+              tc_mma_bf16_pair(dcol, ad + kk * A_STEP, bd + kk * B_STEP, idesc, kk ? 1u : accum);
+          }
+        } else {
+          const int nk = min(BK / 16, (k_ext - (kb - kb_main) * BK) / 16);
+          for (int kk = 0; kk < nk; ++kk)
+            tc_mma_bf16_pair(dcol, ad + kk * A_STEP, bd + kk * B_STEP, idesc, kk ? 1u : accum);
+        }
+      };
       int stage = 0;
       uint32_t phase = 0;
       bool ok = true;
@@ -693,7 +711,11 @@ __global__ void __launch_bounds__(Q4 ? Q4_THREADS : WIDE ? WIDE_THREADS : NUM_TH
         // shows up as idle tensor cycles.
         uint64_t ad = a_desc0 + stage * (A_BYTES >> 4);
         uint64_t bd = b_desc0 + stage * (B_BYTES >> 4);
-        uint32_t accum = 0;
+        uint32_t accum = 0, accum1 = 0;  // per accumulator half: 0 until its first MMA
+        // Wide: while the previous tile's half 1 is still being drained, the
+        // half-0 MMAs of up to STAGES - 1 K blocks go ahead; their stages
+        // stay held until the half-1 MMAs catch up.
+        int deferred = 0;
         for (int kb = kb_lo; kb < kb_hi; ++kb) {
           // 4-bit W: the phase also publishes the dequantising warps' stores,
           // some made by the other CTA of the pair
@@ -702,49 +724,39 @@ __global__ void __launch_bounds__(Q4 ? Q4_THREADS : WIDE ? WIDE_THREADS : NUM_TH
             break;
           }
           tc_fence_after();
-          const int nk = kb < kb_main ? BK / 16 : min(BK / 16, (k_ext - (kb - kb_main) * BK) / 16);
-          if (kb < kb_main) {
-            // fp8: four K = 32 steps of 32 bytes each, like bf16's K = 16
-#pragma unroll
-            for (int kk = 0; kk < BK / 16; ++kk) {
-              if constexpr (FP8)
-                tc_mma_f8_pair(d, ad + kk * A_STEP, bd + kk * B_STEP, idesc8, kk ? 1u : accum);
-              else
-                tc_mma_bf16_pair(d, ad + kk * A_STEP, bd + kk * B_STEP, idesc, kk ? 1u : accum);
-            }
-          } else {
-            for (int kk = 0; kk < nk; ++kk)
-              tc_mma_bf16_pair(d, ad + kk * A_STEP, bd + kk * B_STEP, idesc, kk ? 1u : accum);
-          }
+          issue(d, ad, bd, kb, accum);
+          accum = 1u;
+          bool hold = false;
           if constexpr (WIDE) {  // the same A tile against the second half of B
             if (!half1_free) {
-              if (!mbar_wait(smem_u32(&tail->tempty[1]), (use & 1u) ^ 1u, abort_flag,
-                             dev_status)) {
-                ok = false;
-                break;
+              if (deferred + 1 < STAGES && kb + 1 < kb_hi &&
+                  !mbar_peek(smem_u32(&tail->tempty[1]), (use & 1u) ^ 1u)) {
+                ++deferred;
+                hold = true;
+              } else {
+                if (!mbar_wait(smem_u32(&tail->tempty[1]), (use & 1u) ^ 1u, abort_flag,
+                               dev_status)) {
+                  ok = false;
+                  break;
+                }
+                tc_fence_after();
+                half1_free = true;
+                for (int j = deferred; j > 0; --j) {  // oldest first: K order within half 1
+                  const int sj = stage >= j ? stage - j : stage - j + STAGES;
+                  issue(d + BN, a_desc0 + sj * (A_BYTES >> 4),
+                        b_desc0 + sj * (B_BYTES >> 4) + (B_HALF >> 4), kb - j, accum1);
+                  accum1 = 1u;
+                  tc_commit_pair_mc(smem_u32(&tail->empty[sj]), PAIR_MASK);
+                }
+                deferred = 0;
               }
-              tc_fence_after();
-              half1_free = true;
             }
-            const uint64_t bd1 = bd + (B_HALF >> 4);
-            if (kb < kb_main) {
-#pragma unroll
-              for (int kk = 0; kk < BK / 16; ++kk) {
-                if constexpr (FP8)
-                  tc_mma_f8_pair(d + BN, ad + kk * A_STEP, bd1 + kk * B_STEP, idesc8,
-                                 kk ? 1u : accum);
-                else
-                  tc_mma_bf16_pair(d + BN, ad + kk * A_STEP, bd1 + kk * B_STEP, idesc,
-                                   kk ? 1u : accum);
-              }
-            } else {
-              for (int kk = 0; kk < nk; ++kk)
-                tc_mma_bf16_pair(d + BN, ad + kk * A_STEP, bd1 + kk * B_STEP, idesc,
-                                 kk ? 1u : accum);
+            if (!hold) {
+              issue(d + BN, ad, bd + (B_HALF >> 4), kb, accum1);
+              accum1 = 1u;
             }
           }
-          accum = 1u;
-          tc_commit_pair_mc(smem_u32(&tail->empty[stage]), PAIR_MASK);  // free in both CTAs
+          if (!hold) tc_commit_pair_mc(smem_u32(&tail->empty[stage]), PAIR_MASK);  // free in both CTAs
           ad += A_BYTES >> 4;
           bd += B_BYTES >> 4;
           if (++stage == STAGES) {
