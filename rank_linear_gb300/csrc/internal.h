@@ -138,6 +138,10 @@ struct SkinnyArgs {
   // pairs start on the other SMs at once instead of waiting for this pass to
   // leave them.
   int feeds_gemm = 0;
+  // With feeds_gemm: the GEMM gives every CTA pair two tiles or more, so the
+  // pairs that start when this pass leaves end last; its CTAs (one per SM,
+  // beside the GEMM's) then take a ring of twice the depth and leave sooner.
+  int deep_ring = 0;
 };
 constexpr int kSkinnyFeedMaxCtas = 64;
 // One CTA streams its 128 rows at about 40 GB/s, so a 128-block (K = 8192)

@@ -326,14 +326,22 @@ lora_status_t check_ws(const void *ws, size_t have, size_t need) {
 uint8_t *at(void *base, size_t off) { return static_cast<uint8_t *>(base) + off; }
 
 // ---------------------------------------------------------------- bf16 path
+// At least two 256 x 512 pair tiles of an M x N output for every CTA pair.
+bool many_wide_tiles(int64_t M, int64_t N, int pairs) {
+  const int64_t tiles = ((M + 255) / 256) * ((N + 511) / 512);
+  return tiles >= 2 * static_cast<int64_t>(pairs);
+}
+
 // sH = s X A^T into saved (row-major [M][r_pad]) and its transpose.
-// feeds_gemm: the forward GEMM follows and may start beside this pass.
+// feeds_gemm: the forward GEMM follows and may start beside this pass;
+// deep_ring: that GEMM gives every pair two tiles or more.
 lora_status_t down_fwd_bf16(const DevInfo &di, const Plan &P, const void *X, const void *A,
                             float s, int r, int64_t M, int64_t d_in, void *saved,
                             cudaStream_t st, unsigned *zero_ptr = nullptr, int zero_words = 0,
-                            bool feeds_gemm = false) {
+                            bool feeds_gemm = false, bool deep_ring = false) {
   SkinnyArgs f1;
   f1.feeds_gemm = feeds_gemm ? 1 : 0;
+  f1.deep_ring = deep_ring ? 1 : 0;
   f1.zero_ptr = zero_ptr;
   f1.zero_words = zero_words;
   LORA_TRY(tmap(&f1.tmA, X, d_in, M, d_in * 2, 64, 128, "X"));
@@ -377,7 +385,8 @@ lora_status_t fwd_bf16(const void *X, const void *W, const void *A, const void *
   // with 256 x 512 tiles (about 33 us each at K = 4096) the pass can run
   // beside the GEMM's start: the pairs that start late have a tile's slack
   LORA_TRY(down_fwd_bf16(di, P, X, A, s, r, M, d_in, saved, st, counters,
-                         split ? 2 * P.fsplit.rem : 0, wide));
+                         split ? 2 * P.fsplit.rem : 0, wide,
+                         wide && many_wide_tiles(M, d_out, main_gemm_pairs(false, di.sms))));
   MainGemmArgs f2;
   if (split) {
     f2.split_k = P.fsplit.k;
@@ -490,6 +499,7 @@ lora_status_t bwd_bf16(const void *dY, const void *X, const void *W, const void 
   b4.dev_status = di.status;
   if (wide) {
     b1.feeds_gemm = 1;
+    b1.deep_ring = many_wide_tiles(M, d_in, main_gemm_pairs(true, di.sms)) ? 1 : 0;
     LORA_TRY(run(LORA_K_DOWN_BWD, st, "s dY B pass",
                  [&] { return launch_skinny(&b1, 1, di.sms, st); }));
   } else {

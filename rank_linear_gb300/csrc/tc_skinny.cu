@@ -30,10 +30,13 @@ namespace lora {
 namespace {
 
 constexpr int BM = 128, BK = 64;
-constexpr int MAX_STAGES = 8;
+constexpr int MAX_STAGES = 12;
 constexpr int NUM_THREADS = 192;
 constexpr uint32_t A_BYTES = BM * BK * 2;   // 16 KB
 constexpr size_t kSmemBudget = 100 * 1024;  // two CTAs per SM when RP <= 128
+// The feeding layout's CTAs cannot share an SM with the GEMM beside them: with
+// deep_ring each takes a ring of twice the depth, twice the bytes in flight.
+constexpr size_t kSmemBudgetAlone = 200 * 1024;
 
 struct __align__(8) SkinnyTail {
   uint64_t full[MAX_STAGES];
@@ -70,6 +73,7 @@ struct Params {
   unsigned *dev_status = nullptr;
   int withhold = 0;  // test hook: CTA 0 never fills its first stage
   int after_gemm = 0;  // no wait at the start; the last cluster waits at the end
+  int alone = 0;       // feeding layout with deep_ring: the deep ring
 };
 
 struct SkinnyLayout {
@@ -80,7 +84,7 @@ struct SkinnyLayout {
   uint32_t tmem_cols;
 };
 
-__host__ __device__ inline SkinnyLayout skinny_layout(int RP, int RK) {
+__host__ __device__ inline SkinnyLayout skinny_layout(int RP, int RK, bool alone) {
   SkinnyLayout L;
   L.b_bytes = static_cast<uint32_t>(RP) * BK * 2;
   const uint32_t stage_bytes = A_BYTES + L.b_bytes;
@@ -89,7 +93,8 @@ __host__ __device__ inline SkinnyLayout skinny_layout(int RP, int RK) {
   // their partials into it while this CTA's pipeline is still running;
   // wide ones overlay the pipeline buffers and are pulled after a barrier.
   L.push = RK <= 64;
-  const size_t budget = L.push ? kSmemBudget + 10 * 1024 - L.red_bytes : kSmemBudget;
+  const size_t cap = alone ? kSmemBudgetAlone : kSmemBudget;
+  const size_t budget = L.push ? cap + 10 * 1024 - L.red_bytes : cap;
   int st = static_cast<int>(budget / stage_bytes);
   st = st < 2 ? 2 : (st > MAX_STAGES ? MAX_STAGES : st);
   L.stages = st;
@@ -123,7 +128,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
   unsigned *dev_status = P.dev_status;
 
   extern __shared__ uint8_t smem_raw[];
-  const SkinnyLayout L = skinny_layout(RP, RK);
+  const SkinnyLayout L = skinny_layout(RP, RK, P.alone != 0);
   const uint32_t raw = smem_u32(smem_raw);
   const uint32_t base = (raw + 1023u) & ~1023u;
   uint8_t *base_ptr = smem_raw + (base - raw);
@@ -462,17 +467,21 @@ cudaError_t launch_skinny(const SkinnyArgs *probs, int nprob, int num_sms, cudaS
     const int kb = (use[i]->K + BK - 1) / BK;
     max_kb = kb > max_kb ? kb : max_kb;
   }
-  bool feeds = true;
-  for (int i = 0; i < P.nprob; ++i) feeds = feeds && use[i]->feeds_gemm != 0;
-  const int S = (feeds && total_mt <= kSkinnyFeedMaxCtas && max_kb <= kSkinnyFeedMaxKb)
-                    ? 1
-                    : skinny_split_launch(total_mt, max_kb, num_sms);
+  bool feeds = true, deep = true;
+  for (int i = 0; i < P.nprob; ++i) {
+    feeds = feeds && use[i]->feeds_gemm != 0;
+    deep = deep && use[i]->deep_ring != 0;
+  }
+  const bool feed_layout =
+      feeds && total_mt <= kSkinnyFeedMaxCtas && max_kb <= kSkinnyFeedMaxKb;
+  const int S = feed_layout ? 1 : skinny_split_launch(total_mt, max_kb, num_sms);
   P.S = S;
+  P.alone = feed_layout && deep ? 1 : 0;
   size_t smem = 0;
   unsigned grid = 0;
   for (int i = 0; i < P.nprob; ++i) {
     P.p[i] = to_prob(*use[i], S);
-    const SkinnyLayout L = skinny_layout(P.p[i].RP, P.p[i].RK);
+    const SkinnyLayout L = skinny_layout(P.p[i].RP, P.p[i].RK, P.alone != 0);
     smem = L.smem_bytes > smem ? L.smem_bytes : smem;
     grid += static_cast<unsigned>(P.p[i].ctas);
   }
