@@ -915,17 +915,21 @@ __global__ void __launch_bounds__(Q4 ? Q4_THREADS : WIDE ? WIDE_THREADS : NUM_TH
       if (WIDE && !GATED && (!SPLIT || !split)) {
         // Eight warps: warp w drains its lane quadrant's rows, columns
         // [h*BN + p*BN/2, +BN/2) of half h (p = which of the two warps of
-        // the quadrant), half 0 first; each half is released to the MMA
-        // issuer as soon as all sixteen warps of the pair have drained it.
+        // the quadrant), half 0 first.  The warp reads its part of a half
+        // out of TMEM (packed to bf16 in registers) before it stores any of
+        // it, and releases the half to the MMA issuer as soon as it has read
+        // it: the next tile's MMAs on that half then run under the stores.
         // Each 32 x 64 chunk goes out as one TMA store of the warp's staging
         // buffer (its layout is the map's 128-byte swizzle; the copy writes
         // only rows < M and columns < N); before the buffer is refilled the
         // previous store has read it.
         uint8_t *wstage = epi_stage + (warp - 2) * EPI_WB;
+        constexpr int CH = BN / 128;  // 64-column chunks of a half per warp
 #pragma unroll 1
         for (int h = 0; h < 2; ++h) {
-#pragma unroll 1
-          for (int c = 0; c < BN / 128; ++c) {  // 64 columns at a time
+          uint32_t pk[CH][32];
+#pragma unroll
+          for (int c = 0; c < CH; ++c) {
             const int col = h * BN + cpart * (BN / 2) + c * 64;
             float v[32], u[32];
             tmem_ld_32cols(taddr + col, v);
@@ -937,17 +941,19 @@ __global__ void __launch_bounds__(Q4 ? Q4_THREADS : WIDE ? WIDE_THREADS : NUM_TH
                 u[i] *= sc;
               }
             }
-            uint32_t pk[32];
 #pragma unroll
             for (int i = 0; i < 16; ++i) {
-              pk[i] = pack_bf16x2(v[2 * i], v[2 * i + 1]);
-              pk[16 + i] = pack_bf16x2(u[2 * i], u[2 * i + 1]);
+              pk[c][i] = pack_bf16x2(v[2 * i], v[2 * i + 1]);
+              pk[c][16 + i] = pack_bf16x2(u[2 * i], u[2 * i + 1]);
             }
-            tma_chunk128(pk, wstage, lane, &tmOut, nb * TN + col, row0, M, N);
           }
           tc_fence_before();
           __syncwarp();
           if (lane == 0) mbar_arrive_cluster(dsmem_map(smem_u32(&tail->tempty[h]), 0));
+#pragma unroll
+          for (int c = 0; c < CH; ++c)
+            tma_chunk128(pk[c], wstage, lane, &tmOut,
+                         nb * TN + h * BN + cpart * (BN / 2) + c * 64, row0, M, N);
         }
         continue;
       }
