@@ -142,6 +142,10 @@ struct SkinnyArgs {
   // pairs that start when this pass leaves end last; its CTAs (one per SM,
   // beside the GEMM's) then take a ring of twice the depth and leave sooner.
   int deep_ring = 0;
+  // Largest K split (cluster size) the launch may take; 0: no limit.  Must
+  // depend on the shape only, so that results do not depend on whether a
+  // GEMM runs beside the pass.
+  int max_split = 0;
 };
 constexpr int kSkinnyFeedMaxCtas = 64;
 // One CTA streams its 128 rows at about 40 GB/s, so a 128-block (K = 8192)

@@ -474,7 +474,9 @@ cudaError_t launch_skinny(const SkinnyArgs *probs, int nprob, int num_sms, cudaS
   }
   const bool feed_layout =
       feeds && total_mt <= kSkinnyFeedMaxCtas && max_kb <= kSkinnyFeedMaxKb;
-  const int S = feed_layout ? 1 : skinny_split_launch(total_mt, max_kb, num_sms);
+  int S = feed_layout ? 1 : skinny_split_launch(total_mt, max_kb, num_sms);
+  for (int i = 0; i < P.nprob; ++i)
+    while (use[i]->max_split > 0 && S > use[i]->max_split) S /= 2;
   P.S = S;
   P.alone = feed_layout && deep ? 1 : 0;
   size_t smem = 0;
