@@ -49,10 +49,13 @@
 //          Per SM a K block then moves A 16 KB + B 32 KB for 1024 MMA cycles
 //          (48 B/clock) instead of 32 KB for 512 (64 B/clock, above the
 //          ~58 B/clock the TMA feed sustains).  Eight epilogue warps drain
-//          half 0 first, so the next tile's half-0 MMAs start while half 1
-//          is still being written out.  A split wide tile's partial holds
-//          both halves (256 x 512 fp32 per pair), and its fix-up brings the
-//          other range's in one half at a time through the stage ring.
+//          half 0 first; a half is released to the MMAs as soon as it has
+//          been read into registers (plain and fp8 tiles), and the next
+//          tile's half-0 MMAs go ahead while half 1 is still being read,
+//          so the next tile runs under this one's stores.  A split wide
+//          tile's partial holds both halves (256 x 512 fp32 per pair), and
+//          its fix-up brings the other range's in one half at a time
+//          through the stage ring.
 #include <cuda_bf16.h>
 
 #include <atomic>
