@@ -1283,7 +1283,10 @@ int main_gemm_pick_bn(int, int, int) { return 256; }
 // Time of one 256 x 512 tile in units of one 256 x 256 tile.  The narrow
 // tile is bound by the TMA feed (~684 cycles per 64-wide K block against
 // 512 of MMA); the wide one by its MMAs (1024 cycles per K block) plus the
-// drain of the half the next tile waits for.
+// drain of the half the next tile waited for when this was measured.  The
+// next tile now starts on a half as soon as it has been read out, so the
+// figure errs towards narrow tiles; every benchmark shape picks the wide
+// ones all the same.
 constexpr double kWideTileCost = 1.6;
 // A split tile's fix-up (its partial out, the other in, the combine and the
 // drain), in microseconds, against a K block's time in the tile: 8 us
